@@ -1,0 +1,224 @@
+/*
+ * csa.h -- C ABI of the hybrid compressed attention library (libcsa.so, CUDA sm_103a).
+ *
+ * The library computes the attention layer of DeepSeek-V4's hybrid compressed attention:
+ * Compressed Sparse Attention (CSA) and Heavily Compressed Attention (HCA).
+ *
+ * Sources (prose only; the pages print no formula):
+ *  [P2] "DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence"
+ *       (wiki notes): 提案手法 §1 "ハイブリッドアテンション (CSA + HCA)";
+ *       訓練インフラの革新 §5 "推論フレームワーク" (state cache + compressed KV cache,
+ *       KV entries with BF16 RoPE dims and FP8 other dims).
+ *  [P4] "EP 95 DeepSeek-V4論文を読む" (podcast), segment 17:10 (indexer and top-k).
+ *  [P5] "deepseek V4 技术论文", 一.1 "混合注意力机制：CSA + HCA".
+ *
+ * Conventions for every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *    contiguous, 16-byte aligned. The library allocates nothing: scratch memory comes from
+ *    the caller's workspace, sized by csa_workspace_bytes().
+ *  - Every call is asynchronous on `stream` and returns a csa_status. Shapes, dtypes, null
+ *    pointers, alignment and the workspace size are checked on the host before anything is
+ *    launched; a failed check returns CSA_ERR_INVALID / CSA_ERR_WORKSPACE / CSA_ERR_UNSUPPORTED
+ *    and launches nothing. No C++ exception crosses the ABI.
+ *  - Device-side conditions (an index out of range that was skipped, a bounded wait that gave
+ *    up) are recorded in a device status word, read with csa_device_status().
+ *  - Fixed sizes: head dim d = 128, indexer dim d_I = 64, d_rope in {0, 64}.
+ *  - Positions: in prefill, the query of row t of a sequence has position t. In decode, the
+ *    caller has already appended the new token: ctx_len[b] counts it and its position is
+ *    p = ctx_len[b] - 1.
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *csa_stream_t; /* a cudaStream_t; NULL = the legacy default stream */
+
+/* Element types. */
+typedef enum {
+    CSA_F32 = 0,     /* float32 */
+    CSA_BF16 = 1,    /* bfloat16 */
+    CSA_FP8E4M3 = 2, /* FP8 E4M3 ("fn": no infinities, max 448), with a float scale per row */
+    CSA_MIXED = 3    /* compressed entry: dims [0, d-d_rope) FP8 E4M3 + row scale, RoPE dims BF16 */
+} csa_dtype;
+
+typedef enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID = 1,     /* bad shape, dtype, null pointer or misaligned pointer */
+    CSA_ERR_WORKSPACE = 2,   /* workspace smaller than csa_workspace_bytes() */
+    CSA_ERR_UNSUPPORTED = 3, /* well-formed but not provided (e.g. d != 128) */
+    CSA_ERR_LAUNCH = 4,      /* a kernel launch failed */
+    CSA_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up (kernel returned early) */
+    CSA_ERR_BOUNDS = 6,      /* device: an out-of-range index was skipped */
+    CSA_ERR_CUDA = 7         /* another CUDA runtime error */
+} csa_status;
+
+/* Layer description shared by all calls. */
+typedef struct {
+    int B;          /* sequences */
+    int L;          /* prefill: tokens per sequence; decode: cache capacity in raw tokens */
+    int H;          /* query heads (all share one KV head) */
+    int d;          /* head dim; must be 128 */
+    int d_rope;     /* RoPE dims, the last d_rope of d: 64, or 0 for no RoPE */
+    int m;          /* compression ratio of this layer: m = 4 (CSA) or m' = 128 (HCA) */
+    int topk;       /* CSA: entries selected per query (0 disables the compressed branch) */
+    int n_win;      /* sliding-window length (128) */
+    int H_I;        /* CSA indexer heads */
+    int d_I;        /* CSA indexer dim; must be 64 */
+    float scale;    /* softmax scale of the logits (1/sqrt(d)) */
+    int act_t;      /* csa_dtype of q, raw kv, kv_rope, the SWA ring and the output: F32 | BF16 */
+    int kv_t;       /* csa_dtype of compressed entries: F32 | BF16 | MIXED */
+    int idx_t;      /* csa_dtype of the indexer operands: F32 | FP8E4M3 */
+    int rope_len;   /* rows of the RoPE table (positions 0 .. rope_len-1) */
+} csa_params;
+
+/* Compressed entries of B sequences, N_cap = ceil(L / m) rows per sequence.
+ *  F32 / BF16: data = [B, N_cap, d];  rope = scale = NULL.
+ *  MIXED     : data = [B, N_cap, d - d_rope] FP8 E4M3 codes, rope = [B, N_cap, d_rope] BF16,
+ *              scale = [B, N_cap] float; value = decode(code) * scale on the first dims.
+ * Entries hold RoPE already applied at the entry position (j+1)m - 1. */
+typedef struct {
+    void *data;
+    void *rope;
+    float *scale;
+} csa_entries;
+
+/* Rows of indexer operands (queries [.., H_I, d_I] or keys [.., d_I]).
+ *  F32     : data = float rows, scale = NULL.
+ *  FP8E4M3 : data = uint8 E4M3 codes, scale = one float per row of d_I values. */
+typedef struct {
+    void *data;
+    float *scale;
+} csa_index_rows;
+
+/* Operation selector for csa_workspace_bytes. */
+typedef enum {
+    CSA_OP_INDEX_TOPK = 0,
+    CSA_OP_CSA_PREFILL = 1,
+    CSA_OP_HCA_PREFILL = 2,
+    CSA_OP_CSA_DECODE = 3,
+    CSA_OP_HCA_DECODE = 4
+} csa_op;
+
+/* Human-readable text of a status code (static storage). */
+const char *csa_strerror(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int csa_version(void);
+
+/* Bytes of caller workspace the operation needs for this layer; 0 if none. (size_t)-1 when
+ * the parameters are invalid. Pure host function. */
+size_t csa_workspace_bytes(const csa_params *p, int op);
+
+/* Host-only validation of a layer description; returns CSA_OK or CSA_ERR_INVALID /
+ * CSA_ERR_UNSUPPORTED without touching the GPU. `op` as in csa_workspace_bytes. */
+int csa_check_params(const csa_params *p, int op);
+
+/* RoPE table for partial RoPE ([P2] 提案手法 §1, last bullet: RoPE on the last 64 dims).
+ * tab [rope_len, d_rope/2, 2] float receives (cos, sin) of pos * theta^(-i/(d_rope/2)),
+ * evaluated in double precision on the device and rounded to float. */
+int csa_rope_table(float *tab, int rope_len, int d_rope, float theta, csa_stream_t stream);
+
+/* Per-row FP8 E4M3 quantisation of x [rows, cols] float (the indexer's low-precision
+ * operands, [P2] 提案手法 §1 CSA): scale[r] = max|x[r,:]| / 448 (float), codes[r,c] =
+ * E4M3(x[r,c] / scale[r]) rounded to nearest even with saturation to +-448; a zero row gets
+ * scale 0 and zero codes. codes [rows, cols] uint8; scales [rows] float. */
+int csa_quant_fp8_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
+                       csa_stream_t stream);
+
+/* Overlapping compression, one layer ([P2] 提案手法 §1 CSA/HCA: one entry per m tokens by a
+ * weighted average with overlap between adjacent blocks; [P5] 一.1: C^b overlaps C^a).
+ * Entry j of a sequence = sum over t in [(j-1)m, (j+1)m) ∩ [0, L) of alpha_t * kv[t], with
+ * alpha = softmax over those tokens of z[t,0] (t in block j) or z[t,1] (t in block j-1).
+ * Then RoPE at position (j+1)m - 1, then storage per p->kv_t. The same weights compress the
+ * raw indexer keys (if kI_raw is given) into KI, stored per p->idx_t (FP8: one scale per
+ * entry). Optionally writes kv_rope: the raw rows with RoPE at their own positions (the
+ * sliding-window keys), in p->act_t.
+ *   kv [B, L, d] act_t;  z [B, L, 2] float;  kI_raw [B, L, d_I] float or NULL;
+ *   rope_tab: csa_rope_table with rope_len >= ceil(L/m) * m;
+ *   C: entries [B, ceil(L/m), ...];  KI: [B, ceil(L/m), d_I] (ignored if kI_raw is NULL);
+ *   kv_rope [B, L, d] act_t or NULL. */
+int kv_compress(const csa_params *p, const void *kv, const float *z, const float *kI_raw,
+                const float *rope_tab, const csa_entries *C, const csa_index_rows *KI,
+                void *kv_rope, csa_stream_t stream);
+
+/* Lightning-indexer score and top-k selection for prefill rows ([P2] 提案手法 §1 CSA;
+ * [P5] 一.1: each query attends only to its top-k compressed entries; [P4] 17:10).
+ * s(t, j) = sum_h w[t,h] * ReLU(qI[t,h] . KI[j]) over the entries visible to t
+ * ((j+1)m - 1 <= t). F32: fixed order -- acc = fma(q_c, k_c, acc) over c from +0,
+ * r = acc > 0 ? acc : 0, s = fma(w_h, r, s) over h from +0 -- so the selection is exactly
+ * reproducible. FP8: E4M3 operands with row scales, products accumulated in float.
+ * Selection: the k highest scores, ties to the lower index; written in ascending index
+ * order, padded with -1 when fewer than k entries are visible.
+ *   qI rows [B, L, H_I, d_I] (FP8 scale [B, L, H_I]); KI rows [B, N, d_I] (scale [B, N]);
+ *   w [B, L, H_I] float; topk_out [B, L, topk] int32. */
+int csa_index_topk(const csa_params *p, const csa_index_rows *qI, const csa_index_rows *KI,
+                   const float *w, int32_t *topk_out, void *ws, size_t ws_bytes,
+                   csa_stream_t stream);
+
+/* CSA prefill ([P2] 提案手法 §1 CSA + sliding window + sink + partial RoPE; [P5] 一.1).
+ * Per query row t and head h: one softmax over (a) the top-k entries of t (indexer as in
+ * csa_index_topk), (b) the raw rows u in [max(0, t - n_win + 1), t] (kv_rope), and (c) the
+ * sink logit sink[h] (denominator only). Logits = scale * RoPE(q[t,h], t) . key; a key is
+ * also its value. The output is the weighted sum with dims [d-d_rope, d) rotated back by
+ * the inverse RoPE at t.
+ *   q [B, L, H, d] act_t (before RoPE); kv_rope [B, L, d] act_t; C entries [B, N, ...];
+ *   qI, KI, w as in csa_index_topk; sink [H] float or NULL (no sink);
+ *   topk_out [B, L, topk] int32 or NULL; out [B, L, H, d] act_t;
+ *   lse_out [B, L, H] float or NULL: natural log of the sum of exp(logit) over keys
+ *   (sink excluded), so the weights of a head sum to exp(lse) / (exp(lse) + exp(sink)). */
+int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const csa_entries *C,
+                const csa_index_rows *qI, const csa_index_rows *KI, const float *w,
+                const float *sink, const float *rope_tab, int32_t *topk_out, void *out,
+                float *lse_out, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/* The attention stage of csa_prefill with the selection given by the caller: topk_idx
+ * [B, L, topk] int32 as written by csa_index_topk (ascending, -1 padded). Everything else as
+ * in csa_prefill. Uses no workspace. */
+int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope,
+                         const csa_entries *C, const int32_t *topk_idx, const float *sink,
+                         const float *rope_tab, void *out, float *lse_out, csa_stream_t stream);
+
+/* HCA prefill ([P2] 提案手法 §1 HCA: m' = 128, no sparse selection, dense attention over the
+ * compressed entries; plus sliding window and sink as for CSA). Key set of row t: every
+ * entry visible to t, then the raw rows of the window. Arguments as in csa_prefill. */
+int hca_prefill(const csa_params *p, const void *q, const void *kv_rope, const csa_entries *C,
+                const float *sink, const float *rope_tab, void *out, float *lse_out, void *ws,
+                size_t ws_bytes, csa_stream_t stream);
+
+/* CSA decode step, one new query per sequence against the caches ([P2] 訓練インフラの革新
+ * §5: state cache of recent raw tokens + compressed KV cache).
+ *   q [B, H, d] act_t (before RoPE); ctx_len [B] int32 (device), 1 <= ctx_len[b] <= L;
+ *   C: entry cache [B, ceil(L/m), ...] (entries j < ctx_len/m are read);
+ *   qI rows [B, H_I, d_I] (+scale [B, H_I]); KI cache rows [B, ceil(L/m), d_I] (+scale);
+ *   w [B, H_I]; swa_ring [B, n_win, d] act_t: the raw row of position u, after RoPE at u,
+ *   at slot u mod n_win, for u in [max(0, p - n_win + 1), p];
+ *   topk_out [B, topk] or NULL; out [B, H, d]; lse_out [B, H] or NULL. */
+int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
+               const csa_index_rows *qI, const csa_index_rows *KI, const float *w,
+               const void *swa_ring, const float *sink, const float *rope_tab,
+               int32_t *topk_out, void *out, float *lse_out, void *ws, size_t ws_bytes,
+               csa_stream_t stream);
+
+/* HCA decode step: every visible cached entry plus the window, arguments as csa_decode. */
+int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
+               const void *swa_ring, const float *sink, const float *rope_tab, void *out,
+               float *lse_out, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/* Number of kernels this library has launched in the process so far (host counter). */
+uint64_t csa_launch_count(void);
+
+/* Synchronises the device, returns the device status word (CSA_OK or the first device-side
+ * code recorded since the last reset) in *status, and clears it when reset != 0. */
+int csa_device_status(int *status, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H */

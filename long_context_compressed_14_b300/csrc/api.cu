@@ -1,0 +1,371 @@
+// api.cu -- the C ABI of libcsa.so: host-side validation, workspace carving and launches.
+// Declarations and argument contracts are in include/csa.h.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace csa {
+__device__ int g_status = 0;
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+uint64_t launch_counter() { return g_launches.load(std::memory_order_relaxed); }
+}
+
+using namespace csa;
+
+namespace {
+
+constexpr size_t kScoreBudget = (size_t)1 << 31;  // bytes of indexer scores per chunk
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+inline int64_t ncap_of(const csa_params *p) { return ceil_div64(p->L, p->m); }
+
+// Stride of a score row in floats (kept a multiple of 4 so rows stay 16-byte aligned).
+inline int64_t score_ld(const csa_params *p) { return (ncap_of(p) + 3) / 4 * 4; }
+
+// Prefill rows whose scores share one workspace chunk.
+inline int64_t score_chunk_rows(const csa_params *p) {
+    int64_t rows = (int64_t)(kScoreBudget / (sizeof(float) * (size_t)score_ld(p)));
+    if (rows >= p->L) return p->L;
+    rows = rows / 32 * 32;
+    return rows < 32 ? 32 : rows;
+}
+
+bool is_csa(int op) {
+    return op == CSA_OP_INDEX_TOPK || op == CSA_OP_CSA_PREFILL || op == CSA_OP_CSA_DECODE;
+}
+bool is_decode(int op) { return op == CSA_OP_CSA_DECODE || op == CSA_OP_HCA_DECODE; }
+
+int check(const csa_params *p, int op) {
+    if (!p) return CSA_ERR_INVALID;
+    if (op < CSA_OP_INDEX_TOPK || op > CSA_OP_HCA_DECODE) return CSA_ERR_INVALID;
+    if (p->B < 1 || p->L < 1 || p->H < 1 || p->m < 1 || p->n_win < 1) return CSA_ERR_INVALID;
+    if (!(p->scale > 0.0f) || !isfinite(p->scale)) return CSA_ERR_INVALID;
+    if (p->d != kD) return CSA_ERR_UNSUPPORTED;
+    if (p->d_rope != 0 && p->d_rope != 64) return CSA_ERR_UNSUPPORTED;
+    if (p->H > 64) return CSA_ERR_UNSUPPORTED;
+    if (p->m > 1024) return CSA_ERR_UNSUPPORTED;
+    if (p->act_t != CSA_F32 && p->act_t != CSA_BF16) return CSA_ERR_INVALID;
+    if (p->kv_t != CSA_F32 && p->kv_t != CSA_BF16 && p->kv_t != CSA_MIXED) return CSA_ERR_INVALID;
+    if (p->kv_t == CSA_MIXED && p->d_rope != 64) return CSA_ERR_INVALID;
+    if ((int64_t)p->B * p->L > ((int64_t)1 << 40)) return CSA_ERR_UNSUPPORTED;
+    if (p->d_rope > 0) {
+        // positions used: raw rows < L, entries at (j+1)m-1 < ceil(L/m)*m
+        const int64_t need = ncap_of(p) * p->m;
+        if (p->rope_len < need || p->rope_len < p->L) return CSA_ERR_INVALID;
+    }
+    if (is_csa(op)) {
+        if (p->topk < 0 || p->topk > kMaxTopk) return CSA_ERR_UNSUPPORTED;
+        if (op == CSA_OP_INDEX_TOPK && p->topk < 1) return CSA_ERR_INVALID;
+        if (p->topk > 0) {
+            if (p->d_I != kDI) return CSA_ERR_UNSUPPORTED;
+            if (p->H_I < 1 || p->H_I > 16) return CSA_ERR_UNSUPPORTED;
+            if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3) return CSA_ERR_INVALID;
+        }
+    }
+    return CSA_OK;
+}
+
+size_t ws_bytes(const csa_params *p, int op) {
+    switch (op) {
+    case CSA_OP_INDEX_TOPK:
+        return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
+    case CSA_OP_CSA_PREFILL:
+        if (p->topk == 0) return 0;
+        return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p)) +
+               align_up(sizeof(int32_t) * (size_t)p->B * p->L * p->topk);
+    case CSA_OP_CSA_DECODE:
+        if (p->topk == 0) return 0;
+        return align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) +
+               align_up(sizeof(int32_t) * (size_t)p->B * p->topk);
+    default:
+        return 0;
+    }
+}
+
+int launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? CSA_OK : CSA_ERR_LAUNCH;
+}
+
+inline cudaStream_t cs(csa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool entries_ok(const csa_params *p, const csa_entries *C) {
+    if (!C || !C->data || !aligned16(C->data)) return false;
+    if (p->kv_t == CSA_MIXED) return C->rope && C->scale && aligned16(C->rope) && aligned16(C->scale);
+    return true;
+}
+
+bool index_rows_ok(const csa_params *p, const csa_index_rows *r) {
+    if (!r || !r->data || !aligned16(r->data)) return false;
+    if (p->idx_t == CSA_FP8E4M3) return r->scale && aligned16(r->scale);
+    return true;
+}
+
+// indexer + top-k over all prefill rows, chunked through the score workspace
+int run_index_topk(const csa_params *p, const csa_index_rows *qI, const csa_index_rows *KI,
+                   const float *w, int32_t *idx_out, float *S, cudaStream_t st) {
+    const int64_t chunk = score_chunk_rows(p);
+    const int ncap = (int)ncap_of(p);
+    for (int b = 0; b < p->B; ++b) {
+        for (int64_t t0 = 0; t0 < p->L; t0 += chunk) {
+            const int nrows = (int)((p->L - t0) < chunk ? (p->L - t0) : chunk);
+            IndexArgs ia{};
+            ia.qI = qI->data;
+            ia.qI_scale = qI->scale;
+            ia.KI = KI->data;
+            ia.KI_scale = KI->scale;
+            ia.w = w;
+            ia.S = S;
+            ia.ldS = score_ld(p);
+            ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap;
+            ia.idx_t = p->idx_t;
+            ia.b = b; ia.t0 = (int)t0; ia.nrows = nrows;
+            launch_indexer(ia, st);
+            TopkArgs ta{};
+            ta.S = S;
+            ta.ldS = score_ld(p);
+            ta.out = idx_out;
+            ta.L = p->L; ta.m = p->m; ta.ncap = ncap; ta.k = p->topk;
+            ta.b = b; ta.t0 = (int)t0; ta.nrows = nrows;
+            launch_topk(ta, st);
+        }
+    }
+    return launch_status();
+}
+
+AttnArgs attn_args(const csa_params *p, const void *q, const void *kvr, const csa_entries *C,
+                   const int32_t *idx, const int32_t *ctx, const float *sink, const float *rope,
+                   void *out, float *lse, int decode, int topk) {
+    AttnArgs a{};
+    a.q = q;
+    a.kv_rope = kvr;
+    a.c_data = C ? C->data : nullptr;
+    a.c_rope = C ? C->rope : nullptr;
+    a.c_scale = C ? C->scale : nullptr;
+    a.idx = idx;
+    a.ctx = ctx;
+    a.sink = sink;
+    a.rope_tab = rope;
+    a.out = out;
+    a.lse = lse;
+    a.B = p->B; a.L = p->L; a.H = p->H; a.m = p->m; a.topk = topk; a.n_win = p->n_win;
+    a.d_rope = p->d_rope; a.ncap = (int)ncap_of(p); a.scale = p->scale;
+    a.decode = decode; a.act_t = p->act_t; a.kv_t = p->kv_t;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *csa_strerror(int s) {
+    switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID: return "invalid argument (shape, dtype, null or misaligned pointer)";
+    case CSA_ERR_WORKSPACE: return "workspace too small";
+    case CSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CSA_ERR_LAUNCH: return "kernel launch failed";
+    case CSA_ERR_TIMEOUT: return "device wait timed out";
+    case CSA_ERR_BOUNDS: return "device index out of range (skipped)";
+    case CSA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+    }
+}
+
+int csa_version(void) { return 100; }
+
+int csa_check_params(const csa_params *p, int op) { return check(p, op); }
+
+size_t csa_workspace_bytes(const csa_params *p, int op) {
+    if (check(p, op) != CSA_OK) return (size_t)-1;
+    return ws_bytes(p, op);
+}
+
+int csa_rope_table(float *tab, int rope_len, int d_rope, float theta, csa_stream_t stream) {
+    if (!tab || !aligned16(tab) || rope_len < 1 || (d_rope != 64 && d_rope != 0) || !(theta > 1.0f))
+        return CSA_ERR_INVALID;
+    if (d_rope == 0) return CSA_OK;
+    launch_rope_table(tab, rope_len, d_rope, theta, cs(stream));
+    return launch_status();
+}
+
+int csa_quant_fp8_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
+                       csa_stream_t stream) {
+    if (!x || !codes || !scales || rows < 0 || cols < 1) return CSA_ERR_INVALID;
+    if (rows == 0) return CSA_OK;
+    launch_quant_rows(x, rows, cols, codes, scales, cs(stream));
+    return launch_status();
+}
+
+int kv_compress(const csa_params *p, const void *kv, const float *z, const float *kI_raw,
+                const float *rope_tab, const csa_entries *C, const csa_index_rows *KI,
+                void *kv_rope, csa_stream_t stream) {
+    int s = check(p, CSA_OP_HCA_PREFILL);
+    if (s) return s;
+    if (!kv || !z || !aligned16(kv) || !entries_ok(p, C)) return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    if (kI_raw) {
+        if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3) return CSA_ERR_INVALID;
+        if (!index_rows_ok(p, KI) || p->d_I != kDI) return CSA_ERR_INVALID;
+    }
+    if (kv_rope && !aligned16(kv_rope)) return CSA_ERR_INVALID;
+    CompressArgs a{};
+    a.kv = kv; a.z = z; a.kI_raw = kI_raw; a.rope_tab = rope_tab;
+    a.c_data = C->data; a.c_rope = C->rope; a.c_scale = C->scale;
+    a.ki_data = kI_raw ? KI->data : nullptr;
+    a.ki_scale = kI_raw ? KI->scale : nullptr;
+    a.kv_rope = kv_rope;
+    a.B = p->B; a.L = p->L; a.m = p->m; a.N = (int)ncap_of(p); a.d_rope = p->d_rope;
+    a.act_t = p->act_t; a.kv_t = p->kv_t; a.idx_t = p->idx_t;
+    launch_kv_compress(a, cs(stream));
+    return launch_status();
+}
+
+int csa_index_topk(const csa_params *p, const csa_index_rows *qI, const csa_index_rows *KI,
+                   const float *w, int32_t *topk_out, void *ws, size_t wsb, csa_stream_t stream) {
+    int s = check(p, CSA_OP_INDEX_TOPK);
+    if (s) return s;
+    if (!index_rows_ok(p, qI) || !index_rows_ok(p, KI) || !w || !topk_out) return CSA_ERR_INVALID;
+    if (wsb < ws_bytes(p, CSA_OP_INDEX_TOPK) || !ws || !aligned16(ws)) return CSA_ERR_WORKSPACE;
+    return run_index_topk(p, qI, KI, w, topk_out, reinterpret_cast<float *>(ws), cs(stream));
+}
+
+int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const csa_entries *C,
+                const csa_index_rows *qI, const csa_index_rows *KI, const float *w,
+                const float *sink, const float *rope_tab, int32_t *topk_out, void *out,
+                float *lse_out, void *ws, size_t wsb, csa_stream_t stream) {
+    int s = check(p, CSA_OP_CSA_PREFILL);
+    if (s) return s;
+    if (!q || !kv_rope || !out || !aligned16(q) || !aligned16(kv_rope) || !aligned16(out))
+        return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    if (p->topk > 0) {
+        if (!entries_ok(p, C) || !index_rows_ok(p, qI) || !index_rows_ok(p, KI) || !w) return CSA_ERR_INVALID;
+        if (wsb < ws_bytes(p, CSA_OP_CSA_PREFILL) || !ws || !aligned16(ws)) return CSA_ERR_WORKSPACE;
+    }
+    cudaStream_t st = cs(stream);
+    int32_t *idx = nullptr;
+    if (p->topk > 0) {
+        float *S = reinterpret_cast<float *>(ws);
+        const size_t sbytes = align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
+        idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
+        s = run_index_topk(p, qI, KI, w, idx, S, st);
+        if (s) return s;
+    }
+    AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, idx, nullptr, sink, rope_tab, out,
+                           lse_out, 0, p->topk);
+    if (p->topk == 0) a.ncap = 0;
+    launch_attn_simple(a, st);
+    return launch_status();
+}
+
+int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope,
+                         const csa_entries *C, const int32_t *topk_idx, const float *sink,
+                         const float *rope_tab, void *out, float *lse_out, csa_stream_t stream) {
+    int s = check(p, CSA_OP_CSA_PREFILL);
+    if (s) return s;
+    if (!q || !kv_rope || !out || !aligned16(q) || !aligned16(kv_rope) || !aligned16(out)) return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    if (p->topk > 0 && (!entries_ok(p, C) || !topk_idx)) return CSA_ERR_INVALID;
+    AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, p->topk > 0 ? topk_idx : nullptr, nullptr, sink,
+                           rope_tab, out, lse_out, 0, p->topk);
+    if (p->topk == 0) a.ncap = 0;
+    launch_attn_simple(a, cs(stream));
+    return launch_status();
+}
+
+int hca_prefill(const csa_params *p, const void *q, const void *kv_rope, const csa_entries *C,
+                const float *sink, const float *rope_tab, void *out, float *lse_out, void *ws,
+                size_t wsb, csa_stream_t stream) {
+    (void)ws;
+    (void)wsb;
+    int s = check(p, CSA_OP_HCA_PREFILL);
+    if (s) return s;
+    if (!q || !kv_rope || !out || !aligned16(q) || !aligned16(kv_rope) || !aligned16(out) ||
+        !entries_ok(p, C))
+        return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    AttnArgs a = attn_args(p, q, kv_rope, C, nullptr, nullptr, sink, rope_tab, out, lse_out, 0, 0);
+    launch_attn_simple(a, cs(stream));
+    return launch_status();
+}
+
+int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
+               const csa_index_rows *qI, const csa_index_rows *KI, const float *w,
+               const void *swa_ring, const float *sink, const float *rope_tab, int32_t *topk_out,
+               void *out, float *lse_out, void *ws, size_t wsb, csa_stream_t stream) {
+    int s = check(p, CSA_OP_CSA_DECODE);
+    if (s) return s;
+    if (!q || !ctx_len || !swa_ring || !out || !aligned16(q) || !aligned16(swa_ring) || !aligned16(out))
+        return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    if (p->topk > 0) {
+        if (!entries_ok(p, C) || !index_rows_ok(p, qI) || !index_rows_ok(p, KI) || !w) return CSA_ERR_INVALID;
+        if (wsb < ws_bytes(p, CSA_OP_CSA_DECODE) || !ws || !aligned16(ws)) return CSA_ERR_WORKSPACE;
+    }
+    cudaStream_t st = cs(stream);
+    int32_t *idx = nullptr;
+    const int ncap = (int)ncap_of(p);
+    if (p->topk > 0) {
+        float *S = reinterpret_cast<float *>(ws);
+        const size_t sbytes = align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p));
+        idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
+        IndexArgs ia{};
+        ia.qI = qI->data; ia.qI_scale = qI->scale; ia.KI = KI->data; ia.KI_scale = KI->scale;
+        ia.w = w; ia.ctx = ctx_len; ia.S = S; ia.ldS = score_ld(p);
+        ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap; ia.idx_t = p->idx_t;
+        ia.decode = 1;
+        launch_indexer(ia, st);
+        TopkArgs ta{};
+        ta.S = S; ta.ldS = score_ld(p); ta.ctx = ctx_len; ta.out = idx;
+        ta.L = p->L; ta.m = p->m; ta.ncap = ncap; ta.k = p->topk; ta.nrows = p->B; ta.decode = 1;
+        launch_topk(ta, st);
+    }
+    AttnArgs a = attn_args(p, q, swa_ring, p->topk > 0 ? C : nullptr, idx, ctx_len, sink, rope_tab, out,
+                           lse_out, 1, p->topk);
+    if (p->topk == 0) a.ncap = 0;
+    launch_attn_simple(a, st);
+    return launch_status();
+}
+
+int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
+               const void *swa_ring, const float *sink, const float *rope_tab, void *out,
+               float *lse_out, void *ws, size_t wsb, csa_stream_t stream) {
+    (void)ws;
+    (void)wsb;
+    int s = check(p, CSA_OP_HCA_DECODE);
+    if (s) return s;
+    if (!q || !ctx_len || !swa_ring || !out || !aligned16(q) || !aligned16(swa_ring) || !aligned16(out) ||
+        !entries_ok(p, C))
+        return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    AttnArgs a = attn_args(p, q, swa_ring, C, nullptr, ctx_len, sink, rope_tab, out, lse_out, 1, 0);
+    launch_attn_simple(a, cs(stream));
+    return launch_status();
+}
+
+uint64_t csa_launch_count(void) { return launch_counter(); }
+
+int csa_device_status(int *status, int reset) {
+    if (!status) return CSA_ERR_INVALID;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CSA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
+    *status = v;
+    if (reset) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
+    }
+    return CSA_OK;
+}
+
+}  // extern "C"

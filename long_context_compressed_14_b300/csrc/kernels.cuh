@@ -1,0 +1,78 @@
+// kernels.cuh -- launch interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa {
+
+struct CompressArgs {
+    const void *kv;
+    const float *z;
+    const float *kI_raw;
+    const float *rope_tab;
+    void *c_data;
+    void *c_rope;
+    float *c_scale;
+    void *ki_data;
+    float *ki_scale;
+    void *kv_rope;
+    int B, L, m, N, d_rope, act_t, kv_t, idx_t;
+};
+
+// Indexer scores of a block of query rows of ONE sequence (prefill) or of one query per
+// sequence (decode) into S[r][j], r = local row, j < visible(row).
+struct IndexArgs {
+    const void *qI;        // rows [.., H_I, d_I] (F32 float or FP8 codes)
+    const float *qI_scale; // FP8: [.., H_I]
+    const void *KI;        // [B, ncap, d_I]
+    const float *KI_scale; // FP8: [B, ncap]
+    const float *w;        // [.., H_I]
+    const int32_t *ctx;    // decode: [B]
+    float *S;              // [rows, ldS]
+    int64_t ldS;
+    int B, L, H_I, m, ncap, idx_t;
+    int b, t0, nrows;      // prefill: sequence and row range of this launch
+    int decode;
+};
+
+struct TopkArgs {
+    const float *S;
+    int64_t ldS;
+    const int32_t *ctx;    // decode positions (ctx-1) or NULL for prefill
+    int32_t *out;          // prefill: out + ((b*L)+t)*k; decode: out + b*k
+    int L, m, ncap, k;
+    int b, t0, nrows;
+    int decode;
+};
+
+struct AttnArgs {
+    const void *q;         // prefill [B, L, H, d]; decode [B, H, d]
+    const void *kv_rope;   // prefill [B, L, d]; decode ring [B, n_win, d]
+    const void *c_data;    // entries
+    const void *c_rope;
+    const float *c_scale;
+    const int32_t *idx;    // CSA: [B, L, k] / [B, k]; HCA: NULL
+    const int32_t *ctx;    // decode: [B]
+    const float *sink;     // [H] or NULL
+    const float *rope_tab; // [rope_len, half, 2]
+    void *out;
+    float *lse;
+    int B, L, H, m, topk, n_win, d_rope, ncap;
+    float scale;
+    int decode, act_t, kv_t;
+};
+
+// host-side count of kernel launches (every launch_* adds the kernels it launched)
+void count_launches(int n);
+uint64_t launch_counter();
+
+void launch_rope_table(float *tab, int rope_len, int d_rope, float theta, cudaStream_t st);
+void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
+                       cudaStream_t st);
+void launch_kv_compress(const CompressArgs &a, cudaStream_t st);
+void launch_indexer(const IndexArgs &a, cudaStream_t st);
+void launch_topk(const TopkArgs &a, cudaStream_t st);
+void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
+
+}  // namespace csa

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for hybrid compressed attention.
+"""Seeded synthetic inputs for hybrid compressed attention (a module of its own).
 
 This module only draws random numbers and names shapes; it holds none of the method's
 arithmetic. Both the CUDA library's tests/benchmark and the CPU oracle take their inputs

@@ -1,0 +1,73 @@
+"""Shared helpers of the parity tests: run the oracle on synth inputs, compare results."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+
+def np64(t: torch.Tensor) -> np.ndarray:
+    """Exact float64 copy of a float32/bfloat16 tensor."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def np32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def oracle_prefill(wl, inp: dict, b: int, rows, csa: bool, q_rows=None):
+    """Oracle result of one prefill layer for rows of sequence b (CPU torch inputs)."""
+    m = wl.m if csa else wl.m_hca
+    rows = np.asarray(rows, np.int64)
+    comp = oracle.kv_compress(np64(inp["kv"][b]), np64(inp["z"][b]),
+                              np64(inp["kI_raw"][b]) if csa and wl.topk > 0 else None, m, wl.d_rope, wl.theta,
+                              c_store=wl.c_t, idx_store=wl.idx_t if csa else "f64", q_store=wl.q_t)
+    qr = np64(inp["q"][b][rows]) if q_rows is None else q_rows
+    kw = dict(d_rope=wl.d_rope, theta=wl.theta, n_win=wl.n_win, scale=wl.scale)
+    sink = np64(inp["sink"]) if inp.get("sink") is not None else None
+    if csa:
+        if wl.topk > 0:
+            res = oracle.csa_rows(qr, comp["kv_rope"], comp["C"], np32(inp["qI"][b][rows]), comp["KI"],
+                                  np32(inp["w"][b][rows]), sink, rows, m=m, k=wl.topk, idx_store=wl.idx_t, **kw)
+        else:
+            res = oracle.csa_rows(qr, comp["kv_rope"], comp["C"], None, None, None, sink, rows, m=m, k=0,
+                                  idx_store=wl.idx_t, **kw)
+    else:
+        res = oracle.hca_rows(qr, comp["kv_rope"], comp["C"], sink, rows, m=m, **kw)
+    res["comp"] = comp
+    return res
+
+
+def check_topk_by_score(gpu_idx, scores, pos, m, k, rel_eps=1e-3):
+    """Selections that differ only by near-ties are both correct. Checks that every
+    GPU-selected index is visible and has an oracle score >= (oracle k-th score - eps), with
+    eps = rel_eps * max |score| of the row, that the GPU set has the right size, and returns
+    the fraction of rows whose sets agree exactly."""
+    gpu_idx = np.asarray(gpu_idx)
+    same = 0
+    for r in range(gpu_idx.shape[0]):
+        t = int(pos[r])
+        vis = min((t + 1) // m, scores.shape[1])
+        g = gpu_idx[r]
+        kept = g[g >= 0]
+        assert len(kept) == min(k, vis), (r, len(kept), min(k, vis))
+        assert np.all(np.diff(kept) > 0), "kept set must be ascending"
+        assert np.all(g[len(kept):] == -1)
+        if len(kept) == 0:
+            same += 1
+            continue
+        assert kept.max() < vis
+        s = scores[r, :vis]
+        kth = np.sort(s)[::-1][min(k, vis) - 1]
+        eps = rel_eps * max(np.abs(s).max(), 1e-30)
+        assert np.all(s[kept] >= kth - eps), (r, s[kept].min(), kth)
+        order = np.lexsort((np.arange(vis), -s))[:k]
+        same += int(np.array_equal(np.sort(order), kept))
+    return same / max(gpu_idx.shape[0], 1)
