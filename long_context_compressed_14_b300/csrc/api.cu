@@ -10,6 +10,7 @@
 
 namespace csa {
 __device__ int g_status = 0;
+__device__ int g_abort = 0;
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 uint64_t launch_counter() { return g_launches.load(std::memory_order_relaxed); }
@@ -264,7 +265,7 @@ int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
     AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, idx, nullptr, sink, rope_tab, out,
                            lse_out, 0, p->topk);
     if (p->topk == 0) a.ncap = 0;
-    launch_attn_simple(a, st);
+    if (!launch_csa_tc(a, st)) launch_attn_simple(a, st);
     return launch_status();
 }
 
@@ -279,7 +280,7 @@ int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope
     AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, p->topk > 0 ? topk_idx : nullptr, nullptr, sink,
                            rope_tab, out, lse_out, 0, p->topk);
     if (p->topk == 0) a.ncap = 0;
-    launch_attn_simple(a, cs(stream));
+    if (!launch_csa_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
     return launch_status();
 }
 
@@ -295,7 +296,7 @@ int hca_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
         return CSA_ERR_INVALID;
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
     AttnArgs a = attn_args(p, q, kv_rope, C, nullptr, nullptr, sink, rope_tab, out, lse_out, 0, 0);
-    launch_attn_simple(a, cs(stream));
+    if (!launch_hca_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
     return launch_status();
 }
 
@@ -333,7 +334,7 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     AttnArgs a = attn_args(p, q, swa_ring, p->topk > 0 ? C : nullptr, idx, ctx_len, sink, rope_tab, out,
                            lse_out, 1, p->topk);
     if (p->topk == 0) a.ncap = 0;
-    launch_attn_simple(a, st);
+    if (!launch_csa_tc(a, st)) launch_attn_simple(a, st);
     return launch_status();
 }
 
@@ -364,6 +365,7 @@ int csa_device_status(int *status, int reset) {
     if (reset) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
+        if (cudaMemcpyToSymbol(g_abort, &zero, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
     }
     return CSA_OK;
 }

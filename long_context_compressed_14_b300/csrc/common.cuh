@@ -14,10 +14,17 @@ constexpr int kD = 128;      // head dim
 constexpr int kDI = 64;      // indexer dim
 constexpr int kMaxTopk = 2048;
 
-// Device status word (first error wins). Defined in api.cu.
+// Device status word (first error wins) and the abort flag raised with a timeout, which makes
+// every other bounded wait give up at once. Both defined in api.cu, cleared by
+// csa_device_status(reset).
 extern __device__ int g_status;
+extern __device__ int g_abort;
 
 __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_status, 0, code); }
+__device__ __forceinline__ void set_timeout() {
+    atomicCAS(&g_status, 0, CSA_ERR_TIMEOUT);
+    atomicExch(&g_abort, 1);
+}
 
 // ---- element loads / stores ------------------------------------------------------------
 __device__ __forceinline__ float to_f(float x) { return x; }

@@ -74,5 +74,9 @@ void launch_kv_compress(const CompressArgs &a, cudaStream_t st);
 void launch_indexer(const IndexArgs &a, cudaStream_t st);
 void launch_topk(const TopkArgs &a, cudaStream_t st);
 void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
+// tensor-core kernels: return false (launching nothing) when the configuration is outside
+// what they handle
+bool launch_hca_tc(const AttnArgs &a, cudaStream_t st);
+bool launch_csa_tc(const AttnArgs &a, cudaStream_t st);
 
 }  // namespace csa
