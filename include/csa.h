@@ -205,6 +205,28 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
                int32_t *topk_out, void *out, float *lse_out, void *ws, size_t ws_bytes,
                csa_stream_t stream);
 
+/* csa_decode for callers that cannot allocate device memory (code running under CUDA-graph
+ * capture or replay, real-time serving loops that must not touch the allocator, hosts whose
+ * device memory is owned by another framework). This entry point has no counterpart in the
+ * paper; it exists only for such callers.
+ * It computes exactly what csa_decode computes, with the same arguments minus the workspace:
+ * the scratch it needs (indexer scores and selected indices) comes from one fixed array of
+ * CSA_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads the library holds
+ * until the process exits. It allocates nothing.
+ *  - A layer whose scratch (csa_workspace_bytes(p, CSA_OP_CSA_DECODE)) exceeds the array is
+ *    refused with CSA_ERR_WORKSPACE before anything is launched; use csa_decode for it.
+ *  - The first call made on a device looks up the array's device address for that device
+ *    (cudaGetSymbolAddress, with the device current); make that first call before any stream
+ *    capture begins.
+ *  - All calls on a device share the array: calls that overlap on the GPU (unordered streams)
+ *    race on it. Nothing in it needs to start at zero. */
+#define CSA_STATIC_SCRATCH_BYTES (4u << 20)
+int csa_decode_static_scratch(const csa_params *p, const void *q, const int32_t *ctx_len,
+                              const csa_entries *C, const csa_index_rows *qI,
+                              const csa_index_rows *KI, const float *w, const void *swa_ring,
+                              const float *sink, const float *rope_tab, int32_t *topk_out,
+                              void *out, float *lse_out, csa_stream_t stream);
+
 /* HCA decode step: every visible cached entry plus the window, arguments as csa_decode. */
 int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
                const void *swa_ring, const float *sink, const float *rope_tab, void *out,

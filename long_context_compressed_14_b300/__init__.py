@@ -78,6 +78,7 @@ def _load():
             "csa_decode": (I, [PP, P, P, PE, PI, PI, P, P, P, P, P, P, P, P, Z, P]),
             "hca_decode": (I, [PP, P, P, PE, P, P, P, P, P, P, Z, P]),
             "csa_sparse_attention": (I, [PP, P, P, PE, P, P, P, P, P, P]),
+            "csa_decode_static_scratch": (I, [PP, P, P, PE, PI, PI, P, P, P, P, P, P, P, P]),
             "csa_launch_count": (ctypes.c_uint64, []),
             "csa_device_status": (I, [ctypes.POINTER(ctypes.c_int), I]),
         }
@@ -207,6 +208,19 @@ def csa_decode(p: Params, q, ctx_len, C, qI, KI, w, swa_ring, sink, rope_tab, to
                            _ptr(topk_out), _ptr(out), _ptr(lse_out), _ptr(ws),
                            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
         "csa_decode")
+
+
+STATIC_SCRATCH_BYTES = 4 << 20  # CSA_STATIC_SCRATCH_BYTES in include/csa.h
+
+
+def csa_decode_static_scratch(p: Params, q, ctx_len, C, qI, KI, w, swa_ring, sink, rope_tab, topk_out, out, lse_out,
+                              stream=None):
+    """csa_decode without a workspace argument, for callers that cannot allocate device
+    memory: the scratch lives in a fixed array inside the library (see include/csa.h)."""
+    _ok(_load().csa_decode_static_scratch(ctypes.byref(p), _ptr(q), _ptr(ctx_len), _byref(_entries(C)),
+                                          _byref(_rows(qI)), _byref(_rows(KI)), _ptr(w), _ptr(swa_ring), _ptr(sink),
+                                          _ptr(rope_tab), _ptr(topk_out), _ptr(out), _ptr(lse_out), _stream(stream)),
+        "csa_decode_static_scratch")
 
 
 def hca_decode(p: Params, q, ctx_len, C, swa_ring, sink, rope_tab, out, lse_out, ws, stream=None):
