@@ -163,6 +163,7 @@ void launch_indexer(const IndexArgs &a, cudaStream_t st) {
     }
     const int last_vis = visible_entries((int64_t)a.t0 + a.nrows - 1, a.m, a.ncap);
     if (last_vis <= 0) return;
+    if (a.idx_t == CSA_FP8E4M3 && launch_indexer_tc(a, st)) return;  // tensor-core FP8 path
     dim3 grid((unsigned)ceil_div64(last_vis, kIdxTJ), (unsigned)ceil_div64(a.nrows, kIdxTQ));
     const size_t smem = sizeof(float) * ((size_t)kIdxTQ * a.H_I * kDI + kIdxTQ * a.H_I +
                                          kIdxTJ * (kDI + 1) + kIdxTJ);

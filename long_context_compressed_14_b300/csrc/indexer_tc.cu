@@ -1,0 +1,268 @@
+// indexer_tc.cu -- FP8 lightning-indexer scores on the tensor cores (tcgen05 kind::f8f6f4).
+//
+// Sources: [P2] "DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence"
+// (wiki notes), 提案手法 §1 CSA (a lightning indexer scores every compressed entry for the
+// top-k selection, in low precision) and 事後学習 §3 (the indexer's QK path in low precision);
+// [P5] "deepseek V4 技术论文" 一.1 (low-rank, cheap indexer).
+//
+// s(t, j) = sk_j * sum_h (w[t,h] * sq[t,h]) * ReLU(qcode[t,h] . kcode_j), the FP8 form of
+// sum_h w[t,h] ReLU(qI[t,h] . KI_j) with per-row scales (positive, so they leave the ReLU).
+//
+// One MMA tile: D[128 entries][T_q tokens x H_I heads = 256] = KI_tile (128 x 64 E4M3) times
+// qI_tile^T (256 x 64 E4M3), K = 64 as two MMAs of K = 32, FP32 accumulation in TMEM. Both
+// operands are 64-byte rows, stored with the 64-byte swizzle (TMA SWIZZLE_64B, descriptor
+// layout type 4). Entries sit on the MMA's M dimension so that one epilogue thread owns one
+// entry: it reads its accumulators, applies ReLU and the per-head weight, sums the heads of
+// each token and stores the token's score -- the 128 threads of a warpgroup write 128
+// consecutive entries of one score row at a time.
+//
+// CTA (persistent): warps 0-7 epilogue (two warpgroups, one per half of the tokens), warp 8
+// lane 0 loads tiles by TMA and issues the MMAs. Query tiles are dealt round-robin; each walks
+// only the entry tiles its last token can see (causal skipping). D is double-buffered in TMEM
+// (2 x 256 columns), entry tiles flow through a 4-deep ring, query tiles through 2 buffers.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tma_host.cuh"
+#include "umma.cuh"
+
+namespace csa {
+using namespace umma;
+
+namespace idx_tc {
+constexpr int kEpi = 256;               // epilogue threads (warps 0-7)
+constexpr int kThreads = kEpi + 32;     // + warp 8
+constexpr int kJ = 128;                 // entries per tile (M)
+constexpr int kN = 256;                 // (token, head) rows per query tile (N)
+constexpr int kNK = 4;                  // entry-tile ring
+constexpr int kKBytes = kJ * 64;        // 8 KB
+constexpr int kQBytes = kN * 64;        // 16 KB
+constexpr int kQOff = 0;                // 2 query tiles
+constexpr int kKOff = 2 * kQBytes;      // kNK entry tiles
+constexpr int kSmemBytes = kKOff + kNK * kKBytes + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kBarEpi = 1;
+}  // namespace idx_tc
+
+struct IndexTcParams {
+    CUtensorMap mq;  // qI codes as [rows][64] u8, box 64 x 256, 64-byte swizzle
+    CUtensorMap mk;  // KI codes as [B*ncap][64] u8, box 64 x 128, 64-byte swizzle
+    const float *q_scale;  // [rows of (t, h)]
+    const float *k_scale;  // [B*ncap]
+    const float *w;        // [rows of (t, h)]
+    float *S;
+    int64_t ldS;
+    int L, m, ncap, b, t0, nrows;
+    int n_qt;  // query tiles in this launch
+};
+
+// Shared-memory matrix descriptor with the 64-byte swizzle (layout type 4): rows of 64 bytes,
+// 8-row atoms of 512 bytes (stride-dimension offset 512).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(512 >> 4) << 32) | (1ull << 46) |
+           (4ull << 61);
+}
+
+template <int HI>
+__global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const __grid_constant__ IndexTcParams P) {
+    using namespace idx_tc;
+    constexpr int TQ = kN / HI;  // tokens per query tile
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t b_qfull[2], b_qempty[2], b_kfull[kNK], b_kempty[kNK], b_dfull[2], b_dempty[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ float s_wq[kN];  // w * q_scale per (token, head) of the current query tile
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t s_base = smem_u32(sm);
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&b_qfull[i]), 1);
+            mbar_init(smem_u32(&b_qempty[i]), 1);
+            mbar_init(smem_u32(&b_dfull[i]), 1);
+            mbar_init(smem_u32(&b_dempty[i]), kEpi);
+        }
+        for (int i = 0; i < kNK; ++i) {
+            mbar_init(smem_u32(&b_kfull[i]), 1);
+            mbar_init(smem_u32(&b_kempty[i]), 1);
+        }
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int last_row = P.t0 + P.nrows - 1;
+    auto n_et_of = [&](int qt) {
+        const int tq0 = P.t0 + qt * TQ;
+        const int tq_last = min(tq0 + TQ - 1, last_row);
+        return (visible_entries(tq_last, P.m, P.ncap) + kJ - 1) / kJ;
+    };
+    bool ok = true;
+
+    if (warp == 8) {
+        if (lane == 0) {
+            // ---- producer + MMA issue (one thread) ----
+            // Two cursors walk the same item sequence (query tiles of this CTA, each with its
+            // visible entry tiles): the load cursor runs up to kNK items ahead of the MMA
+            // cursor. It never blocks on a query buffer whose release needs an MMA that has not
+            // been issued yet; it only blocks when nothing else can make progress.
+            const uint32_t idesc = idesc_e4m3(128, kN);
+            int lq = blockIdx.x, le = 0, lqn = 0, ln = 0;  // load cursor (qn counts non-empty tiles)
+            int mq = blockIdx.x, me = 0, mqn = 0, mn = 0;  // MMA cursor
+            while (lq < P.n_qt && n_et_of(lq) == 0) lq += gridDim.x;
+            while (mq < P.n_qt && n_et_of(mq) == 0) mq += gridDim.x;
+            while (mq < P.n_qt && ok) {
+                while (lq < P.n_qt && ln - mn < kNK) {
+                    const int net = n_et_of(lq);
+                    if (le == 0) {
+                        const int qb = lqn & 1;
+                        if (lqn >= 2) {
+                            const uint32_t par = ((lqn >> 1) - 1) & 1;
+                            if (ln == mn) {
+                                if (!mbar_wait(smem_u32(&b_qempty[qb]), par, kMaxPolls, &g_abort)) { ok = false; break; }
+                            } else if (!mbar_try_wait(smem_u32(&b_qempty[qb]), par)) {
+                                break;  // do MMA work first
+                            }
+                        }
+                        mbar_expect_tx(smem_u32(&b_qfull[qb]), kQBytes);
+                        tma_load_3d(s_base + kQOff + qb * kQBytes, &P.mq, smem_u32(&b_qfull[qb]), 0,
+                                    (int)(((int64_t)P.b * P.L + P.t0 + lq * TQ) * HI), 0);
+                    }
+                    const int kb = ln % kNK;
+                    if (ln >= kNK && !mbar_wait(smem_u32(&b_kempty[kb]), ((ln / kNK) - 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
+                    mbar_expect_tx(smem_u32(&b_kfull[kb]), kKBytes);
+                    tma_load_3d(s_base + kKOff + kb * kKBytes, &P.mk, smem_u32(&b_kfull[kb]), 0, P.b * P.ncap + le * kJ, 0);
+                    ++ln;
+                    if (++le == net) {
+                        le = 0;
+                        ++lqn;
+                        do { lq += gridDim.x; } while (lq < P.n_qt && n_et_of(lq) == 0);
+                    }
+                }
+                if (!ok) break;
+                const int net = n_et_of(mq);
+                const int qb = mqn & 1, kb = mn % kNK, db = mn & 1;
+                if (me == 0 && !mbar_wait(smem_u32(&b_qfull[qb]), (mqn >> 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&b_kfull[kb]), (mn / kNK) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
+                if (mn >= 2 && !mbar_wait(smem_u32(&b_dempty[db]), ((mn >> 1) - 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                    mma_e4m3(tmem + db * kN, sdesc_sw64(s_base + kKOff + kb * kKBytes + kk * 32),
+                             sdesc_sw64(s_base + kQOff + qb * kQBytes + kk * 32), idesc, kk);
+                mma_commit(smem_u32(&b_dfull[db]));
+                mma_commit(smem_u32(&b_kempty[kb]));
+                if (me == net - 1) mma_commit(smem_u32(&b_qempty[qb]));
+                ++mn;
+                if (++me == net) {
+                    me = 0;
+                    ++mqn;
+                    do { mq += gridDim.x; } while (mq < P.n_qt && n_et_of(mq) == 0);
+                }
+            }
+            if (!ok) set_timeout();
+        }
+    } else {
+        // ---- epilogue: warpgroup g = warp / 4 takes tokens [g*TQ/2, (g+1)*TQ/2) ----
+        const int g = warp >> 2;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        auto ewait = [&](uint32_t bar, uint32_t par) -> bool {
+            const bool w = mbar_wait(bar, par, kMaxPolls, &g_abort);
+            return !named_sync_or(kBarEpi, kEpi, !w);
+        };
+        int n = 0;
+        for (int qt = blockIdx.x; qt < P.n_qt && ok; qt += gridDim.x) {
+            const int tq0 = P.t0 + qt * TQ;
+            const int n_et = n_et_of(qt);
+            if (n_et == 0) continue;
+            // per (token, head) weights of this query tile (rows past the chunk weigh 0)
+            {
+                const int rr = tid;  // 0..255 = token * HI + head
+                const int tok = tq0 + rr / HI;
+                float v = 0.0f;
+                if (tok <= last_row) {
+                    const int64_t gr = ((int64_t)P.b * P.L + tok) * HI + rr % HI;
+                    v = P.w[gr] * P.q_scale[gr];
+                }
+                s_wq[rr] = v;
+            }
+            named_sync(kBarEpi, kEpi);
+            for (int et = 0; et < n_et; ++et, ++n) {
+                const int db = n & 1;
+                if (!ewait(smem_u32(&b_dfull[db]), (n >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const int j = et * kJ + 32 * (warp & 3) + lane;  // this thread's entry
+                const float sk = j < P.ncap ? P.k_scale[(int64_t)P.b * P.ncap + j] : 0.0f;
+#pragma unroll
+                for (int c = 0; c < (kN / 2) / 32; ++c) {
+                    const int col0 = g * (kN / 2) + c * 32;  // 32 columns = 32/HI tokens
+                    float v[32];
+                    tmem_ld32_sync(tmem + lane_base + db * kN + col0, v);
+#pragma unroll
+                    for (int q = 0; q < 32 / HI; ++q) {
+                        const int tl = col0 / HI + q;  // token within the query tile
+                        const int t = tq0 + tl;
+                        float s = 0.0f;
+#pragma unroll
+                        for (int h = 0; h < HI; ++h) {
+                            const float a = v[q * HI + h];
+                            s = fmaf(s_wq[tl * HI + h], a > 0.0f ? a : 0.0f, s);
+                        }
+                        s *= sk;
+                        if (s == 0.0f) s = 0.0f;
+                        if (t <= last_row && j < visible_entries(t, P.m, P.ncap))
+                            P.S[(int64_t)(t - P.t0) * P.ldS + j] = s;
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&b_dempty[db]));
+            }
+            named_sync(kBarEpi, kEpi);  // s_wq is rewritten for the next query tile
+        }
+        if (!ok && tid == 0) set_timeout();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+bool launch_indexer_tc(const IndexArgs &a, cudaStream_t st) {
+    using namespace idx_tc;
+    if (a.decode || a.idx_t != CSA_FP8E4M3) return false;
+    if (a.H_I != 4 && a.H_I != 8 && a.H_I != 16) return false;
+    IndexTcParams P;
+    memset(&P, 0, sizeof(P));
+    const int TQ = kN / a.H_I;
+    const uint64_t qrows = (uint64_t)a.B * a.L * a.H_I;
+    bool ok = make_map_3d(&P.mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.qI, 64, qrows, 1, 64, kN,
+                          CU_TENSOR_MAP_SWIZZLE_64B);
+    ok = ok && make_map_3d(&P.mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.KI, 64, (uint64_t)a.B * a.ncap, 1, 64, kJ,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) return false;
+    P.q_scale = a.qI_scale;
+    P.k_scale = a.KI_scale;
+    P.w = a.w;
+    P.S = a.S;
+    P.ldS = a.ldS;
+    P.L = a.L; P.m = a.m; P.ncap = a.ncap; P.b = a.b; P.t0 = a.t0; P.nrows = a.nrows;
+    P.n_qt = (a.nrows + TQ - 1) / TQ;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = P.n_qt < sms ? P.n_qt : sms;
+    auto go = [&](auto kern) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        kern<<<grid, kThreads, kSmemBytes, st>>>(P);
+    };
+    if (a.H_I == 4) go(indexer_tc_kernel<4>);
+    else if (a.H_I == 8) go(indexer_tc_kernel<8>);
+    else go(indexer_tc_kernel<16>);
+    count_launches(1);
+    return true;
+}
+
+}  // namespace csa

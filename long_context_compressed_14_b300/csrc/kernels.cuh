@@ -78,5 +78,6 @@ void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
 // what they handle
 bool launch_hca_tc(const AttnArgs &a, cudaStream_t st);
 bool launch_csa_tc(const AttnArgs &a, cudaStream_t st);
+bool launch_indexer_tc(const IndexArgs &a, cudaStream_t st);
 
 }  // namespace csa
