@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
     __shared__ float s_f[kH];          // rescale factor per head of the current update
     __shared__ float s_red[4][kH];     // cross-warp reduction scratch
     __shared__ float s_fo[kH];         // final output factor per head
+    __shared__ int s_cnt[3];           // producer warps' counts of valid top-k entries
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t s_base = smem_u32(sm);
@@ -157,6 +158,22 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         };
         int n = 0;           // global tile item counter
         int pending = -1;    // item whose k_full arrival is outstanding
+        // Fetch of a token's top-k row (bulk copy) and query rows (TMA) into slot it & 1, issued
+        // by one thread as early as the slot is free, so it overlaps the previous token.
+        auto fetch = [&](int it2) {
+            const int row2 = (int)blockIdx.x + it2 * (int)gridDim.x;
+            const int qs2 = it2 & 1;
+            const uint32_t qb = smem_u32(&b_qraw[qs2]);
+            mbar_expect_tx(qb, 2 * kH * 128 + P.topk * 4);
+            bulk_load(s_base + kIdxOff + qs2 * kMaxTopk * 4, P.idx + (int64_t)row2 * P.topk, P.topk * 4, qb);
+            tma_load_3d(s_base + kQOff + qs2 * 16384, &P.mq, qb, 0, row2 * kH, 0);
+            tma_load_3d(s_base + kQOff + qs2 * 16384 + 8192, &P.mq, qb, 64, row2 * kH, 0);
+        };
+        int fetched = 0;  // tokens whose fetch has been issued
+        if (ptid == 0 && n_tok_cta > 0) {
+            fetch(0);
+            fetched = 1;
+        }
         for (int it = 0; it < n_tok_cta && ok; ++it) {
             const int row = (int)blockIdx.x + it * (int)gridDim.x;
             const int qs = it & 1;
@@ -167,7 +184,14 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 mbar_arrive(smem_u32(&b_kfull[pending % kNB]));
                 pending = -1;
             }
-            if (it >= 2 && !pwait(smem_u32(&b_qempty[qs]), ((it >> 1) - 1) & 1)) { ok = false; break; }
+            if (ptid == 0 && fetched == it) {  // not prefetched: the slot must be free first
+                if (it >= 2 && !mbar_wait(smem_u32(&b_qempty[qs]), ((it >> 1) - 1) & 1, kMaxPolls, &g_abort)) ok = false;
+                if (ok) {
+                    fetch(it);
+                    fetched = it + 1;
+                }
+            }
+            if (named_sync_or(kBarProd, kProducers, !ok)) { ok = false; break; }
             int b, t;
             if (P.decode) {
                 b = row;
@@ -177,30 +201,21 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 t = row % P.L;
             }
             const bool pos_ok = t >= 0 && t < P.L;
-            // top-k row -> shared memory; count the valid prefix
-            int32_t *sidx = reinterpret_cast<int32_t *>(sm + kIdxOff) + qs * kMaxTopk;
-            const int32_t *gidx = P.idx + (int64_t)row * P.topk;
-            for (int i = ptid; i < P.topk; i += kProducers) sidx[i] = pos_ok ? gidx[i] : -1;
-            named_sync(kBarProd, kProducers);
-            if (ptid == 0) {
-                int ns = 0;
-                while (ns < P.topk && sidx[ns] >= 0) ++ns;  // ascending, -1 padded
-                TokenMeta mt;
-                mt.n_sel = ns;
-                mt.n_ct = (ns + kTile - 1) / kTile;
-                mt.t = t;
-                mt.b = b;
-                mt.n_win_t = pos_ok ? min(P.n_win, t + 1) : 0;
-                meta[qs] = mt;
-                // query rows: 64 heads x 128 dims
-                const uint32_t qb = smem_u32(&b_qraw[qs]);
-                mbar_expect_tx(qb, 2 * kH * 128);
-                tma_load_3d(s_base + kQOff + qs * 16384, &P.mq, qb, 0, row * kH, 0);
-                tma_load_3d(s_base + kQOff + qs * 16384 + 8192, &P.mq, qb, 64, row * kH, 0);
-            }
-            named_sync(kBarProd, kProducers);
-            const TokenMeta mt = meta[qs];
             if (!pwait(smem_u32(&b_qraw[qs]), (it >> 1) & 1)) { ok = false; break; }
+            // count the valid prefix of the top-k row (ascending, -1 padded) in parallel
+            int32_t *sidx = reinterpret_cast<int32_t *>(sm + kIdxOff) + qs * kMaxTopk;
+            int cnt = 0;
+            for (int i = ptid; i < P.topk; i += kProducers) cnt += (pos_ok && sidx[i] >= 0) ? 1 : 0;
+            cnt = __reduce_add_sync(0xffffffffu, cnt);
+            if ((ptid & 31) == 0) s_cnt[(tid - kProd0) >> 5] = cnt;
+            named_sync(kBarProd, kProducers);
+            TokenMeta mt;
+            mt.n_sel = s_cnt[0] + s_cnt[1] + s_cnt[2];
+            mt.n_ct = (mt.n_sel + kTile - 1) / kTile;
+            mt.t = t;
+            mt.b = b;
+            mt.n_win_t = pos_ok ? min(P.n_win, t + 1) : 0;
+            if (ptid == 0) meta[qs] = mt;
             // RoPE on dims 64..127 at position t: head h, chunk pair (c, c+4) of the second half
             if (P.d_rope == 64 && pos_ok) {
                 uint8_t *q1 = sm + kQOff + qs * 16384 + 8192;
@@ -295,6 +310,12 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     }
                 }
                 cp_async_commit();
+                // fetch the next token's rows once its slot is free (never blocking here)
+                if (ptid == 0 && fetched == it + 1 && it + 1 < n_tok_cta &&
+                    (it + 1 < 2 || mbar_try_wait(smem_u32(&b_qempty[(it + 1) & 1]), (((it + 1) >> 1) - 1) & 1))) {
+                    fetch(it + 1);
+                    fetched = it + 2;
+                }
                 if (pending >= 0) {
                     cp_async_wait_1();
                     fence_async_smem();
@@ -491,8 +512,8 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int h = ch * 8 + 2 * e;
-                        const float p0 = s[h] == -INFINITY ? 0.0f : exp2f(s[h] - s_m[h]);
-                        const float p1 = s[h + 1] == -INFINITY ? 0.0f : exp2f(s[h + 1] - s_m[h + 1]);
+                        const float p0 = s[h] == -INFINITY ? 0.0f : fast_exp2(s[h] - s_m[h]);
+                        const float p1 = s[h + 1] == -INFINITY ? 0.0f : fast_exp2(s[h + 1] - s_m[h + 1]);
                         lpart[h] += p0;
                         lpart[h + 1] += p1;
                         pk[e] = pack2(p0, p1);
@@ -561,27 +582,28 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             if (mt.t >= 0 && mt.t < P.L) {
                 const int64_t orow = P.decode ? (int64_t)mt.b : (int64_t)mt.b * P.L + mt.t;
                 __nv_bfloat16 *out = P.out + orow * kH * 128;
-                for (int u = tid; u < kH * 16; u += kSoftmax) {
-                    const int h = u >> 4, q = u & 15;
+                // thread tid always handles dims [8q, 8q+8), q = tid & 15, of heads (tid >> 4) + 8k,
+                // so its RoPE factors are fetched once
+                const int q = tid & 15;
+                const bool rot = P.d_rope == 64 && q >= 8;
+                const int i0 = 8 * ((q - 8) & 3);
+                float2 cs[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) cs[e] = rot ? P.rope[(int64_t)mt.t * 32 + i0 + e] : make_float2(1.0f, 0.0f);
+#pragma unroll
+                for (int k = 0; k < kH / 8; ++k) {
+                    const int h = (tid >> 4) + 8 * k;
                     const float *src = os + h * 128;
                     float y[8];
-                    if (q < 8 || P.d_rope != 64) {
+                    if (!rot) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) y[e] = src[8 * q + e];
                     } else if (q < 12) {  // dims 64 + i, partner 96 + i
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = 8 * (q - 8) + e;
-                            const float2 cs = P.rope[(int64_t)mt.t * 32 + i];
-                            y[e] = src[64 + i] * cs.x + src[96 + i] * cs.y;
-                        }
+                        for (int e = 0; e < 8; ++e) y[e] = src[64 + i0 + e] * cs[e].x + src[96 + i0 + e] * cs[e].y;
                     } else {  // dims 96 + i
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = 8 * (q - 12) + e;
-                            const float2 cs = P.rope[(int64_t)mt.t * 32 + i];
-                            y[e] = -src[64 + i] * cs.y + src[96 + i] * cs.x;
-                        }
+                        for (int e = 0; e < 8; ++e) y[e] = -src[64 + i0 + e] * cs[e].y + src[96 + i0 + e] * cs[e].x;
                     }
                     *reinterpret_cast<uint4 *>(out + h * 128 + 8 * q) =
                         make_uint4(pack2(y[0], y[1]), pack2(y[2], y[3]), pack2(y[4], y[5]), pack2(y[6], y[7]));
@@ -599,9 +621,10 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
 bool csa_tc_supported(const AttnArgs &a) {
     if (a.act_t != CSA_BF16) return false;
     if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED) return false;
-    if (a.H != csa_tc::kH || a.n_win != 128 || a.topk < 1 || a.topk > kMaxTopk) return false;
+    if (a.H != csa_tc::kH || a.n_win != 128 || a.topk < 4 || a.topk > kMaxTopk || a.topk % 4 != 0) return false;
     if (a.d_rope != 0 && a.d_rope != 64) return false;
-    return a.idx != nullptr;
+    // top-k rows are fetched with a bulk copy: 16-byte aligned rows
+    return a.idx != nullptr && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0;
 }
 
 bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {

@@ -259,8 +259,8 @@ __global__ void __launch_bounds__(128, 1) hca_tc_kernel(const __grid_constant__ 
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
-                const float p0 = (c0 + e >= lo && c0 + e < hi) ? exp2f(v[e] * P.scale_log2 - m_run) : 0.0f;
-                const float p1 = (c0 + e + 1 >= lo && c0 + e + 1 < hi) ? exp2f(v[e + 1] * P.scale_log2 - m_run) : 0.0f;
+                const float p0 = (c0 + e >= lo && c0 + e < hi) ? fast_exp2(v[e] * P.scale_log2 - m_run) : 0.0f;
+                const float p1 = (c0 + e + 1 >= lo && c0 + e + 1 < hi) ? fast_exp2(v[e + 1] * P.scale_log2 - m_run) : 0.0f;
                 l_run += p0 + p1;
                 pk[e >> 1] = pack_bf16x2(p0, p1);
             }

@@ -54,6 +54,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     return false;
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: about 2 ulp, -inf -> +0); the
+// softmax weights it produces are rounded to BF16 (8 bits) afterwards.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- proxy fences ----------------------------------------------------------------------
 // generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma / TMA)
 __device__ __forceinline__ void fence_async_smem() {
@@ -186,6 +194,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
             dst),
         "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of 16), completion
+// counted in bytes on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled region whose
