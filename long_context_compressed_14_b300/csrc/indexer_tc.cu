@@ -16,8 +16,8 @@
 // each token and stores the token's score -- the 128 threads of a warpgroup write 128
 // consecutive entries of one score row at a time.
 //
-// CTA (persistent): warps 0-7 epilogue (two warpgroups, one per half of the tokens), warp 8
-// lane 0 loads tiles by TMA and issues the MMAs. Query tiles are dealt round-robin; each walks
+// CTA (persistent): warps 0-15 epilogue (four warpgroups, one per quarter of the tokens of a
+// query tile), warp 16 lane 0 loads tiles by TMA and issues the MMAs. Query tiles are dealt round-robin; each walks
 // only the entry tiles its last token can see (causal skipping). D is double-buffered in TMEM
 // (2 x 256 columns), entry tiles flow through a 4-deep ring, query tiles through 2 buffers.
 #include "common.cuh"
@@ -29,8 +29,10 @@ namespace csa {
 using namespace umma;
 
 namespace idx_tc {
-constexpr int kEpi = 256;               // epilogue threads (warps 0-7)
-constexpr int kThreads = kEpi + 32;     // + warp 8
+constexpr int kEpiWG = 4;               // epilogue warpgroups
+constexpr int kEpi = 128 * kEpiWG;      // epilogue threads (warps 0-15)
+constexpr int kMmaWarp = kEpi / 32;     // warp 16: TMA loads + MMA issue
+constexpr int kThreads = kEpi + 32;
 constexpr int kJ = 128;                 // entries per tile (M)
 constexpr int kN = 256;                 // (token, head) rows per query tile (N)
 constexpr int kNK = 4;                  // entry-tile ring
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t b_qfull[2], b_qempty[2], b_kfull[kNK], b_kempty[kNK], b_dfull[2], b_dempty[2];
     __shared__ uint32_t tmem_slot;
-    __shared__ float s_wq[kN];  // w * q_scale per (token, head) of the current query tile
+    __shared__ __align__(16) float s_wq[kN];  // w * q_scale per (token, head) of the current query tile
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t s_base = smem_u32(sm);
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
     };
     bool ok = true;
 
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         if (lane == 0) {
             // ---- producer + MMA issue (one thread) ----
             // Two cursors walk the same item sequence (query tiles of this CTA, each with its
@@ -167,7 +169,10 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
             if (!ok) set_timeout();
         }
     } else {
-        // ---- epilogue: warpgroup g = warp / 4 takes tokens [g*TQ/2, (g+1)*TQ/2) ----
+        // ---- epilogue: warpgroup g = warp / 4 takes the columns [g*C, (g+1)*C) of D, i.e.
+        // tokens [g*C/HI, (g+1)*C/HI) of the query tile; thread = one entry of the tile ----
+        constexpr int C = kN / kEpiWG;  // 64 columns
+        constexpr int TW = C / HI;      // tokens per warpgroup
         const int g = warp >> 2;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         auto ewait = [&](uint32_t bar, uint32_t par) -> bool {
@@ -180,8 +185,7 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
             const int n_et = n_et_of(qt);
             if (n_et == 0) continue;
             // per (token, head) weights of this query tile (rows past the chunk weigh 0)
-            {
-                const int rr = tid;  // 0..255 = token * HI + head
+            for (int rr = tid; rr < kN; rr += kEpi) {  // rr = token * HI + head
                 const int tok = tq0 + rr / HI;
                 float v = 0.0f;
                 if (tok <= last_row) {
@@ -191,35 +195,36 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
                 s_wq[rr] = v;
             }
             named_sync(kBarEpi, kEpi);
+            const int t_g = tq0 + g * TW;  // first token of this warpgroup
+            float *srow0 = P.S + (int64_t)(t_g - P.t0) * P.ldS;
             for (int et = 0; et < n_et; ++et, ++n) {
                 const int db = n & 1;
                 if (!ewait(smem_u32(&b_dfull[db]), (n >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                const int j = et * kJ + 32 * (warp & 3) + lane;  // this thread's entry
-                const float sk = j < P.ncap ? P.k_scale[(int64_t)P.b * P.ncap + j] : 0.0f;
-#pragma unroll
-                for (int c = 0; c < (kN / 2) / 32; ++c) {
-                    const int col0 = g * (kN / 2) + c * 32;  // 32 columns = 32/HI tokens
-                    float v[32];
-                    tmem_ld32_sync(tmem + lane_base + db * kN + col0, v);
-#pragma unroll
-                    for (int q = 0; q < 32 / HI; ++q) {
-                        const int tl = col0 / HI + q;  // token within the query tile
-                        const int t = tq0 + tl;
-                        float s = 0.0f;
-#pragma unroll
-                        for (int h = 0; h < HI; ++h) {
-                            const float a = v[q * HI + h];
-                            s = fmaf(s_wq[tl * HI + h], a > 0.0f ? a : 0.0f, s);
-                        }
-                        s *= sk;
-                        if (s == 0.0f) s = 0.0f;
-                        if (t <= last_row && j < visible_entries(t, P.m, P.ncap))
-                            P.S[(int64_t)(t - P.t0) * P.ldS + j] = s;
-                    }
-                }
+                float v[C];
+                tmem_ld64_sync(tmem + lane_base + db * kN + g * C, v);
+                // the accumulators are in registers: hand the TMEM buffer back to the MMA
                 tc_fence_before();
                 mbar_arrive(smem_u32(&b_dempty[db]));
+                const int j = et * kJ + 32 * (warp & 3) + lane;  // this thread's entry
+                const int t_first = (j + 1) * P.m - 1;            // first token that sees entry j
+                const float sk = j < P.ncap ? P.k_scale[(int64_t)P.b * P.ncap + j] : 0.0f;
+#pragma unroll
+                for (int q = 0; q < TW; ++q) {
+                    const int t = t_g + q;
+                    const float4 *wq = reinterpret_cast<const float4 *>(s_wq + (g * TW + q) * HI);
+                    float s = 0.0f;
+#pragma unroll
+                    for (int h4 = 0; h4 < HI / 4; ++h4) {
+                        const float4 w4 = wq[h4];
+                        s = fmaf(w4.x, fmaxf(v[q * HI + 4 * h4 + 0], 0.0f), s);
+                        s = fmaf(w4.y, fmaxf(v[q * HI + 4 * h4 + 1], 0.0f), s);
+                        s = fmaf(w4.z, fmaxf(v[q * HI + 4 * h4 + 2], 0.0f), s);
+                        s = fmaf(w4.w, fmaxf(v[q * HI + 4 * h4 + 3], 0.0f), s);
+                    }
+                    s = s * sk + 0.0f;  // + 0 turns -0 into +0
+                    if (t >= t_first && t <= last_row) srow0[(int64_t)q * P.ldS + j] = s;
+                }
             }
             named_sync(kBarEpi, kEpi);  // s_wq is rewritten for the next query tile
         }

@@ -147,6 +147,50 @@ def test_index_topk_ties_prefer_lower_index(lib):
     np.testing.assert_array_equal(out.cpu().numpy()[0], oracle.topk(s, m, rows, k))
 
 
+@pytest.mark.parametrize("L,m,k", [(20000, 1, 64), (70000, 1, 1024)])
+def test_index_topk_f32_long_rows(lib, L, m, k):
+    # rows of up to 70000 visible entries (longer than any shared-memory staging), FP32
+    # bit-exact on the last rows and a random sample
+    g = torch.Generator().manual_seed(L)
+    H_I = 2
+    N = math.ceil(L / m)
+    qI = torch.randn((1, L, H_I, 64), generator=g)
+    KI = torch.randn((1, N, 64), generator=g)
+    w = torch.randn((1, L, H_I), generator=g)
+    p = lib.make_params(B=1, L=L, H=8, m=m, topk=k, H_I=H_I, act="f32", kv="f32", idx="f32")
+    out = torch.empty((1, L, k), dtype=torch.int32, device=DEV)
+    lib.csa_index_topk(p, (qI.to(DEV), None), (KI.to(DEV), None), w.to(DEV), out,
+                       lib.alloc_workspace(p, lib.OP_INDEX_TOPK))
+    rows = np.unique(np.concatenate([np.arange(L - 40, L), np.random.default_rng(L).integers(0, L, 40)]))
+    s = oracle.index_scores_f32(qI[0].numpy()[rows], KI[0].numpy(), w[0].numpy()[rows], m, rows)
+    np.testing.assert_array_equal(out.cpu().numpy()[0][rows], oracle.topk(s, m, rows, k))
+
+
+def test_index_topk_heavy_ties(lib):
+    # Rows whose weights are all zero score 0 everywhere: the threshold bin holds every entry
+    # (more than fits in shared memory), and the lowest indices must win. Rows with a single
+    # non-zero weight and 0/1 operands score small integers: many exact ties at the threshold.
+    L, m, H_I, k = 12000, 1, 2, 300
+    g = torch.Generator().manual_seed(17)
+    qI = torch.randint(0, 2, (1, L, H_I, 64), generator=g).float()
+    KI = torch.randint(0, 2, (1, L, 64), generator=g).float()
+    w = torch.zeros((1, L, H_I))
+    w[0, ::2, 0] = 1.0  # even rows: integer scores; odd rows: all zero
+    p = lib.make_params(B=1, L=L, H=8, m=m, topk=k, H_I=H_I, act="f32", kv="f32", idx="f32")
+    out = torch.empty((1, L, k), dtype=torch.int32, device=DEV)
+    lib.csa_index_topk(p, (qI.to(DEV), None), (KI.to(DEV), None), w.to(DEV), out,
+                       lib.alloc_workspace(p, lib.OP_INDEX_TOPK))
+    rows = np.concatenate([np.arange(L - 30, L), np.arange(5000, 5030), np.arange(290, 310)])
+    s = oracle.index_scores_f32(qI[0].numpy()[rows], KI[0].numpy(), w[0].numpy()[rows], m, rows)
+    got = out.cpu().numpy()[0][rows]
+    np.testing.assert_array_equal(got, oracle.topk(s, m, rows, k))
+    odd = rows % 2 == 1
+    big = rows + 1 > k
+    assert np.all(got[odd & big] == np.arange(k)[None, :])
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
+
+
 def test_index_topk_fp8(lib):
     L, m, H_I, k = 4096, 4, 8, 512
     g = torch.Generator().manual_seed(9)
