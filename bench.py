@@ -114,6 +114,7 @@ class PrefillStep:
         self.layer = PrefillLayer.create(wl, csa)
         p = self.layer.p
         self.ws_idx = lib.alloc_workspace(p, lib.OP_INDEX_TOPK) if (csa and p.topk > 0) else None
+        self.ws_attn = lib.alloc_workspace(p, lib.OP_SPARSE_ATTENTION) if csa else None
 
     def stages(self):
         lib, L, inp, p = self.lib, self.layer, self.inp, self.layer.p
@@ -128,13 +129,15 @@ class PrefillStep:
                                                                          L.C, L.KI, L.kv_rope)))
             out.append((f"{self.tag}index_topk", lambda: lib.csa_index_topk(p, qI, L.KI, inp["w"], L.topk, self.ws_idx)))
             out.append((f"{self.tag}attention", lambda: lib.csa_sparse_attention(p, inp["q"], L.kv_rope, L.C, L.topk,
-                                                                                 inp["sink"], L.rope, L.out, None)))
+                                                                                 inp["sink"], L.rope, L.out, None,
+                                                                                 self.ws_attn)))
         else:
             out.append((f"{self.tag}kv_compress", lambda: lib.kv_compress(p, inp["kv"], inp["z"], None, L.rope, L.C, None,
                                                                          L.kv_rope)))
             if self.csa:
                 out.append((f"{self.tag}attention", lambda: lib.csa_sparse_attention(p, inp["q"], L.kv_rope, None, None,
-                                                                                     inp["sink"], L.rope, L.out, None)))
+                                                                                     inp["sink"], L.rope, L.out, None,
+                                                                                     self.ws_attn)))
             else:
                 out.append((f"{self.tag}attention", lambda: lib.hca_prefill(p, inp["q"], L.kv_rope, L.C, inp["sink"],
                                                                             L.rope, L.out, None, L.ws)))

@@ -102,7 +102,8 @@ typedef enum {
     CSA_OP_CSA_PREFILL = 1,
     CSA_OP_HCA_PREFILL = 2,
     CSA_OP_CSA_DECODE = 3,
-    CSA_OP_HCA_DECODE = 4
+    CSA_OP_HCA_DECODE = 4,
+    CSA_OP_SPARSE_ATTENTION = 5
 } csa_op;
 
 /* Human-readable text of a status code (static storage). */
@@ -179,10 +180,13 @@ int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
 
 /* The attention stage of csa_prefill with the selection given by the caller: topk_idx
  * [B, L, topk] int32 as written by csa_index_topk (ascending, -1 padded). Everything else as
- * in csa_prefill. Uses no workspace. */
+ * in csa_prefill. Workspace: csa_workspace_bytes(p, CSA_OP_SPARSE_ATTENTION) bytes (non-zero
+ * only for mixed-precision entries, which are widened to BF16 once per call); ws may be NULL
+ * when that is 0. */
 int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope,
                          const csa_entries *C, const int32_t *topk_idx, const float *sink,
-                         const float *rope_tab, void *out, float *lse_out, csa_stream_t stream);
+                         const float *rope_tab, void *out, float *lse_out, void *ws,
+                         size_t ws_bytes, csa_stream_t stream);
 
 /* HCA prefill ([P2] 提案手法 §1 HCA: m' = 128, no sparse selection, dense attention over the
  * compressed entries; plus sliding window and sink as for CSA). Key set of row t: every

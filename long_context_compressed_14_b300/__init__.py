@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 # csa_dtype
 F32, BF16, FP8E4M3, MIXED = 0, 1, 2, 3
 # csa_op
-OP_INDEX_TOPK, OP_CSA_PREFILL, OP_HCA_PREFILL, OP_CSA_DECODE, OP_HCA_DECODE = range(5)
+OP_INDEX_TOPK, OP_CSA_PREFILL, OP_HCA_PREFILL, OP_CSA_DECODE, OP_HCA_DECODE, OP_SPARSE_ATTENTION = range(6)
 # csa_status
 OK, ERR_INVALID, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_TIMEOUT, ERR_BOUNDS, ERR_CUDA = range(8)
 
@@ -77,7 +77,7 @@ def _load():
             "hca_prefill": (I, [PP, P, P, PE, P, P, P, P, P, Z, P]),
             "csa_decode": (I, [PP, P, P, PE, PI, PI, P, P, P, P, P, P, P, P, Z, P]),
             "hca_decode": (I, [PP, P, P, PE, P, P, P, P, P, P, Z, P]),
-            "csa_sparse_attention": (I, [PP, P, P, PE, P, P, P, P, P, P]),
+            "csa_sparse_attention": (I, [PP, P, P, PE, P, P, P, P, P, P, ctypes.c_size_t, P]),
             "csa_decode_static_scratch": (I, [PP, P, P, PE, PI, PI, P, P, P, P, P, P, P, P]),
             "csa_launch_count": (ctypes.c_uint64, []),
             "csa_device_status": (I, [ctypes.POINTER(ctypes.c_int), I]),
@@ -100,6 +100,10 @@ def _ptr(t: Optional[torch.Tensor]):
     if not t.is_contiguous():
         raise ValueError("tensors passed to libcsa must be contiguous")
     return t.data_ptr()
+
+
+def _nbytes(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
 
 
 def _stream(stream) -> Optional[int]:
@@ -184,9 +188,10 @@ def csa_prefill(p: Params, q, kv_rope, C, qI, KI, w, sink, rope_tab, topk_out, o
         "csa_prefill")
 
 
-def csa_sparse_attention(p: Params, q, kv_rope, C, topk_idx, sink, rope_tab, out, lse_out, stream=None):
+def csa_sparse_attention(p: Params, q, kv_rope, C, topk_idx, sink, rope_tab, out, lse_out, ws=None, stream=None):
     _ok(_load().csa_sparse_attention(ctypes.byref(p), _ptr(q), _ptr(kv_rope), _byref(_entries(C)), _ptr(topk_idx),
-                                     _ptr(sink), _ptr(rope_tab), _ptr(out), _ptr(lse_out), _stream(stream)),
+                                     _ptr(sink), _ptr(rope_tab), _ptr(out), _ptr(lse_out), _ptr(ws), _nbytes(ws),
+                                     _stream(stream)),
         "csa_sparse_attention")
 
 

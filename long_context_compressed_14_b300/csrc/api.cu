@@ -41,13 +41,14 @@ inline int64_t score_chunk_rows(const csa_params *p) {
 }
 
 bool is_csa(int op) {
-    return op == CSA_OP_INDEX_TOPK || op == CSA_OP_CSA_PREFILL || op == CSA_OP_CSA_DECODE;
+    return op == CSA_OP_INDEX_TOPK || op == CSA_OP_CSA_PREFILL || op == CSA_OP_CSA_DECODE ||
+           op == CSA_OP_SPARSE_ATTENTION;
 }
 bool is_decode(int op) { return op == CSA_OP_CSA_DECODE || op == CSA_OP_HCA_DECODE; }
 
 int check(const csa_params *p, int op) {
     if (!p) return CSA_ERR_INVALID;
-    if (op < CSA_OP_INDEX_TOPK || op > CSA_OP_HCA_DECODE) return CSA_ERR_INVALID;
+    if (op < CSA_OP_INDEX_TOPK || op > CSA_OP_SPARSE_ATTENTION) return CSA_ERR_INVALID;
     if (p->B < 1 || p->L < 1 || p->H < 1 || p->m < 1 || p->n_win < 1) return CSA_ERR_INVALID;
     if (!(p->scale > 0.0f) || !isfinite(p->scale)) return CSA_ERR_INVALID;
     if (p->d != kD) return CSA_ERR_UNSUPPORTED;
@@ -75,6 +76,11 @@ int check(const csa_params *p, int op) {
     return CSA_OK;
 }
 
+// Bytes of the entries widened to BF16 (prefill with mixed-precision entries).
+size_t widen_bytes(const csa_params *p) {
+    return p->kv_t == CSA_MIXED ? align_up((size_t)p->B * (size_t)ncap_of(p) * kD * 2) : 0;
+}
+
 size_t ws_bytes(const csa_params *p, int op) {
     switch (op) {
     case CSA_OP_INDEX_TOPK:
@@ -82,7 +88,11 @@ size_t ws_bytes(const csa_params *p, int op) {
     case CSA_OP_CSA_PREFILL:
         if (p->topk == 0) return 0;
         return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p)) +
-               align_up(sizeof(int32_t) * (size_t)p->B * p->L * p->topk);
+               align_up(sizeof(int32_t) * (size_t)p->B * p->L * p->topk) + widen_bytes(p);
+    case CSA_OP_SPARSE_ATTENTION:
+        return p->topk > 0 ? widen_bytes(p) : 0;
+    case CSA_OP_HCA_PREFILL:
+        return widen_bytes(p);
     case CSA_OP_CSA_DECODE:
         if (p->topk == 0) return 0;
         return align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) +
@@ -145,8 +155,10 @@ int run_index_topk(const csa_params *p, const csa_index_rows *qI, const csa_inde
 
 AttnArgs attn_args(const csa_params *p, const void *q, const void *kvr, const csa_entries *C,
                    const int32_t *idx, const int32_t *ctx, const float *sink, const float *rope,
-                   void *out, float *lse, int decode, int topk) {
+                   void *out, float *lse, int decode, int topk, void *ws = nullptr, size_t wsb = 0) {
     AttnArgs a{};
+    a.ws = ws;
+    a.ws_bytes = wsb;
     a.q = q;
     a.kv_rope = kvr;
     a.c_data = C ? C->data : nullptr;
@@ -255,15 +267,18 @@ int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
     }
     cudaStream_t st = cs(stream);
     int32_t *idx = nullptr;
+    void *wide = nullptr;
     if (p->topk > 0) {
         float *S = reinterpret_cast<float *>(ws);
         const size_t sbytes = align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
+        const size_t ibytes = align_up(sizeof(int32_t) * (size_t)p->B * p->L * p->topk);
         idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
+        wide = reinterpret_cast<char *>(ws) + sbytes + ibytes;
         s = run_index_topk(p, qI, KI, w, idx, S, st);
         if (s) return s;
     }
     AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, idx, nullptr, sink, rope_tab, out,
-                           lse_out, 0, p->topk);
+                           lse_out, 0, p->topk, wide, widen_bytes(p));
     if (p->topk == 0) a.ncap = 0;
     if (!launch_csa_tc(a, st)) launch_attn_simple(a, st);
     return launch_status();
@@ -271,14 +286,17 @@ int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
 
 int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope,
                          const csa_entries *C, const int32_t *topk_idx, const float *sink,
-                         const float *rope_tab, void *out, float *lse_out, csa_stream_t stream) {
-    int s = check(p, CSA_OP_CSA_PREFILL);
+                         const float *rope_tab, void *out, float *lse_out, void *ws, size_t wsb,
+                         csa_stream_t stream) {
+    int s = check(p, CSA_OP_SPARSE_ATTENTION);
     if (s) return s;
     if (!q || !kv_rope || !out || !aligned16(q) || !aligned16(kv_rope) || !aligned16(out)) return CSA_ERR_INVALID;
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
     if (p->topk > 0 && (!entries_ok(p, C) || !topk_idx)) return CSA_ERR_INVALID;
+    const size_t need = ws_bytes(p, CSA_OP_SPARSE_ATTENTION);
+    if (need > 0 && (wsb < need || !ws || !aligned16(ws))) return CSA_ERR_WORKSPACE;
     AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, p->topk > 0 ? topk_idx : nullptr, nullptr, sink,
-                           rope_tab, out, lse_out, 0, p->topk);
+                           rope_tab, out, lse_out, 0, p->topk, ws, wsb);
     if (p->topk == 0) a.ncap = 0;
     if (!launch_csa_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
     return launch_status();

@@ -11,26 +11,32 @@
 // puts the KEYS on the MMA's M dimension and the heads on N:
 //   S^T[key, head] = K Q^T     (M = 128 keys, N = 64 heads, K = 128 dims)
 //   O^T[dim, head] += V^T P^T  (M = 128 dims, N = 64 heads, K = 128 keys)
-// which keeps both MMAs at M = 128 (full tensor-core rate). The key tile is one shared-memory
-// buffer read as the K-major A operand of the first MMA and, through an MN-major descriptor,
-// as V^T for the second; P^T is written by the softmax threads as 128-byte key rows and read as
-// an MN-major B operand.
+// which keeps both MMAs at M = 128. The key tile is one shared-memory buffer read as the
+// K-major A operand of the first MMA and, through an MN-major descriptor, as V^T for the
+// second; P^T is written by the softmax threads as 128-byte key rows and read as an MN-major
+// B operand.
 //
-// One softmax thread owns one key (TMEM lane) and holds its 64 head logits; the per-head
-// running max is shared across the 128 keys of a tile. It is kept lazily: a tile only triggers
-// a CTA-wide max reduction when some logit exceeds the current max by more than 8 (log2
-// units), which in practice happens on a token's first tile; O^T (in TMEM) and the partial
-// sums are rescaled only then. Per-head sums are partial per thread and reduced once per
-// token.
+// Softmax: two warpgroups, WG w owning heads [32w, 32w + 32); thread = one key (TMEM lane) x
+// 32 heads. The per-head running maximum is shared by the 128 keys of a tile and kept lazily:
+// P = exp2(s - m) is computed with the current maximum, and only when some value exceeds 2^8
+// does the warpgroup reduce the tile's per-head maxima, move m, and rescale its partial sums
+// and O^T (in TMEM). That happens on a token's first tile and rarely after. Per-head sums are
+// partial per thread and reduced once per token.
 //
-// Warp roles (256 threads, persistent over tokens):
-//   warps 0-3  softmax and epilogue (they own TMEM lanes 0-127);
-//   warp 4     MMA issue (one thread);
-//   warps 5-7  producers: query rows by TMA + RoPE, top-k row, key tiles gathered with
-//              cp.async (mixed entries: the FP8 half widened to BF16 by the threads), the
-//              window tile by TMA (prefill) or gathered from the ring (decode).
-// Pipelines: key tiles in a 3-buffer ring, S^T double-buffered in TMEM, P^T double-buffered in
-// shared memory, query rows double-buffered; every wait is bounded.
+// Warp roles (416 threads, persistent over tokens):
+//   warps 0-7   softmax and epilogue (two warpgroups; TMEM lanes 0-127 each);
+//   warp 8      MMA issue (one thread);
+//   warps 9-12  producers: query rows by TMA + RoPE, top-k row by bulk copy, key tiles gathered
+//               with cp.async (decode with mixed entries: the FP8 half widened to BF16 by the
+//               threads), the window tile by TMA (prefill) or gathered from the ring (decode).
+// Pipelines: key tiles in a 3-buffer ring, S^T and O^T double-buffered in TMEM (O^T by token),
+// P^T double-buffered in shared memory, query rows double-buffered; every wait is bounded.
+// Epilogue: O^T is normalised per head, the RoPE half is rotated back (the two dims of a pair
+// live in different warps and meet in shared memory), staged as BF16 [head][dim] and written
+// with one 16 KB bulk copy per token.
+//
+// Prefill with mixed-precision entries first widens every entry to BF16 once (code * row
+// scale, rounded to nearest even) into caller workspace; the gather then reads BF16 rows.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tma_host.cuh"
@@ -40,26 +46,27 @@ namespace csa {
 using namespace umma;
 
 namespace csa_tc {
-constexpr int kThreads = 256;
-constexpr int kSoftmax = 128;                 // warps 0-3
-constexpr int kMmaWarp = 4;
-constexpr int kProd0 = 160;                   // first producer thread (warp 5)
-constexpr int kProducers = 96;                // warps 5-7
+constexpr int kSoftmax = 256;                 // warps 0-7
+constexpr int kMmaWarp = 8;
+constexpr int kProd0 = 288;                   // first producer thread (warp 9)
+constexpr int kProducers = 128;               // warps 9-12
+constexpr int kThreads = kProd0 + kProducers; // 416
 constexpr int kH = 64;                        // heads (N of both MMAs)
 constexpr int kTile = 128;                    // keys per tile
 constexpr int kNB = 3;                        // key-tile buffers
 constexpr int kQOff = 0;                      // Q: 2 buffers x 16 KB (two 64-dim halves of 8 KB)
 constexpr int kKOff = 32768;                  // keys: kNB x 32 KB (two 64-dim halves of 16 KB)
 constexpr int kPOff = kKOff + kNB * 32768;    // P^T: 2 x 16 KB
-constexpr int kOsOff = kPOff + 2 * 16384;     // epilogue staging [64 heads][128 dims] float
-constexpr int kIdxOff = kOsOff + 32768;       // top-k rows: 2 x kMaxTopk int32
+constexpr int kOutOff = kPOff + 2 * 16384;    // output staging: [64 heads][128 dims] BF16
+constexpr int kXOff = kOutOff + 16384;        // RoPE exchange: [2 WG][2 halves][32 heads][32] float
+constexpr int kIdxOff = kXOff + 16384;        // top-k rows: 2 x kMaxTopk int32
 constexpr int kSmemBytes = kIdxOff + 2 * kMaxTopk * 4 + 1024;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 0;                 // O^T: columns [0, 64)
-constexpr uint32_t kSCol = 64;                // S^T slots: [64, 128) and [128, 192)
-constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSCol = 0;                 // S^T slots: [0, 64) and [64, 128)
+constexpr uint32_t kOCol = 128;               // O^T slots: [128, 192) and [192, 256)
+constexpr float kOver = 8.0f;                 // log2 of the largest unnormalised weight allowed
 // named barriers (0 is __syncthreads)
-constexpr uint32_t kBarSoftmax = 1, kBarProd = 2;
+constexpr uint32_t kBarSoftmax = 1, kBarProd = 2, kBarWG0 = 3;  // kBarWG0 + w per warpgroup
 }  // namespace csa_tc
 
 struct CsaTcParams {
@@ -87,11 +94,44 @@ struct TokenMeta {
     int t;       // query position
     int b;       // sequence
     int n_win_t; // window rows that exist (<= n_win)
+    int pos_ok;  // 0: a decode position outside the cache (nothing is stored)
 };
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// bulk copy shared -> global (both 16-byte aligned, size a multiple of 16), bulk-group tracked
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Transposed warp reduction of 32 values per lane: afterwards lane L holds the reduction of
+// value L over the 32 lanes (the upper half of the lanes keeps the upper half of the values at
+// every step, so the surviving index is the lane number). OP: 0 = max, 1 = sum.
+template <int OP>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step;
+        const int w = 32 >> (step + 1);  // values kept after this step
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float keep = upper ? v[j + w] : v[j];
+            const float send = upper ? v[j] : v[j + w];
+            const float got = __shfl_xor_sync(0xffffffffu, send, o);
+            v[j] = OP == 0 ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
 }
 
 }  // namespace
@@ -104,14 +144,14 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
     __shared__ __align__(8) uint64_t b_qraw[2], b_qfull[2], b_qempty[2];
     __shared__ __align__(8) uint64_t b_kfull[kNB], b_kempty[kNB];
     __shared__ __align__(8) uint64_t b_sfull[2], b_sempty[2], b_pfull[2], b_pempty[2];
-    __shared__ __align__(8) uint64_t b_ofull, b_oempty;
+    __shared__ __align__(8) uint64_t b_ofull[2], b_oempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ TokenMeta meta[2];
-    __shared__ float s_m[kH];          // running max per head (log2 units)
-    __shared__ float s_f[kH];          // rescale factor per head of the current update
-    __shared__ float s_red[4][kH];     // cross-warp reduction scratch
-    __shared__ float s_fo[kH];         // final output factor per head
-    __shared__ int s_cnt[3];           // producer warps' counts of valid top-k entries
+    __shared__ __align__(16) float s_m[kH];   // running max per head (log2 units)
+    __shared__ __align__(16) float s_f[kH];   // rescale factor per head of the current update
+    __shared__ float s_red[8][32];            // cross-warp reduction scratch
+    __shared__ __align__(16) float s_fo[kH];  // final output factor per head
+    __shared__ int s_cnt[4];                  // producer warps' counts of valid top-k entries
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t s_base = smem_u32(sm);
@@ -126,19 +166,19 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             mbar_init(smem_u32(&b_qraw[i]), 1);
             mbar_init(smem_u32(&b_qfull[i]), kProducers);
             // query slot free: the last S^T MMA of its token is done (commit) and the softmax
-            // group has copied the token's metadata (128 arrivals)
+            // threads have copied the token's metadata
             mbar_init(smem_u32(&b_qempty[i]), 1 + kSoftmax);
             mbar_init(smem_u32(&b_sfull[i]), 1);
             mbar_init(smem_u32(&b_sempty[i]), kSoftmax);
             mbar_init(smem_u32(&b_pfull[i]), kSoftmax);
             mbar_init(smem_u32(&b_pempty[i]), 1);
+            mbar_init(smem_u32(&b_ofull[i]), 1);
+            mbar_init(smem_u32(&b_oempty[i]), kSoftmax);
         }
         for (int i = 0; i < kNB; ++i) {
             mbar_init(smem_u32(&b_kfull[i]), kProducers);
             mbar_init(smem_u32(&b_kempty[i]), 1);
         }
-        mbar_init(smem_u32(&b_ofull), 1);
-        mbar_init(smem_u32(&b_oempty), kSoftmax);
         mbar_fence_init();
     }
     tc_fence_before();
@@ -170,10 +210,13 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             tma_load_3d(s_base + kQOff + qs2 * 16384 + 8192, &P.mq, qb, 64, row2 * kH, 0);
         };
         int fetched = 0;  // tokens whose fetch has been issued
+        int landed = 0;   // tokens whose fetch has been waited for
         if (ptid == 0 && n_tok_cta > 0) {
             fetch(0);
             fetched = 1;
         }
+        const int key_i0 = ptid >> 4, ch = ptid & 15;  // this thread: chunk ch of keys key_i0 + 8q
+        const uint32_t ch_off = (ch >> 3) * 16384;
         for (int it = 0; it < n_tok_cta && ok; ++it) {
             const int row = (int)blockIdx.x + it * (int)gridDim.x;
             const int qs = it & 1;
@@ -201,26 +244,33 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 t = row % P.L;
             }
             const bool pos_ok = t >= 0 && t < P.L;
+            if (!pos_ok && ptid == 0) set_status(CSA_ERR_BOUNDS);
             if (!pwait(smem_u32(&b_qraw[qs]), (it >> 1) & 1)) { ok = false; break; }
+            landed = it + 1;
             // count the valid prefix of the top-k row (ascending, -1 padded) in parallel
-            int32_t *sidx = reinterpret_cast<int32_t *>(sm + kIdxOff) + qs * kMaxTopk;
+            const int32_t *sidx = reinterpret_cast<const int32_t *>(sm + kIdxOff) + qs * kMaxTopk;
             int cnt = 0;
             for (int i = ptid; i < P.topk; i += kProducers) cnt += (pos_ok && sidx[i] >= 0) ? 1 : 0;
             cnt = __reduce_add_sync(0xffffffffu, cnt);
-            if ((ptid & 31) == 0) s_cnt[(tid - kProd0) >> 5] = cnt;
+            if ((ptid & 31) == 0) s_cnt[ptid >> 5] = cnt;
             named_sync(kBarProd, kProducers);
             TokenMeta mt;
-            mt.n_sel = s_cnt[0] + s_cnt[1] + s_cnt[2];
+            mt.n_sel = s_cnt[0] + s_cnt[1] + s_cnt[2] + s_cnt[3];
             mt.n_ct = (mt.n_sel + kTile - 1) / kTile;
             mt.t = t;
             mt.b = b;
             mt.n_win_t = pos_ok ? min(P.n_win, t + 1) : 0;
+            mt.pos_ok = pos_ok;
             if (ptid == 0) meta[qs] = mt;
             // RoPE on dims 64..127 at position t: head h, chunk pair (c, c+4) of the second half
             if (P.d_rope == 64 && pos_ok) {
                 uint8_t *q1 = sm + kQOff + qs * 16384 + 8192;
                 for (int u = ptid; u < kH * 4; u += kProducers) {
                     const int h = u >> 2, c = u & 3;
+                    const float4 *rp = reinterpret_cast<const float4 *>(P.rope + (int64_t)t * 32 + 8 * c);
+                    float4 rc[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) rc[e] = __ldg(rp + e);  // (cos, sin) of pairs 8c .. 8c+7
                     uint4 *pa = reinterpret_cast<uint4 *>(q1 + sw128_off(h, c));
                     uint4 *pb = reinterpret_cast<uint4 *>(q1 + sw128_off(h, c + 4));
                     uint4 va = *pa, vb = *pb;
@@ -230,10 +280,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     for (int e = 0; e < 4; ++e) {
                         const float2 x = __bfloat1622float2(a2[e]);
                         const float2 y = __bfloat1622float2(b2[e]);
-                        const float2 c0 = P.rope[(int64_t)t * 32 + 8 * c + 2 * e];
-                        const float2 c1 = P.rope[(int64_t)t * 32 + 8 * c + 2 * e + 1];
-                        a2[e] = __floats2bfloat162_rn(x.x * c0.x - y.x * c0.y, x.y * c1.x - y.y * c1.y);
-                        b2[e] = __floats2bfloat162_rn(x.x * c0.y + y.x * c0.x, x.y * c1.y + y.y * c1.x);
+                        const float4 cs = rc[e];  // (cos, sin) of pair 8c + 2e and 8c + 2e + 1
+                        a2[e] = __floats2bfloat162_rn(x.x * cs.x - y.x * cs.y, x.y * cs.z - y.y * cs.w);
+                        b2[e] = __floats2bfloat162_rn(x.x * cs.y + y.x * cs.x, x.y * cs.w + y.y * cs.z);
                     }
                     *pa = va;
                     *pb = vb;
@@ -252,10 +301,11 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 uint8_t *kbuf = sm + kKOff + kb * 32768;
                 const uint32_t kbuf_s = s_base + kKOff + kb * 32768;
                 if (c < mt.n_ct) {
-                    for (int u = ptid; u < kTile * 16; u += kProducers) {
-                        const int i = u >> 4, ch = u & 15;
+#pragma unroll 4
+                    for (int q = 0; q < kTile / 8; ++q) {
+                        const int i = key_i0 + 8 * q;
                         const int pos = c * kTile + i;
-                        const uint32_t off = (ch >> 3) * 16384 + sw128_off(i, ch & 7);
+                        const uint32_t off = ch_off + sw128_off(i, ch & 7);
                         int j = pos < mt.n_sel ? sidx[pos] : -1;
                         if (j >= P.ncap) {
                             set_status(CSA_ERR_BOUNDS);
@@ -277,13 +327,13 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                             const uint32_t cw[2] = {codes.x, codes.y};
                             uint32_t pk[4];
 #pragma unroll
-                            for (int q = 0; q < 2; ++q)
+                            for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                                 for (int e = 0; e < 2; ++e) {
-                                    const uint16_t two = (uint16_t)(cw[q] >> (16 * e));
+                                    const uint16_t two = (uint16_t)(cw[h2] >> (16 * e));
                                     __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
                                     const float2 f = __half22float2(__half2(hr));
-                                    pk[2 * q + e] = pack2(f.x * sc, f.y * sc);
+                                    pk[2 * h2 + e] = pack2(f.x * sc, f.y * sc);
                                 }
                             *reinterpret_cast<uint4 *>(kbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
@@ -298,9 +348,10 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     }
                 } else {
                     // decode: window rows from the ring, row u at slot u mod n_win
-                    for (int u = ptid; u < kTile * 16; u += kProducers) {
-                        const int i = u >> 4, ch = u & 15;
-                        const uint32_t off = (ch >> 3) * 16384 + sw128_off(i, ch & 7);
+#pragma unroll 4
+                    for (int q = 0; q < kTile / 8; ++q) {
+                        const int i = key_i0 + 8 * q;
+                        const uint32_t off = ch_off + sw128_off(i, ch & 7);
                         const int uu = mt.t - kTile + 1 + i;  // position of key row i
                         if (uu < 0 || uu <= mt.t - mt.n_win_t) {
                             *reinterpret_cast<uint4 *>(kbuf + off) = make_uint4(0, 0, 0, 0);
@@ -329,42 +380,44 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             fence_async_smem();
             mbar_arrive(smem_u32(&b_kfull[pending % kNB]));
         }
+        // after a failure: let copies still in flight into this CTA's shared memory land
+        // (bounded) before the CTA exits
+        if (!ok && ptid == 0)
+            for (int f = landed; f < fetched; ++f) mbar_wait(smem_u32(&b_qraw[f & 1]), (f >> 1) & 1, 1u << 16);
     } else if (warp == kMmaWarp) {
         // =============================== MMA issue ===============================
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16(128, kH, 0, 0);  // S^T = K Q^T
             const uint32_t idesc_o = idesc_bf16(128, kH, 1, 1);  // O^T = V^T P^T, both MN-major
             int n = 0;
-            int prev_n = -1, prev_first = 0, prev_last = 0;  // the item whose P V is still to issue
-            auto issue_pv = [&](int pn, bool first, bool last, int tok_it) -> bool {
-                const int ps = pn & 1;
-                if (!mbar_wait(smem_u32(&b_pfull[ps]), (pn >> 1) & 1, kMaxPolls, &g_abort)) return false;
-                if (first && tok_it >= 1 &&
-                    !mbar_wait(smem_u32(&b_oempty), (tok_it - 1) & 1, kMaxPolls, &g_abort))
+            int prev_n = -1, prev_first = 0, prev_last = 0, prev_tok = 0;  // the item whose P V is still to issue
+            auto issue_pv = [&](int pn, bool first, bool last, int tok) -> bool {
+                const int pb = pn & 1, ob = tok & 1;
+                if (!mbar_wait(smem_u32(&b_pfull[pb]), (pn >> 1) & 1, kMaxPolls, &g_abort)) return false;
+                if (first && tok >= 2 && !mbar_wait(smem_u32(&b_oempty[ob]), ((tok >> 1) - 1) & 1, kMaxPolls, &g_abort))
                     return false;
                 tc_fence_after();
                 const uint32_t kb = s_base + kKOff + (pn % kNB) * 32768;
-                const uint32_t pb = s_base + kPOff + ps * 16384;
+                const uint32_t pbuf = s_base + kPOff + pb * 16384;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);  // V^T, M = dims
-                    const uint64_t bd = sdesc_sw128(pb + kk * 2048, 16384, 1024);  // P^T, N = heads
-                    mma_bf16(tmem + kOCol, ad, bd, idesc_o, (!first || kk > 0) ? 1u : 0u);
+                    const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);    // V^T, M = dims
+                    const uint64_t bd = sdesc_sw128(pbuf + kk * 2048, 16384, 1024);  // P^T, N = heads
+                    mma_bf16(tmem + kOCol + ob * kH, ad, bd, idesc_o, (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(smem_u32(&b_pempty[ps]));
+                mma_commit(smem_u32(&b_pempty[pb]));
                 mma_commit(smem_u32(&b_kempty[pn % kNB]));
-                if (last) mma_commit(smem_u32(&b_ofull));
+                if (last) mma_commit(smem_u32(&b_ofull[ob]));
                 return true;
             };
-            int prev_tok_it = 0;
             for (int it = 0; it < n_tok_cta && ok; ++it) {
                 const int qs = it & 1;
                 if (!mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
                 const int n_tiles = meta[qs].n_ct + 1;
                 for (int c = 0; c < n_tiles; ++c, ++n) {
-                    const int kb = n % kNB, ss = n & 1;
+                    const int kb = n % kNB, sb = n & 1;
                     if (!mbar_wait(smem_u32(&b_kfull[kb]), (n / kNB) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
-                    if (n >= 2 && !mbar_wait(smem_u32(&b_sempty[ss]), ((n >> 1) - 1) & 1, kMaxPolls, &g_abort)) {
+                    if (n >= 2 && !mbar_wait(smem_u32(&b_sempty[sb]), ((n >> 1) - 1) & 1, kMaxPolls, &g_abort)) {
                         ok = false;
                         break;
                     }
@@ -375,247 +428,269 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t ad = sdesc_sw128(kbuf + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(qbuf + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                        mma_bf16(tmem + kSCol + ss * 64, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                        mma_bf16(tmem + kSCol + sb * kH, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(smem_u32(&b_sfull[ss]));
+                    mma_commit(smem_u32(&b_sfull[sb]));
                     if (c == n_tiles - 1) mma_commit(smem_u32(&b_qempty[qs]));
-                    if (prev_n >= 0 && !issue_pv(prev_n, prev_first, prev_last, prev_tok_it)) { ok = false; break; }
+                    if (prev_n >= 0 && !issue_pv(prev_n, prev_first, prev_last, prev_tok)) { ok = false; break; }
                     prev_n = n;
                     prev_first = c == 0;
                     prev_last = c == n_tiles - 1;
-                    prev_tok_it = it;
+                    prev_tok = it;
                 }
             }
-            if (ok && prev_n >= 0) ok = issue_pv(prev_n, prev_first, prev_last, prev_tok_it);
+            if (ok && prev_n >= 0) ok = issue_pv(prev_n, prev_first, prev_last, prev_tok);
             if (!ok) set_timeout();
         }
-    } else if (warp < 4) {
+    } else {
         // ============================ softmax + epilogue ============================
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        // group-uniform wait (see the producers)
-        auto swait = [&](uint32_t bar, uint32_t par) -> bool {
-            const bool w = mbar_wait(bar, par, kMaxPolls, &g_abort);
-            return !named_sync_or(kBarSoftmax, kSoftmax, !w);
-        };
-        float lpart[kH];
+        const int wg = warp >> 2;                 // warpgroup: heads [32 wg, 32 wg + 32)
+        const int kl = 32 * (warp & 3) + lane;    // this thread's key (TMEM lane) / output dim
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t bar_wg = kBarWG0 + wg;
+        const int h0 = 32 * wg;
+        // Every wait result is kept in okl and acted upon only through an OR-reduction over all
+        // softmax threads, so that all of them leave together and no named barrier is ever left
+        // short of threads.
+        bool okl = true;
+        auto note = [&](bool w) { okl = okl && w; };
+        float lpart[32];
         int n = 0;
-        for (int it = 0; it < n_tok_cta && ok; ++it) {
-            const int qs = it & 1;
-            if (!swait(smem_u32(&b_qfull[qs]), (it >> 1) & 1)) { ok = false; break; }
+        for (int it = 0; it < n_tok_cta; ++it) {
+            const int qs = it & 1, ob = it & 1;
+            note(mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kMaxPolls, &g_abort));
+            if (tid < kH) s_m[tid] = -INFINITY;
+            if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
             const TokenMeta mt = meta[qs];
             mbar_arrive(smem_u32(&b_qempty[qs]));
             const int n_tiles = mt.n_ct + 1;
-            for (int h = tid; h < kH; h += kSoftmax) s_m[h] = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < kH; ++h) lpart[h] = 0.0f;
-            named_sync(kBarSoftmax, kSoftmax);
+            for (int e = 0; e < 32; ++e) lpart[e] = 0.0f;
+            bool failed = false;
             for (int c = 0; c < n_tiles; ++c, ++n) {
-                const int ss = n & 1;
-                if (!swait(smem_u32(&b_sfull[ss]), (n >> 1) & 1)) { ok = false; break; }
+                const int sb = n & 1, pb = n & 1;
+                note(mbar_wait(smem_u32(&b_sfull[sb]), (n >> 1) & 1, kMaxPolls, &g_abort));
                 tc_fence_after();
+                float s[32];
+                tmem_ld32_sync(tmem + lane_base + kSCol + sb * kH + h0, s);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&b_sempty[sb]));
                 // key validity of this thread's key (TMEM lane = key within the tile)
                 bool valid;
-                if (c < mt.n_ct) valid = c * kTile + tid < mt.n_sel;
-                else valid = tid >= kTile - mt.n_win_t;  // key row tid is position t - 127 + tid
-                float s[kH];
+                if (c < mt.n_ct) valid = c * kTile + kl < mt.n_sel;
+                else valid = kl >= kTile - mt.n_win_t;  // key row kl is position t - 127 + kl
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[e] = valid ? s[e] * P.scale_log2 : -INFINITY;
+                float p[32];
+                bool over = false;
                 {
+                    const float4 *m4 = reinterpret_cast<const float4 *>(s_m + h0);
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 mm = m4[e4];
+                        const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float x = s[4 * e4 + q] - mv[q];
+                            over |= x > kOver;
+                            p[4 * e4 + q] = fast_exp2(x);
+                        }
+                    }
+                }
+                if (n >= 2) note(mbar_wait(smem_u32(&b_pempty[pb]), ((n >> 1) - 1) & 1, kMaxPolls, &g_abort));
+                if (named_sync_or(kBarSoftmax, kSoftmax, over || !okl)) {
+                    // rare: a first tile, a jump of the maximum, or a failed wait
+                    if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) { failed = true; break; }
+                    over = true;
+                } else {
+                    over = false;
+                }
+                if (over) {
+                    // per-head maximum of this tile over the warpgroup's 128 keys
                     float v[32];
-                    tmem_ld32_sync(tmem + lane_base + kSCol + ss * 64, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[e] = valid ? v[e] * P.scale_log2 : -INFINITY;
-                    tmem_ld32_sync(tmem + lane_base + kSCol + ss * 64 + 32, v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[32 + e] = valid ? v[e] * P.scale_log2 : -INFINITY;
-                }
-                tc_fence_before();
-                mbar_arrive(smem_u32(&b_sempty[ss]));
-                // lazy max: reduce across the 128 keys only if some logit jumps the current max
-                bool need = false;
-#pragma unroll
-                for (int h = 0; h < kH; ++h) need |= s[h] > s_m[h] + kRescaleThreshold;
-                need = named_sync_or(kBarSoftmax, kSoftmax, need);
-                if (need) {
-                    // warp butterfly: after 5 steps lane holds the max of 2 heads over its warp
-                    float v[kH];
-#pragma unroll
-                    for (int h = 0; h < kH; ++h) v[h] = s[h];
-#pragma unroll
-                    for (int step = 0; step < 5; ++step) {
-                        const int o = 16 >> step;
-                        const int w = kH >> (step + 1);  // values kept after this step
-                        const bool upper = (lane & o) != 0;
-#pragma unroll
-                        for (int j = 0; j < w; ++j) {
-                            const float keep = upper ? v[j + w] : v[j];
-                            const float send = upper ? v[j] : v[j + w];
-                            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
-                        }
-                    }
-                    // lane's heads: base = 32*b4 + 16*b3 + 8*b2 + 4*b1 + 2*b0
-                    const int hb = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 +
-                                   ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
-                    s_red[warp][hb] = v[0];
-                    s_red[warp][hb + 1] = v[1];
-                    named_sync(kBarSoftmax, kSoftmax);
-                    if (tid < kH) {
-                        const float mnew = fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid]));
-                        const float mold = s_m[tid];
+                    for (int e = 0; e < 32; ++e) v[e] = s[e];
+                    const float wmax = warp_transpose_reduce<0>(v, lane);
+                    s_red[warp][lane] = wmax;
+                    named_sync(bar_wg, 128);
+                    if ((warp & 3) == 0) {
+                        const int h = h0 + lane;
+                        const float mnew = fmaxf(fmaxf(s_red[4 * wg][lane], s_red[4 * wg + 1][lane]),
+                                                 fmaxf(s_red[4 * wg + 2][lane], s_red[4 * wg + 3][lane]));
+                        const float mold = s_m[h];
                         float f = 1.0f;
-                        if (mnew > mold + kRescaleThreshold) {
+                        if (mnew > mold + kOver) {
                             f = exp2f(mold - mnew);  // 0 when mold is -inf
-                            s_m[tid] = mnew;
+                            s_m[h] = mnew;
                         }
-                        s_f[tid] = f;
+                        s_f[h] = f;
                     }
-                    named_sync(kBarSoftmax, kSoftmax);
-#pragma unroll
-                    for (int h = 0; h < kH; ++h) lpart[h] *= s_f[h];
+                    named_sync(bar_wg, 128);
                     bool rescale_o = false;
-                    if (c > 0) {
 #pragma unroll
-                        for (int h = 0; h < kH; ++h) rescale_o |= s_f[h] != 1.0f;
+                    for (int e = 0; e < 32; ++e) {
+                        const float f = s_f[h0 + e];
+                        lpart[e] *= f;
+                        rescale_o |= f != 1.0f;
                     }
-                    rescale_o = named_sync_or(kBarSoftmax, kSoftmax, rescale_o);
+                    rescale_o = c > 0 && named_sync_or(bar_wg, 128, rescale_o);
                     if (rescale_o) {
-                        // O^T holds the P V of the previous tile of this token: wait for it
-                        const int pn = n - 1;
-                        if (!swait(smem_u32(&b_pempty[pn & 1]), (pn >> 1) & 1)) {
-                            ok = false;
-                            break;
-                        }
+                        // O^T holds the P V of the previous tiles of this token: wait for the last
+                        note(mbar_wait(smem_u32(&b_pempty[(n - 1) & 1]), ((n - 1) >> 1) & 1, kMaxPolls, &g_abort));
                         tc_fence_after();
-                        for (int c0 = 0; c0 < kH; c0 += 32) {
-                            float o[32];
-                            tmem_ld32_sync(tmem + lane_base + kOCol + c0, o);
-                            float o1[16], o2[16];
+                        float o[32];
+                        tmem_ld32_sync(tmem + lane_base + kOCol + ob * kH + h0, o);
+                        float o1[16], o2[16];
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                o1[e] = o[e] * s_f[c0 + e];
-                                o2[e] = o[16 + e] * s_f[c0 + 16 + e];
-                            }
-                            tmem_st16(tmem + lane_base + kOCol + c0, o1);
-                            tmem_st16(tmem + lane_base + kOCol + c0 + 16, o2);
+                        for (int e = 0; e < 16; ++e) {
+                            o1[e] = o[e] * s_f[h0 + e];
+                            o2[e] = o[16 + e] * s_f[h0 + 16 + e];
                         }
+                        tmem_st16(tmem + lane_base + kOCol + ob * kH + h0, o1);
+                        tmem_st16(tmem + lane_base + kOCol + ob * kH + h0 + 16, o2);
                         tmem_st_wait();
+                        tc_fence_before();
+                    }
+                    const float4 *m4 = reinterpret_cast<const float4 *>(s_m + h0);
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 mm = m4[e4];
+                        const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) p[4 * e4 + q] = fast_exp2(s[4 * e4 + q] - mv[q]);
                     }
                 }
-                // P^T row of this key: exp2(s - m) for the 64 heads, BF16
-                const int ps = n & 1;
-                if (n >= 2 && !swait(smem_u32(&b_pempty[ps]), ((n >> 1) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *prow = sm + kPOff + ps * 16384;
+                // P^T row of this key: chunks 4 wg .. 4 wg + 3 (heads h0 .. h0 + 31), BF16
+                uint8_t *prow = sm + kPOff + pb * 16384;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int h = ch * 8 + 2 * e;
-                        const float p0 = s[h] == -INFINITY ? 0.0f : fast_exp2(s[h] - s_m[h]);
-                        const float p1 = s[h + 1] == -INFINITY ? 0.0f : fast_exp2(s[h + 1] - s_m[h + 1]);
-                        lpart[h] += p0;
-                        lpart[h + 1] += p1;
-                        pk[e] = pack2(p0, p1);
+                        const int h = 8 * c4 + 2 * e;
+                        lpart[h] += p[h];
+                        lpart[h + 1] += p[h + 1];
+                        pk[e] = pack2(p[h], p[h + 1]);
                     }
-                    *reinterpret_cast<uint4 *>(prow + sw128_off(tid, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(prow + sw128_off(kl, 4 * wg + c4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 fence_async_smem();
                 tc_fence_before();
-                mbar_arrive(smem_u32(&b_pfull[ps]));
+                mbar_arrive(smem_u32(&b_pfull[pb]));
             }
-            if (!ok) break;
+            if (failed) break;
             // ---- epilogue of the token: reduce the sums, normalise, inverse RoPE, store ----
             {
-                float v[kH];
-#pragma unroll
-                for (int h = 0; h < kH; ++h) v[h] = lpart[h];
-#pragma unroll
-                for (int step = 0; step < 5; ++step) {
-                    const int o = 16 >> step;
-                    const int w = kH >> (step + 1);
-                    const bool upper = (lane & o) != 0;
-#pragma unroll
-                    for (int j = 0; j < w; ++j) {
-                        const float keep = upper ? v[j + w] : v[j];
-                        const float send = upper ? v[j] : v[j + w];
-                        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                    }
-                }
-                const int hb = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 +
-                               ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
-                s_red[warp][hb] = v[0];
-                s_red[warp][hb + 1] = v[1];
+                const float lsum = warp_transpose_reduce<1>(lpart, lane);
+                s_red[warp][lane] = lsum;
             }
-            named_sync(kBarSoftmax, kSoftmax);
-            if (tid < kH) {
-                const float l = (s_red[0][tid] + s_red[1][tid]) + (s_red[2][tid] + s_red[3][tid]);
-                const float m = s_m[tid];
+            named_sync(bar_wg, 128);
+            if ((warp & 3) == 0) {
+                const int h = h0 + lane;
+                const float l = (s_red[4 * wg][lane] + s_red[4 * wg + 1][lane]) +
+                                (s_red[4 * wg + 2][lane] + s_red[4 * wg + 3][lane]);
+                const float m = s_m[h];
                 float f;
                 if (P.sink) {
-                    const float s2 = P.sink[tid] * 1.4426950408889634f;
+                    const float s2 = P.sink[h] * 1.4426950408889634f;
                     const float mf = fmaxf(m, s2);
                     f = exp2f(m - mf) / (l * exp2f(m - mf) + exp2f(s2 - mf));
                 } else {
                     f = 1.0f / l;
                 }
-                s_fo[tid] = f;
-                if (P.lse && mt.t >= 0 && mt.t < P.L)
-                    P.lse[(int64_t)((P.decode ? mt.b : mt.b * P.L + mt.t)) * kH + tid] = (m + log2f(l)) * 0.6931471805599453f;
+                s_fo[h] = f;
+                if (P.lse && mt.pos_ok)
+                    P.lse[(int64_t)((P.decode ? mt.b : (int64_t)mt.b * P.L + mt.t)) * kH + h] =
+                        (m + log2f(l)) * 0.6931471805599453f;
             }
-            if (!swait(smem_u32(&b_ofull), it & 1)) { ok = false; break; }
+            note(mbar_wait(smem_u32(&b_ofull[ob]), (it >> 1) & 1, kMaxPolls, &g_abort));
+            if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
             tc_fence_after();
-            named_sync(kBarSoftmax, kSoftmax);
-            float *os = reinterpret_cast<float *>(sm + kOsOff);  // [h][d]
-            {
-                float o[32];
-                tmem_ld32_sync(tmem + lane_base + kOCol, o);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) os[e * 128 + tid] = o[e] * s_fo[e];
-                tmem_ld32_sync(tmem + lane_base + kOCol + 32, o);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) os[(32 + e) * 128 + tid] = o[e] * s_fo[32 + e];
-            }
+            float o[32];
+            tmem_ld32_sync(tmem + lane_base + kOCol + ob * kH + h0, o);  // lane kl = output dim
             tc_fence_before();
-            mbar_arrive(smem_u32(&b_oempty));
-            named_sync(kBarSoftmax, kSoftmax);
-            if (mt.t >= 0 && mt.t < P.L) {
-                const int64_t orow = P.decode ? (int64_t)mt.b : (int64_t)mt.b * P.L + mt.t;
-                __nv_bfloat16 *out = P.out + orow * kH * 128;
-                // thread tid always handles dims [8q, 8q+8), q = tid & 15, of heads (tid >> 4) + 8k,
-                // so its RoPE factors are fetched once
-                const int q = tid & 15;
-                const bool rot = P.d_rope == 64 && q >= 8;
-                const int i0 = 8 * ((q - 8) & 3);
-                float2 cs[8];
+            mbar_arrive(smem_u32(&b_oempty[ob]));
+            {
+                const float4 *f4 = reinterpret_cast<const float4 *>(s_fo + h0);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) cs[e] = rot ? P.rope[(int64_t)mt.t * 32 + i0 + e] : make_float2(1.0f, 0.0f);
-#pragma unroll
-                for (int k = 0; k < kH / 8; ++k) {
-                    const int h = (tid >> 4) + 8 * k;
-                    const float *src = os + h * 128;
-                    float y[8];
-                    if (!rot) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) y[e] = src[8 * q + e];
-                    } else if (q < 12) {  // dims 64 + i, partner 96 + i
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) y[e] = src[64 + i0 + e] * cs[e].x + src[96 + i0 + e] * cs[e].y;
-                    } else {  // dims 96 + i
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) y[e] = -src[64 + i0 + e] * cs[e].y + src[96 + i0 + e] * cs[e].x;
-                    }
-                    *reinterpret_cast<uint4 *>(out + h * 128 + 8 * q) =
-                        make_uint4(pack2(y[0], y[1]), pack2(y[2], y[3]), pack2(y[4], y[5]), pack2(y[6], y[7]));
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 ff = f4[e4];
+                    o[4 * e4] *= ff.x;
+                    o[4 * e4 + 1] *= ff.y;
+                    o[4 * e4 + 2] *= ff.z;
+                    o[4 * e4 + 3] *= ff.w;
                 }
             }
+            if (P.d_rope == 64 && kl >= 64) {
+                // dims 64 + i (warp 2) and 96 + i (warp 3) of a pair meet in shared memory
+                const int half = (kl >> 5) & 1, i = kl & 31;
+                float *x = reinterpret_cast<float *>(sm + kXOff) + wg * 2048;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[half * 1024 + e * 32 + i] = o[e];
+                named_sync(kBarWG0 + 2 + wg, 64);  // warps 2 and 3 of this warpgroup
+                const float2 cs = mt.pos_ok ? P.rope[(int64_t)mt.t * 32 + i] : make_float2(1.0f, 0.0f);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float other = x[(half ^ 1) * 1024 + e * 32 + i];
+                    o[e] = half == 0 ? o[e] * cs.x + other * cs.y : -other * cs.y + o[e] * cs.x;
+                }
+            }
+            // staging buffer: the previous token's bulk store must have finished reading it
+            if (tid == 0) bulk_wait_read_all();
             named_sync(kBarSoftmax, kSoftmax);
+            {
+                __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + kOutOff);  // [h][d]
+#pragma unroll
+                for (int e = 0; e < 32; ++e) os[(h0 + e) * 128 + kl] = __float2bfloat16_rn(o[e]);
+            }
+            fence_async_smem();
+            named_sync(kBarSoftmax, kSoftmax);
+            if (tid == 0 && mt.pos_ok) {
+                const int64_t orow = P.decode ? (int64_t)mt.b : (int64_t)mt.b * P.L + mt.t;
+                bulk_store(P.out + orow * kH * 128, s_base + kOutOff, kH * 128 * 2);
+            }
         }
-        if (!ok && tid == 0) set_timeout();
+        if (tid == 0) bulk_wait_all();
+        if (!okl) set_timeout();
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Mixed-precision entries widened to BF16 rows: dims [0, 64) = code * row scale (rounded to
+// nearest even), dims [64, 128) copied. Thread = one 16-byte output chunk.
+__global__ void widen_mixed_kernel(const uint8_t *__restrict__ codes, const __nv_bfloat16 *__restrict__ rope,
+                                   const float *__restrict__ scale, int64_t rows, __nv_bfloat16 *__restrict__ out) {
+    const int64_t n = rows * 16;
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < n; u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = u >> 4;
+        const int ch = (int)(u & 15);
+        uint4 v;
+        if (ch >= 8) {
+            v = *reinterpret_cast<const uint4 *>(rope + r * 64 + (ch - 8) * 8);
+        } else {
+            const uint2 cw = *reinterpret_cast<const uint2 *>(codes + r * 64 + ch * 8);
+            const float sc = scale[r];
+            const uint32_t w2[2] = {cw.x, cw.y};
+            uint32_t pk[4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint16_t two = (uint16_t)(w2[h2] >> (16 * e));
+                    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+                    const float2 f = __half22float2(__half2(hr));
+                    pk[2 * h2 + e] = pack2(f.x * sc, f.y * sc);
+                }
+            v = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        *reinterpret_cast<uint4 *>(out + r * 128 + ch * 8) = v;
+    }
+}
+
+size_t csa_widen_bytes(const AttnArgs &a) {
+    return (a.kv_t == CSA_MIXED && !a.decode) ? (size_t)a.B * (size_t)a.ncap * 128 * 2 : 0;
 }
 
 bool csa_tc_supported(const AttnArgs &a) {
@@ -623,8 +698,10 @@ bool csa_tc_supported(const AttnArgs &a) {
     if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED) return false;
     if (a.H != csa_tc::kH || a.n_win != 128 || a.topk < 4 || a.topk > kMaxTopk || a.topk % 4 != 0) return false;
     if (a.d_rope != 0 && a.d_rope != 64) return false;
-    // top-k rows are fetched with a bulk copy: 16-byte aligned rows
-    return a.idx != nullptr && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0;
+    if (csa_widen_bytes(a) > a.ws_bytes || (csa_widen_bytes(a) > 0 && !a.ws)) return false;
+    // top-k rows are fetched with a bulk copy and outputs stored with one: 16-byte aligned
+    return a.idx != nullptr && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 &&
+           (reinterpret_cast<uintptr_t>(a.out) & 15) == 0;
 }
 
 bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
@@ -642,6 +719,23 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.c_data = a.c_data;
     P.c_rope = reinterpret_cast<const __nv_bfloat16 *>(a.c_rope);
     P.c_scale = a.c_scale;
+    P.mixed = a.kv_t == CSA_MIXED;
+    if (P.mixed && !a.decode) {
+        // widen every entry once; the attention then gathers BF16 rows
+        const int64_t erows = (int64_t)a.B * a.ncap;
+        __nv_bfloat16 *wide = reinterpret_cast<__nv_bfloat16 *>(a.ws);
+        int blocks = (int)ceil_div64(erows * 16, 256);
+        if (blocks > 148 * 8) blocks = 148 * 8;
+        if (blocks < 1) blocks = 1;
+        widen_mixed_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint8_t *>(a.c_data),
+                                                  reinterpret_cast<const __nv_bfloat16 *>(a.c_rope), a.c_scale, erows,
+                                                  wide);
+        count_launches(1);
+        P.c_data = wide;
+        P.c_rope = nullptr;
+        P.c_scale = nullptr;
+        P.mixed = 0;
+    }
     P.win = a.decode ? reinterpret_cast<const __nv_bfloat16 *>(a.kv_rope) : nullptr;
     P.idx = a.idx;
     P.ctx = a.ctx;
@@ -650,7 +744,7 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
     P.lse = a.lse;
     P.B = a.B; P.L = a.L; P.ncap = a.ncap; P.topk = a.topk; P.n_win = a.n_win; P.d_rope = a.d_rope;
-    P.mixed = a.kv_t == CSA_MIXED; P.decode = a.decode; P.rows = rows;
+    P.decode = a.decode; P.rows = rows;
     P.scale_log2 = a.scale * 1.4426950408889634f;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);

@@ -58,6 +58,8 @@ struct AttnArgs {
     const float *rope_tab; // [rope_len, half, 2]
     void *out;
     float *lse;
+    void *ws;              // prefill with mixed entries: room for the entries widened to BF16
+    size_t ws_bytes;
     int B, L, H, m, topk, n_win, d_rope, ncap;
     float scale;
     int decode, act_t, kv_t;
