@@ -23,10 +23,10 @@
 // and O^T (in TMEM). That happens on a token's first tile and rarely after. Per-head sums are
 // partial per thread and reduced once per token.
 //
-// Warp roles (416 threads, persistent over tokens):
+// Warp roles (384 threads, persistent over tokens):
 //   warps 0-7   softmax and epilogue (two warpgroups; TMEM lanes 0-127 each);
 //   warp 8      MMA issue (one thread);
-//   warps 9-12  producers: query rows by TMA + RoPE, top-k row by bulk copy, key tiles gathered
+//   warps 9-11  producers: query rows by TMA + RoPE, top-k row by bulk copy, key tiles gathered
 //               with cp.async (decode with mixed entries: the FP8 half widened to BF16 by the
 //               threads), the window tile by TMA (prefill) or gathered from the ring (decode).
 // Pipelines: key tiles in a 3-buffer ring, S^T and O^T double-buffered in TMEM (O^T by token),
@@ -49,18 +49,22 @@ namespace csa_tc {
 constexpr int kSoftmax = 256;                 // warps 0-7
 constexpr int kMmaWarp = 8;
 constexpr int kProd0 = 288;                   // first producer thread (warp 9)
-constexpr int kProducers = 128;               // warps 9-12
-constexpr int kThreads = kProd0 + kProducers; // 416
+constexpr int kProducers = 96;                // warps 9-11
+constexpr int kThreads = kProd0 + kProducers; // 384
 constexpr int kH = 64;                        // heads (N of both MMAs)
 constexpr int kTile = 128;                    // keys per tile
-constexpr int kNB = 3;                        // key-tile buffers
-constexpr int kQOff = 0;                      // Q: 2 buffers x 16 KB (two 64-dim halves of 8 KB)
-constexpr int kKOff = 32768;                  // keys: kNB x 32 KB (two 64-dim halves of 16 KB)
-constexpr int kPOff = kKOff + kNB * 32768;    // P^T: 2 x 16 KB
-constexpr int kOutOff = kPOff + 2 * 16384;    // output staging: [64 heads][128 dims] BF16
-constexpr int kXOff = kOutOff + 16384;        // RoPE exchange: [2 WG][2 halves][32 heads][32] float
-constexpr int kIdxOff = kXOff + 16384;        // top-k rows: 2 x kMaxTopk int32
-constexpr int kSmemBytes = kIdxOff + 2 * kMaxTopk * 4 + 1024;
+// Shared memory (1024-aligned), for NB key-tile buffers:
+//   Q       2 buffers x 16 KB (two 64-dim halves of 8 KB)
+//   keys    NB x 32 KB (two 64-dim halves of 16 KB)
+//   P^T     2 x 16 KB; during a token's epilogue buffer 0 also serves as the RoPE exchange
+//           [2 WG][2 halves][32 heads][32] float (every P V of the token has completed then)
+//   output  staging [64 heads][128 dims] BF16, 16 KB
+//   top-k   2 rows of topk int32
+constexpr int kQOff = 0;
+constexpr int kKOff = 32768;
+__host__ __device__ constexpr int p_off(int nb) { return kKOff + nb * 32768; }
+__host__ __device__ constexpr int out_off(int nb) { return p_off(nb) + 2 * 16384; }
+__host__ __device__ constexpr int idx_off(int nb) { return out_off(nb) + 16384; }
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kSCol = 0;                 // S^T slots: [0, 64) and [64, 128)
 constexpr uint32_t kOCol = 128;               // O^T slots: [128, 192) and [192, 256)
@@ -134,10 +138,30 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
     return v[0];
 }
 
+// The same for 16 values: after four halving steps lanes 2i and 2i+1 hold value i over their
+// half of the warp, and one more exchange combines the halves.
+__device__ __forceinline__ float warp_transpose_max16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+        const int o = 16 >> step;
+        const int w = 16 >> (step + 1);
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float keep = upper ? v[j + w] : v[j];
+            const float send = upper ? v[j] : v[j + w];
+            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
+    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+}
+
 }  // namespace
 
+template <int kNB>
 __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __grid_constant__ CsaTcParams P) {
     using namespace csa_tc;
+    constexpr int kPOff = p_off(kNB), kOutOff = out_off(kNB), kIdxOff = idx_off(kNB), kXOff = kPOff;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // mbarriers
@@ -151,7 +175,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
     __shared__ __align__(16) float s_f[kH];   // rescale factor per head of the current update
     __shared__ float s_red[8][32];            // cross-warp reduction scratch
     __shared__ __align__(16) float s_fo[kH];  // final output factor per head
-    __shared__ int s_cnt[4];                  // producer warps' counts of valid top-k entries
+    __shared__ int s_cnt[3];                  // producer warps' counts of valid top-k entries
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t s_base = smem_u32(sm);
@@ -197,7 +221,6 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             return !named_sync_or(kBarProd, kProducers, !w);
         };
         int n = 0;           // global tile item counter
-        int pending = -1;    // item whose k_full arrival is outstanding
         // Fetch of a token's top-k row (bulk copy) and query rows (TMA) into slot it & 1, issued
         // by one thread as early as the slot is free, so it overlaps the previous token.
         auto fetch = [&](int it2) {
@@ -205,7 +228,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             const int qs2 = it2 & 1;
             const uint32_t qb = smem_u32(&b_qraw[qs2]);
             mbar_expect_tx(qb, 2 * kH * 128 + P.topk * 4);
-            bulk_load(s_base + kIdxOff + qs2 * kMaxTopk * 4, P.idx + (int64_t)row2 * P.topk, P.topk * 4, qb);
+            bulk_load(s_base + kIdxOff + qs2 * P.topk * 4, P.idx + (int64_t)row2 * P.topk, P.topk * 4, qb);
             tma_load_3d(s_base + kQOff + qs2 * 16384, &P.mq, qb, 0, row2 * kH, 0);
             tma_load_3d(s_base + kQOff + qs2 * 16384 + 8192, &P.mq, qb, 64, row2 * kH, 0);
         };
@@ -215,18 +238,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             fetch(0);
             fetched = 1;
         }
-        const int key_i0 = ptid >> 4, ch = ptid & 15;  // this thread: chunk ch of keys key_i0 + 8q
-        const uint32_t ch_off = (ch >> 3) * 16384;
         for (int it = 0; it < n_tok_cta && ok; ++it) {
             const int row = (int)blockIdx.x + it * (int)gridDim.x;
             const int qs = it & 1;
-            // flush the previous item before the per-token work
-            if (pending >= 0) {
-                cp_async_wait_all();
-                fence_async_smem();
-                mbar_arrive(smem_u32(&b_kfull[pending % kNB]));
-                pending = -1;
-            }
             if (ptid == 0 && fetched == it) {  // not prefetched: the slot must be free first
                 if (it >= 2 && !mbar_wait(smem_u32(&b_qempty[qs]), ((it >> 1) - 1) & 1, kMaxPolls, &g_abort)) ok = false;
                 if (ok) {
@@ -248,14 +262,14 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             if (!pwait(smem_u32(&b_qraw[qs]), (it >> 1) & 1)) { ok = false; break; }
             landed = it + 1;
             // count the valid prefix of the top-k row (ascending, -1 padded) in parallel
-            const int32_t *sidx = reinterpret_cast<const int32_t *>(sm + kIdxOff) + qs * kMaxTopk;
+            const int32_t *sidx = reinterpret_cast<const int32_t *>(sm + kIdxOff) + qs * P.topk;
             int cnt = 0;
             for (int i = ptid; i < P.topk; i += kProducers) cnt += (pos_ok && sidx[i] >= 0) ? 1 : 0;
             cnt = __reduce_add_sync(0xffffffffu, cnt);
             if ((ptid & 31) == 0) s_cnt[ptid >> 5] = cnt;
             named_sync(kBarProd, kProducers);
             TokenMeta mt;
-            mt.n_sel = s_cnt[0] + s_cnt[1] + s_cnt[2] + s_cnt[3];
+            mt.n_sel = s_cnt[0] + s_cnt[1] + s_cnt[2];
             mt.n_ct = (mt.n_sel + kTile - 1) / kTile;
             mt.t = t;
             mt.b = b;
@@ -300,12 +314,30 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 }
                 uint8_t *kbuf = sm + kKOff + kb * 32768;
                 const uint32_t kbuf_s = s_base + kKOff + kb * 32768;
-                if (c < mt.n_ct) {
-#pragma unroll 4
-                    for (int q = 0; q < kTile / 8; ++q) {
-                        const int i = key_i0 + 8 * q;
+                const uint32_t kf = smem_u32(&b_kfull[kb]);
+                if (c < mt.n_ct && !P.mixed) {
+                    // gathered BF16 rows; an invalid slot reads nothing and is zero-filled (its
+                    // weight is masked to 0 by the softmax)
+                    for (int u = ptid; u < kTile * 16; u += kProducers) {
+                        const int i = u >> 4, ch = u & 15;  // key i of the tile, 16-byte chunk ch
                         const int pos = c * kTile + i;
-                        const uint32_t off = ch_off + sw128_off(i, ch & 7);
+                        int j = pos < mt.n_sel ? sidx[pos] : -1;
+                        if (j >= P.ncap) {
+                            set_status(CSA_ERR_BOUNDS);
+                            j = -1;
+                        }
+                        const int64_t er = (int64_t)mt.b * P.ncap + (j < 0 ? 0 : j);
+                        cp_async16_zfill(kbuf_s + (ch >> 3) * 16384 + sw128_off(i, ch & 7),
+                                         reinterpret_cast<const __nv_bfloat16 *>(P.c_data) + er * 128 + ch * 8,
+                                         j < 0 ? 0u : 16u);
+                    }
+                    cp_async_mbar_arrive(kf);
+                } else if (c < mt.n_ct) {
+                    // decode with mixed entries: the FP8 half is widened by the threads
+                    for (int u = ptid; u < kTile * 16; u += kProducers) {
+                        const int i = u >> 4, ch = u & 15;
+                        const int pos = c * kTile + i;
+                        const uint32_t off = (ch >> 3) * 16384 + sw128_off(i, ch & 7);
                         int j = pos < mt.n_sel ? sidx[pos] : -1;
                         if (j >= P.ncap) {
                             set_status(CSA_ERR_BOUNDS);
@@ -316,9 +348,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                             continue;
                         }
                         const int64_t er = (int64_t)mt.b * P.ncap + j;
-                        if (!P.mixed) {
-                            cp_async16(kbuf_s + off, reinterpret_cast<const __nv_bfloat16 *>(P.c_data) + er * 128 + ch * 8);
-                        } else if (ch >= 8) {
+                        if (ch >= 8) {
                             cp_async16(kbuf_s + off, P.c_rope + er * 64 + (ch - 8) * 8);
                         } else {
                             const uint2 codes = *reinterpret_cast<const uint2 *>(
@@ -338,48 +368,39 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                             *reinterpret_cast<uint4 *>(kbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
                     }
+                    cp_async_wait_all();
+                    fence_async_smem();
+                    mbar_arrive(kf);
                 } else if (!P.decode) {
                     // window rows [t - 127, t] of sequence b by TMA (rows before 0 read as zeros)
                     if (ptid == 0) {
-                        const uint32_t kf = smem_u32(&b_kfull[kb]);
                         mbar_expect_tx_only(kf, 2 * kTile * 128);
                         tma_load_3d(kbuf_s, &P.mkv, kf, 0, mt.t - kTile + 1, mt.b);
                         tma_load_3d(kbuf_s + 16384, &P.mkv, kf, 64, mt.t - kTile + 1, mt.b);
                     }
+                    mbar_arrive(kf);
                 } else {
                     // decode: window rows from the ring, row u at slot u mod n_win
-#pragma unroll 4
-                    for (int q = 0; q < kTile / 8; ++q) {
-                        const int i = key_i0 + 8 * q;
-                        const uint32_t off = ch_off + sw128_off(i, ch & 7);
+                    for (int u = ptid; u < kTile * 16; u += kProducers) {
+                        const int i = u >> 4, ch = u & 15;
                         const int uu = mt.t - kTile + 1 + i;  // position of key row i
-                        if (uu < 0 || uu <= mt.t - mt.n_win_t) {
-                            *reinterpret_cast<uint4 *>(kbuf + off) = make_uint4(0, 0, 0, 0);
-                            continue;
-                        }
-                        cp_async16(kbuf_s + off, P.win + ((int64_t)mt.b * P.n_win + (uu % P.n_win)) * 128 + ch * 8);
+                        const bool have = !(uu < 0 || uu <= mt.t - mt.n_win_t);
+                        const int64_t slot = have ? (uu % P.n_win) : 0;
+                        cp_async16_zfill(kbuf_s + (ch >> 3) * 16384 + sw128_off(i, ch & 7),
+                                         P.win + ((int64_t)mt.b * P.n_win + slot) * 128 + ch * 8, have ? 16u : 0u);
                     }
+                    cp_async_mbar_arrive(kf);
                 }
-                cp_async_commit();
                 // fetch the next token's rows once its slot is free (never blocking here)
                 if (ptid == 0 && fetched == it + 1 && it + 1 < n_tok_cta &&
                     (it + 1 < 2 || mbar_try_wait(smem_u32(&b_qempty[(it + 1) & 1]), (((it + 1) >> 1) - 1) & 1))) {
                     fetch(it + 1);
                     fetched = it + 2;
                 }
-                if (pending >= 0) {
-                    cp_async_wait_1();
-                    fence_async_smem();
-                    mbar_arrive(smem_u32(&b_kfull[pending % kNB]));
-                }
-                pending = n;
             }
         }
-        if (pending >= 0) {
-            cp_async_wait_all();
-            fence_async_smem();
-            mbar_arrive(smem_u32(&b_kfull[pending % kNB]));
-        }
+        // all copies of this thread have landed before the CTA may exit
+        cp_async_wait_all();
         // after a failure: let copies still in flight into this CTA's shared memory land
         // (bounded) before the CTA exits
         if (!ok && ptid == 0)
@@ -421,6 +442,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         ok = false;
                         break;
                     }
+                    // the gathered rows were written by cp.async (generic proxy) and observed through
+                    // the barrier; order them before the tensor core's reads (async proxy)
+                    fence_async_smem();
                     tc_fence_after();
                     const uint32_t kbuf = s_base + kKOff + kb * 32768;
                     const uint32_t qbuf = s_base + kQOff + qs * 16384;
@@ -471,17 +495,15 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 const int sb = n & 1, pb = n & 1;
                 note(mbar_wait(smem_u32(&b_sfull[sb]), (n >> 1) & 1, kMaxPolls, &g_abort));
                 tc_fence_after();
-                float s[32];
-                tmem_ld32_sync(tmem + lane_base + kSCol + sb * kH + h0, s);
-                tc_fence_before();
-                mbar_arrive(smem_u32(&b_sempty[sb]));
+                const uint32_t s_addr = tmem + lane_base + kSCol + sb * kH + h0;
                 // key validity of this thread's key (TMEM lane = key within the tile)
                 bool valid;
                 if (c < mt.n_ct) valid = c * kTile + kl < mt.n_sel;
                 else valid = kl >= kTile - mt.n_win_t;  // key row kl is position t - 127 + kl
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[e] = valid ? s[e] * P.scale_log2 : -INFINITY;
+                // p = exp2(scale * s - m) with the current maxima; the S^T slot stays held until
+                // the P^T row is written, so the rare slow path can read the logits again
                 float p[32];
+                tmem_ld32_sync(s_addr, p);
                 bool over = false;
                 {
                     const float4 *m4 = reinterpret_cast<const float4 *>(s_m + h0);
@@ -491,7 +513,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float x = s[4 * e4 + q] - mv[q];
+                            const float x = valid ? fmaf(p[4 * e4 + q], P.scale_log2, -mv[q]) : -INFINITY;
                             over |= x > kOver;
                             p[4 * e4 + q] = fast_exp2(x);
                         }
@@ -506,12 +528,16 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     over = false;
                 }
                 if (over) {
-                    // per-head maximum of this tile over the warpgroup's 128 keys
-                    float v[32];
+                    // per-head maximum of this tile over the warpgroup's 128 keys, 16 heads at a time
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 32; c0 += 16) {
+                        float v[16];
+                        tmem_ld16_sync(s_addr + c0, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = s[e];
-                    const float wmax = warp_transpose_reduce<0>(v, lane);
-                    s_red[warp][lane] = wmax;
+                        for (int e = 0; e < 16; ++e) v[e] = valid ? v[e] * P.scale_log2 : -INFINITY;
+                        const float wmax = warp_transpose_max16(v, lane);  // head c0 + lane / 2
+                        if ((lane & 1) == 0) s_red[warp][c0 + (lane >> 1)] = wmax;
+                    }
                     named_sync(bar_wg, 128);
                     if ((warp & 3) == 0) {
                         const int h = h0 + lane;
@@ -538,28 +564,30 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         // O^T holds the P V of the previous tiles of this token: wait for the last
                         note(mbar_wait(smem_u32(&b_pempty[(n - 1) & 1]), ((n - 1) >> 1) & 1, kMaxPolls, &g_abort));
                         tc_fence_after();
-                        float o[32];
-                        tmem_ld32_sync(tmem + lane_base + kOCol + ob * kH + h0, o);
-                        float o1[16], o2[16];
+#pragma unroll 1
+                        for (int c0 = 0; c0 < 32; c0 += 16) {
+                            float o[16];
+                            tmem_ld16_sync(tmem + lane_base + kOCol + ob * kH + h0 + c0, o);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            o1[e] = o[e] * s_f[h0 + e];
-                            o2[e] = o[16 + e] * s_f[h0 + 16 + e];
+                            for (int e = 0; e < 16; ++e) o[e] *= s_f[h0 + c0 + e];
+                            tmem_st16(tmem + lane_base + kOCol + ob * kH + h0 + c0, o);
                         }
-                        tmem_st16(tmem + lane_base + kOCol + ob * kH + h0, o1);
-                        tmem_st16(tmem + lane_base + kOCol + ob * kH + h0 + 16, o2);
                         tmem_st_wait();
-                        tc_fence_before();
                     }
+                    tmem_ld32_sync(s_addr, p);
                     const float4 *m4 = reinterpret_cast<const float4 *>(s_m + h0);
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
                         const float4 mm = m4[e4];
                         const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) p[4 * e4 + q] = fast_exp2(s[4 * e4 + q] - mv[q]);
+                        for (int q = 0; q < 4; ++q)
+                            p[4 * e4 + q] = fast_exp2(valid ? fmaf(p[4 * e4 + q], P.scale_log2, -mv[q]) : -INFINITY);
                     }
                 }
+                // the logits are no longer needed: release the S^T slot
+                tc_fence_before();
+                mbar_arrive(smem_u32(&b_sempty[sb]));
                 // P^T row of this key: chunks 4 wg .. 4 wg + 3 (heads h0 .. h0 + 31), BF16
                 uint8_t *prow = sm + kPOff + pb * 16384;
 #pragma unroll
@@ -746,12 +774,22 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.B = a.B; P.L = a.L; P.ncap = a.ncap; P.topk = a.topk; P.n_win = a.n_win; P.d_rope = a.d_rope;
     P.decode = a.decode; P.rows = rows;
     P.scale_log2 = a.scale * 1.4426950408889634f;
-    int dev = 0, sms = 148;
+    int dev = 0, sms = 148, smem_max = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(csa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int grid = rows < sms ? rows : sms;
-    csa_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(P);
+    // four key-tile buffers when they fit next to the top-k rows, else three
+    const int static_bytes = 4096;  // barriers, per-head vectors, reduction scratch (upper bound)
+    const int smem4 = 1024 + idx_off(4) + 2 * a.topk * 4;
+    const int smem3 = 1024 + idx_off(3) + 2 * a.topk * 4;
+    if (smem4 + static_bytes <= smem_max) {
+        cudaFuncSetAttribute(csa_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem4);
+        csa_tc_kernel<4><<<grid, kThreads, smem4, st>>>(P);
+    } else {
+        cudaFuncSetAttribute(csa_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem3);
+        csa_tc_kernel<3><<<grid, kThreads, smem3, st>>>(P);
+    }
     count_launches(1);
     return true;
 }
