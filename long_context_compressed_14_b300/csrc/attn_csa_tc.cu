@@ -53,6 +53,7 @@ constexpr int kProducers = 96;                // warps 9-11
 constexpr int kThreads = kProd0 + kProducers; // 384
 constexpr int kH = 64;                        // heads (N of both MMAs)
 constexpr int kTile = 128;                    // keys per tile
+constexpr int kGatherPer = 22;                // 16-byte chunks of a key tile per producer thread
 // Shared memory (1024-aligned), for NB key-tile buffers:
 //   Q       2 buffers x 16 KB (two 64-dim halves of 8 KB)
 //   keys    NB x 32 KB (two 64-dim halves of 16 KB)
@@ -317,19 +318,33 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 const uint32_t kf = smem_u32(&b_kfull[kb]);
                 if (c < mt.n_ct && !P.mixed) {
                     // gathered BF16 rows; an invalid slot reads nothing and is zero-filled (its
-                    // weight is masked to 0 by the softmax)
-                    for (int u = ptid; u < kTile * 16; u += kProducers) {
-                        const int i = u >> 4, ch = u & 15;  // key i of the tile, 16-byte chunk ch
+                    // weight is masked to 0 by the softmax). 96 threads: thread = chunk ch of keys
+                    // i0 + 6q; all indices are read first so that the copies issue back to back.
+                    static_assert(kProducers == 96 && kTile * 16 <= kProducers * kGatherPer, "gather split");
+                    const int ch = ptid & 15, i0 = ptid >> 4;
+                    int jj[kGatherPer];
+#pragma unroll
+                    for (int q = 0; q < kGatherPer; ++q) {
+                        const int i = i0 + 6 * q;
                         const int pos = c * kTile + i;
-                        int j = pos < mt.n_sel ? sidx[pos] : -1;
+                        int j = (i < kTile && pos < mt.n_sel) ? sidx[pos] : -1;
                         if (j >= P.ncap) {
                             set_status(CSA_ERR_BOUNDS);
                             j = -1;
                         }
-                        const int64_t er = (int64_t)mt.b * P.ncap + (j < 0 ? 0 : j);
-                        cp_async16_zfill(kbuf_s + (ch >> 3) * 16384 + sw128_off(i, ch & 7),
-                                         reinterpret_cast<const __nv_bfloat16 *>(P.c_data) + er * 128 + ch * 8,
-                                         j < 0 ? 0u : 16u);
+                        jj[q] = j;
+                    }
+                    const __nv_bfloat16 *cbase =
+                        reinterpret_cast<const __nv_bfloat16 *>(P.c_data) + (int64_t)mt.b * P.ncap * 128 + ch * 8;
+                    const uint32_t dbase = kbuf_s + (ch >> 3) * 16384;
+#pragma unroll
+                    for (int q = 0; q < kGatherPer; ++q) {
+                        const int i = i0 + 6 * q;
+                        if (i < kTile) {
+                            const int j = jj[q];
+                            cp_async16_zfill(dbase + sw128_off(i, ch & 7), cbase + (int64_t)(j < 0 ? 0 : j) * 128,
+                                             j < 0 ? 0u : 16u);
+                        }
                     }
                     cp_async_mbar_arrive(kf);
                 } else if (c < mt.n_ct) {
