@@ -323,17 +323,16 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     static_assert(kProducers == 96 && kTile * 16 <= kProducers * kGatherPer, "gather split");
                     const int ch = ptid & 15, i0 = ptid >> 4;
                     int jj[kGatherPer];
+                    bool bad = false;
 #pragma unroll
                     for (int q = 0; q < kGatherPer; ++q) {
                         const int i = i0 + 6 * q;
                         const int pos = c * kTile + i;
-                        int j = (i < kTile && pos < mt.n_sel) ? sidx[pos] : -1;
-                        if (j >= P.ncap) {
-                            set_status(CSA_ERR_BOUNDS);
-                            j = -1;
-                        }
-                        jj[q] = j;
+                        const int j = (i < kTile && pos < mt.n_sel) ? sidx[pos] : -1;
+                        bad |= j >= P.ncap;
+                        jj[q] = j >= P.ncap ? -1 : j;
                     }
+                    if (bad) set_status(CSA_ERR_BOUNDS);
                     const __nv_bfloat16 *cbase =
                         reinterpret_cast<const __nv_bfloat16 *>(P.c_data) + (int64_t)mt.b * P.ncap * 128 + ch * 8;
                     const uint32_t dbase = kbuf_s + (ch >> 3) * 16384;
