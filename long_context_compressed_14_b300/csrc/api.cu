@@ -305,15 +305,15 @@ int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope
 int hca_prefill(const csa_params *p, const void *q, const void *kv_rope, const csa_entries *C,
                 const float *sink, const float *rope_tab, void *out, float *lse_out, void *ws,
                 size_t wsb, csa_stream_t stream) {
-    (void)ws;
-    (void)wsb;
     int s = check(p, CSA_OP_HCA_PREFILL);
     if (s) return s;
     if (!q || !kv_rope || !out || !aligned16(q) || !aligned16(kv_rope) || !aligned16(out) ||
         !entries_ok(p, C))
         return CSA_ERR_INVALID;
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
-    AttnArgs a = attn_args(p, q, kv_rope, C, nullptr, nullptr, sink, rope_tab, out, lse_out, 0, 0);
+    const size_t need = ws_bytes(p, CSA_OP_HCA_PREFILL);
+    if (need > 0 && (wsb < need || !ws || !aligned16(ws))) return CSA_ERR_WORKSPACE;
+    AttnArgs a = attn_args(p, q, kv_rope, C, nullptr, nullptr, sink, rope_tab, out, lse_out, 0, 0, ws, wsb);
     if (!launch_hca_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
     return launch_status();
 }

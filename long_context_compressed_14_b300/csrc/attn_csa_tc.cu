@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         // a wait whose outcome is the same for all producer threads (a timeout in one makes
         // them all leave together, so no named barrier is left short of threads)
         auto pwait = [&](uint32_t bar, uint32_t par) -> bool {
-            const bool w = mbar_wait(bar, par, kMaxPolls, &g_abort);
+            const bool w = mbar_wait(bar, par, kWaitNs, &g_abort);
             return !named_sync_or(kBarProd, kProducers, !w);
         };
         int n = 0;           // global tile item counter
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             const int row = (int)blockIdx.x + it * (int)gridDim.x;
             const int qs = it & 1;
             if (ptid == 0 && fetched == it) {  // not prefetched: the slot must be free first
-                if (it >= 2 && !mbar_wait(smem_u32(&b_qempty[qs]), ((it >> 1) - 1) & 1, kMaxPolls, &g_abort)) ok = false;
+                if (it >= 2 && !mbar_wait(smem_u32(&b_qempty[qs]), ((it >> 1) - 1) & 1, kWaitNs, &g_abort)) ok = false;
                 if (ok) {
                     fetch(it);
                     fetched = it + 1;
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         // after a failure: let copies still in flight into this CTA's shared memory land
         // (bounded) before the CTA exits
         if (!ok && ptid == 0)
-            for (int f = landed; f < fetched; ++f) mbar_wait(smem_u32(&b_qraw[f & 1]), (f >> 1) & 1, 1u << 16);
+            for (int f = landed; f < fetched; ++f) mbar_wait(smem_u32(&b_qraw[f & 1]), (f >> 1) & 1, kDrainNs);
     } else if (warp == kMmaWarp) {
         // =============================== MMA issue ===============================
         if (lane == 0) {
@@ -428,8 +428,8 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             int prev_n = -1, prev_first = 0, prev_last = 0, prev_tok = 0;  // the item whose P V is still to issue
             auto issue_pv = [&](int pn, bool first, bool last, int tok) -> bool {
                 const int pb = pn & 1, ob = tok & 1;
-                if (!mbar_wait(smem_u32(&b_pfull[pb]), (pn >> 1) & 1, kMaxPolls, &g_abort)) return false;
-                if (first && tok >= 2 && !mbar_wait(smem_u32(&b_oempty[ob]), ((tok >> 1) - 1) & 1, kMaxPolls, &g_abort))
+                if (!mbar_wait(smem_u32(&b_pfull[pb]), (pn >> 1) & 1, kWaitNs, &g_abort)) return false;
+                if (first && tok >= 2 && !mbar_wait(smem_u32(&b_oempty[ob]), ((tok >> 1) - 1) & 1, kWaitNs, &g_abort))
                     return false;
                 tc_fence_after();
                 const uint32_t kb = s_base + kKOff + (pn % kNB) * 32768;
@@ -447,12 +447,12 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             };
             for (int it = 0; it < n_tok_cta && ok; ++it) {
                 const int qs = it & 1;
-                if (!mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kWaitNs, &g_abort)) { ok = false; break; }
                 const int n_tiles = meta[qs].n_ct + 1;
                 for (int c = 0; c < n_tiles; ++c, ++n) {
                     const int kb = n % kNB, sb = n & 1;
-                    if (!mbar_wait(smem_u32(&b_kfull[kb]), (n / kNB) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
-                    if (n >= 2 && !mbar_wait(smem_u32(&b_sempty[sb]), ((n >> 1) - 1) & 1, kMaxPolls, &g_abort)) {
+                    if (!mbar_wait(smem_u32(&b_kfull[kb]), (n / kNB) & 1, kWaitNs, &g_abort)) { ok = false; break; }
+                    if (n >= 2 && !mbar_wait(smem_u32(&b_sempty[sb]), ((n >> 1) - 1) & 1, kWaitNs, &g_abort)) {
                         ok = false;
                         break;
                     }
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         int n = 0;
         for (int it = 0; it < n_tok_cta; ++it) {
             const int qs = it & 1, ob = it & 1;
-            note(mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kMaxPolls, &g_abort));
+            note(mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kWaitNs, &g_abort));
             if (tid < kH) s_m[tid] = -INFINITY;
             if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
             const TokenMeta mt = meta[qs];
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             bool failed = false;
             for (int c = 0; c < n_tiles; ++c, ++n) {
                 const int sb = n & 1, pb = n & 1;
-                note(mbar_wait(smem_u32(&b_sfull[sb]), (n >> 1) & 1, kMaxPolls, &g_abort));
+                note(mbar_wait(smem_u32(&b_sfull[sb]), (n >> 1) & 1, kWaitNs, &g_abort));
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_base + kSCol + sb * kH + h0;
                 // key validity of this thread's key (TMEM lane = key within the tile)
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         }
                     }
                 }
-                if (n >= 2) note(mbar_wait(smem_u32(&b_pempty[pb]), ((n >> 1) - 1) & 1, kMaxPolls, &g_abort));
+                if (n >= 2) note(mbar_wait(smem_u32(&b_pempty[pb]), ((n >> 1) - 1) & 1, kWaitNs, &g_abort));
                 if (named_sync_or(kBarSoftmax, kSoftmax, over || !okl)) {
                     // rare: a first tile, a jump of the maximum, or a failed wait
                     if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) { failed = true; break; }
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     rescale_o = c > 0 && named_sync_or(bar_wg, 128, rescale_o);
                     if (rescale_o) {
                         // O^T holds the P V of the previous tiles of this token: wait for the last
-                        note(mbar_wait(smem_u32(&b_pempty[(n - 1) & 1]), ((n - 1) >> 1) & 1, kMaxPolls, &g_abort));
+                        note(mbar_wait(smem_u32(&b_pempty[(n - 1) & 1]), ((n - 1) >> 1) & 1, kWaitNs, &g_abort));
                         tc_fence_after();
 #pragma unroll 1
                         for (int c0 = 0; c0 < 32; c0 += 16) {
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     P.lse[(int64_t)((P.decode ? mt.b : (int64_t)mt.b * P.L + mt.t)) * kH + h] =
                         (m + log2f(l)) * 0.6931471805599453f;
             }
-            note(mbar_wait(smem_u32(&b_ofull[ob]), (it >> 1) & 1, kMaxPolls, &g_abort));
+            note(mbar_wait(smem_u32(&b_ofull[ob]), (it >> 1) & 1, kWaitNs, &g_abort));
             if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
             tc_fence_after();
             float o[32];
@@ -735,6 +735,19 @@ size_t csa_widen_bytes(const AttnArgs &a) {
     return (a.kv_t == CSA_MIXED && !a.decode) ? (size_t)a.B * (size_t)a.ncap * 128 * 2 : 0;
 }
 
+const void *launch_widen_mixed(const AttnArgs &a, cudaStream_t st) {
+    const int64_t erows = (int64_t)a.B * a.ncap;
+    __nv_bfloat16 *wide = reinterpret_cast<__nv_bfloat16 *>(a.ws);
+    int blocks = (int)ceil_div64(erows * 16, 256);
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    if (blocks < 1) blocks = 1;
+    widen_mixed_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint8_t *>(a.c_data),
+                                              reinterpret_cast<const __nv_bfloat16 *>(a.c_rope), a.c_scale, erows,
+                                              wide);
+    count_launches(1);
+    return wide;
+}
+
 bool csa_tc_supported(const AttnArgs &a) {
     if (a.act_t != CSA_BF16) return false;
     if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED) return false;
@@ -764,16 +777,7 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.mixed = a.kv_t == CSA_MIXED;
     if (P.mixed && !a.decode) {
         // widen every entry once; the attention then gathers BF16 rows
-        const int64_t erows = (int64_t)a.B * a.ncap;
-        __nv_bfloat16 *wide = reinterpret_cast<__nv_bfloat16 *>(a.ws);
-        int blocks = (int)ceil_div64(erows * 16, 256);
-        if (blocks > 148 * 8) blocks = 148 * 8;
-        if (blocks < 1) blocks = 1;
-        widen_mixed_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint8_t *>(a.c_data),
-                                                  reinterpret_cast<const __nv_bfloat16 *>(a.c_rope), a.c_scale, erows,
-                                                  wide);
-        count_launches(1);
-        P.c_data = wide;
+        P.c_data = launch_widen_mixed(a, st);
         P.c_rope = nullptr;
         P.c_scale = nullptr;
         P.mixed = 0;

@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(128, 1) hca_tc_kernel(const __grid_constant__ 
     bool ok = true;
 
     // Q: wait, then rotate dims 64..127 at position t (pairs (64+i, 96+i)) in shared memory
-    ok = __syncthreads_and(mbar_wait(bar_q, 0, kMaxPolls, &g_abort));
+    ok = __syncthreads_and(mbar_wait(bar_q, 0, kWaitNs, &g_abort));
     if (ok && P.d_rope == 64 && row_ok) {
         uint8_t *q1 = sm + kQOff + 16384;  // dims 64..127
 #pragma unroll
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(128, 1) hca_tc_kernel(const __grid_constant__ 
         const int n_i = ctile ? kCTile : P.n_swa;
         const uint32_t kbuf = s_base + kKOff + buf * 2 * kSub;
         // a timed-out wait is made block-uniform so every thread leaves the loop together
-        if (!__syncthreads_and(mbar_wait(smem_u32(&bars[1 + buf]), (i >> 1) & 1, kMaxPolls, &g_abort))) { ok = false; break; }
+        if (!__syncthreads_and(mbar_wait(smem_u32(&bars[1 + buf]), (i >> 1) & 1, kWaitNs, &g_abort))) { ok = false; break; }
         if (ctile && P.mixed) {
             // widen the FP8 half: row r of the tile = entry j0 + r
             const int j = i * kCTile + r;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(128, 1) hca_tc_kernel(const __grid_constant__ 
             }
             mma_commit(bar_mma);
         }
-        if (!__syncthreads_and(mbar_wait(bar_mma, ph_mma, kMaxPolls, &g_abort))) { ok = false; break; }
+        if (!__syncthreads_and(mbar_wait(bar_mma, ph_mma, kWaitNs, &g_abort))) { ok = false; break; }
         ph_mma ^= 1;
         tc_fence_after();
         // the previous P V is complete: its key buffer takes tile i + 1
@@ -284,13 +284,13 @@ __global__ void __launch_bounds__(128, 1) hca_tc_kernel(const __grid_constant__ 
     }
     if (ok) {
         if (tid == 0) mma_commit(bar_mma);
-        ok = __syncthreads_and(mbar_wait(bar_mma, ph_mma, kMaxPolls, &g_abort));
+        ok = __syncthreads_and(mbar_wait(bar_mma, ph_mma, kWaitNs, &g_abort));
         tc_fence_after();
     }
     if (!ok) {
         if (tid == 0) set_timeout();
         // let in-flight copies land before the shared memory is released (bounded)
-        for (int q = 0; q < 3; ++q) mbar_wait(smem_u32(&bars[q]), 0, 1u << 16);
+        for (int q = 0; q < 3; ++q) mbar_wait(smem_u32(&bars[q]), 0, kDrainNs);
     } else {
         // ---- epilogue of row r. The TMEM loads are warp-collective (.sync.aligned), so every
         // thread executes them; only rows inside the sequence store. ----

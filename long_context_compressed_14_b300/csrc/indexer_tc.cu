@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
                         if (lqn >= 2) {
                             const uint32_t par = ((lqn >> 1) - 1) & 1;
                             if (ln == mn) {
-                                if (!mbar_wait(smem_u32(&b_qempty[qb]), par, kMaxPolls, &g_abort)) { ok = false; break; }
+                                if (!mbar_wait(smem_u32(&b_qempty[qb]), par, kWaitNs, &g_abort)) { ok = false; break; }
                             } else if (!mbar_try_wait(smem_u32(&b_qempty[qb]), par)) {
                                 break;  // do MMA work first
                             }
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
                                     (int)(((int64_t)P.b * P.L + P.t0 + lq * TQ) * HI), 0);
                     }
                     const int kb = ln % kNK;
-                    if (ln >= kNK && !mbar_wait(smem_u32(&b_kempty[kb]), ((ln / kNK) - 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
+                    if (ln >= kNK && !mbar_wait(smem_u32(&b_kempty[kb]), ((ln / kNK) - 1) & 1, kWaitNs, &g_abort)) { ok = false; break; }
                     mbar_expect_tx(smem_u32(&b_kfull[kb]), kKBytes);
                     tma_load_3d(s_base + kKOff + kb * kKBytes, &P.mk, smem_u32(&b_kfull[kb]), 0, P.b * P.ncap + le * kJ, 0);
                     ++ln;
@@ -148,9 +148,9 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
                 if (!ok) break;
                 const int net = n_et_of(mq);
                 const int qb = mqn & 1, kb = mn % kNK, db = mn & 1;
-                if (me == 0 && !mbar_wait(smem_u32(&b_qfull[qb]), (mqn >> 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
-                if (!mbar_wait(smem_u32(&b_kfull[kb]), (mn / kNK) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
-                if (mn >= 2 && !mbar_wait(smem_u32(&b_dempty[db]), ((mn >> 1) - 1) & 1, kMaxPolls, &g_abort)) { ok = false; break; }
+                if (me == 0 && !mbar_wait(smem_u32(&b_qfull[qb]), (mqn >> 1) & 1, kWaitNs, &g_abort)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&b_kfull[kb]), (mn / kNK) & 1, kWaitNs, &g_abort)) { ok = false; break; }
+                if (mn >= 2 && !mbar_wait(smem_u32(&b_dempty[db]), ((mn >> 1) - 1) & 1, kWaitNs, &g_abort)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
         const int g = warp >> 2;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         auto ewait = [&](uint32_t bar, uint32_t par) -> bool {
-            const bool w = mbar_wait(bar, par, kMaxPolls, &g_abort);
+            const bool w = mbar_wait(bar, par, kWaitNs, &g_abort);
             return !named_sync_or(kBarEpi, kEpi, !w);
         };
         int n = 0;

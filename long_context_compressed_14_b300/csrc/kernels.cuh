@@ -81,5 +81,9 @@ void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
 bool launch_hca_tc(const AttnArgs &a, cudaStream_t st);
 bool launch_csa_tc(const AttnArgs &a, cudaStream_t st);
 bool launch_indexer_tc(const IndexArgs &a, cudaStream_t st);
+// Mixed-precision entries (prefill) widened to BF16 rows [B, ncap, 128] in a.ws (csa_widen_bytes
+// bytes); returns the widened array.
+size_t csa_widen_bytes(const AttnArgs &a);
+const void *launch_widen_mixed(const AttnArgs &a, cudaStream_t st);
 
 }  // namespace csa
