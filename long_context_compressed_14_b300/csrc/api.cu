@@ -368,7 +368,8 @@ int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
         return CSA_ERR_INVALID;
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
     AttnArgs a = attn_args(p, q, swa_ring, C, nullptr, ctx_len, sink, rope_tab, out, lse_out, 1, 0);
-    launch_attn_simple(a, cs(stream));
+    a.dense = 1;  // every visible entry, in order
+    if (!launch_csa_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
     return launch_status();
 }
 

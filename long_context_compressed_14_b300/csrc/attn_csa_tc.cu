@@ -88,6 +88,7 @@ struct CsaTcParams {
     __nv_bfloat16 *out;
     float *lse;
     int B, L, ncap, topk, n_win, d_rope, mixed, decode, rows;
+    int dense, m;   // dense: keys are entries 0 .. visible(t) - 1 in order (no top-k row)
     float scale_log2;
 };
 
@@ -228,8 +229,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             const int row2 = (int)blockIdx.x + it2 * (int)gridDim.x;
             const int qs2 = it2 & 1;
             const uint32_t qb = smem_u32(&b_qraw[qs2]);
-            mbar_expect_tx(qb, 2 * kH * 128 + P.topk * 4);
-            bulk_load(s_base + kIdxOff + qs2 * P.topk * 4, P.idx + (int64_t)row2 * P.topk, P.topk * 4, qb);
+            mbar_expect_tx(qb, 2 * kH * 128 + (P.dense ? 0 : P.topk * 4));
+            if (!P.dense)
+                bulk_load(s_base + kIdxOff + qs2 * P.topk * 4, P.idx + (int64_t)row2 * P.topk, P.topk * 4, qb);
             tma_load_3d(s_base + kQOff + qs2 * 16384, &P.mq, qb, 0, row2 * kH, 0);
             tma_load_3d(s_base + kQOff + qs2 * 16384 + 8192, &P.mq, qb, 64, row2 * kH, 0);
         };
@@ -265,12 +267,13 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             // count the valid prefix of the top-k row (ascending, -1 padded) in parallel
             const int32_t *sidx = reinterpret_cast<const int32_t *>(sm + kIdxOff) + qs * P.topk;
             int cnt = 0;
-            for (int i = ptid; i < P.topk; i += kProducers) cnt += (pos_ok && sidx[i] >= 0) ? 1 : 0;
+            if (!P.dense)
+                for (int i = ptid; i < P.topk; i += kProducers) cnt += (pos_ok && sidx[i] >= 0) ? 1 : 0;
             cnt = __reduce_add_sync(0xffffffffu, cnt);
             if ((ptid & 31) == 0) s_cnt[ptid >> 5] = cnt;
             named_sync(kBarProd, kProducers);
             TokenMeta mt;
-            mt.n_sel = s_cnt[0] + s_cnt[1] + s_cnt[2];
+            mt.n_sel = P.dense ? (pos_ok ? visible_entries(t, P.m, P.ncap) : 0) : s_cnt[0] + s_cnt[1] + s_cnt[2];
             mt.n_ct = (mt.n_sel + kTile - 1) / kTile;
             mt.t = t;
             mt.b = b;
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     for (int q = 0; q < kGatherPer; ++q) {
                         const int i = i0 + 6 * q;
                         const int pos = c * kTile + i;
-                        const int j = (i < kTile && pos < mt.n_sel) ? sidx[pos] : -1;
+                        const int j = (i < kTile && pos < mt.n_sel) ? (P.dense ? pos : sidx[pos]) : -1;
                         bad |= j >= P.ncap;
                         jj[q] = j >= P.ncap ? -1 : j;
                     }
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         const int i = u >> 4, ch = u & 15;
                         const int pos = c * kTile + i;
                         const uint32_t off = (ch >> 3) * 16384 + sw128_off(i, ch & 7);
-                        int j = pos < mt.n_sel ? sidx[pos] : -1;
+                        int j = pos < mt.n_sel ? (P.dense ? pos : sidx[pos]) : -1;
                         if (j >= P.ncap) {
                             set_status(CSA_ERR_BOUNDS);
                             j = -1;
@@ -751,12 +754,14 @@ const void *launch_widen_mixed(const AttnArgs &a, cudaStream_t st) {
 bool csa_tc_supported(const AttnArgs &a) {
     if (a.act_t != CSA_BF16) return false;
     if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED) return false;
-    if (a.H != csa_tc::kH || a.n_win != 128 || a.topk < 4 || a.topk > kMaxTopk || a.topk % 4 != 0) return false;
+    if (a.H != csa_tc::kH || a.n_win != 128) return false;
+    if (!a.dense && (a.topk < 4 || a.topk > kMaxTopk || a.topk % 4 != 0)) return false;
+    if (a.dense && !a.decode) return false;
     if (a.d_rope != 0 && a.d_rope != 64) return false;
     if (csa_widen_bytes(a) > a.ws_bytes || (csa_widen_bytes(a) > 0 && !a.ws)) return false;
-    // top-k rows are fetched with a bulk copy and outputs stored with one: 16-byte aligned
-    return a.idx != nullptr && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 &&
-           (reinterpret_cast<uintptr_t>(a.out) & 15) == 0;
+    // outputs are stored with a bulk copy, top-k rows fetched with one: 16-byte aligned
+    if ((reinterpret_cast<uintptr_t>(a.out) & 15) != 0) return false;
+    return a.dense || (a.idx != nullptr && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0);
 }
 
 bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
@@ -791,6 +796,7 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.lse = a.lse;
     P.B = a.B; P.L = a.L; P.ncap = a.ncap; P.topk = a.topk; P.n_win = a.n_win; P.d_rope = a.d_rope;
     P.decode = a.decode; P.rows = rows;
+    P.dense = a.dense; P.m = a.m;
     P.scale_log2 = a.scale * 1.4426950408889634f;
     int dev = 0, sms = 148, smem_max = 0;
     cudaGetDevice(&dev);
@@ -799,8 +805,9 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     const int grid = rows < sms ? rows : sms;
     // four key-tile buffers when they fit next to the top-k rows, else three
     const int static_bytes = 4096;  // barriers, per-head vectors, reduction scratch (upper bound)
-    const int smem4 = 1024 + idx_off(4) + 2 * a.topk * 4;
-    const int smem3 = 1024 + idx_off(3) + 2 * a.topk * 4;
+    const int idx_bytes = a.dense ? 0 : 2 * a.topk * 4;
+    const int smem4 = 1024 + idx_off(4) + idx_bytes;
+    const int smem3 = 1024 + idx_off(3) + idx_bytes;
     if (smem4 + static_bytes <= smem_max) {
         cudaFuncSetAttribute(csa_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem4);
         csa_tc_kernel<4><<<grid, kThreads, smem4, st>>>(P);

@@ -63,6 +63,7 @@ struct AttnArgs {
     int B, L, H, m, topk, n_win, d_rope, ncap;
     float scale;
     int decode, act_t, kv_t;
+    int dense;             // 1: the key list is every visible entry in order (HCA decode), no idx
 };
 
 // host-side count of kernel launches (every launch_* adds the kernels it launched)
