@@ -209,10 +209,11 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
                int32_t *topk_out, void *out, float *lse_out, void *ws, size_t ws_bytes,
                csa_stream_t stream);
 
-/* csa_decode for callers that cannot allocate device memory (code running under CUDA-graph
- * capture or replay, real-time serving loops that must not touch the allocator, hosts whose
- * device memory is owned by another framework). This entry point has no counterpart in the
- * paper; it exists only for such callers.
+/* csa_decode for callers that cannot allocate device memory. Examples: a host application
+ * whose device memory is owned by another framework's allocator, which hands out no scratch
+ * buffers; a real-time serving loop that must not call cudaMalloc, because it can synchronise
+ * the device and take unbounded time; a caller held to a fixed device-memory budget. This
+ * entry point has no counterpart in the paper; it exists only for such callers.
  * It computes exactly what csa_decode computes, with the same arguments minus the workspace:
  * the scratch it needs (indexer scores and selected indices) comes from one fixed array of
  * CSA_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads the library holds
@@ -223,7 +224,8 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
  *    (cudaGetSymbolAddress, with the device current); make that first call before any stream
  *    capture begins.
  *  - All calls on a device share the array: calls that overlap on the GPU (unordered streams)
- *    race on it. Nothing in it needs to start at zero. */
+ *    race on it. Nothing in it needs to start at zero: each call writes the scores and indices
+ *    before it reads them. */
 #define CSA_STATIC_SCRATCH_BYTES (4u << 20)
 int csa_decode_static_scratch(const csa_params *p, const void *q, const int32_t *ctx_len,
                               const csa_entries *C, const csa_index_rows *qI,

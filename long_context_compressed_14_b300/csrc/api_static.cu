@@ -1,10 +1,11 @@
 // api_static.cu -- csa_decode for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at all: code that runs while a CUDA graph is being
-// captured or replayed, real-time serving loops that must not touch the allocator, or hosts
-// whose memory is owned by a framework that gives out no scratch buffers. csa_decode needs
-// scratch (indexer scores and the selected indices); this entry point takes it from one
-// fixed array compiled into the library instead of from the caller.
+// Some callers cannot call cudaMalloc at all: a host application whose device memory belongs
+// to another framework's allocator that gives out no scratch buffers, a real-time serving loop
+// that must not call cudaMalloc (it can synchronise the device and take unbounded time), or a
+// caller held to a fixed device-memory budget. csa_decode needs scratch (indexer scores and the
+// selected indices); this entry point takes it from one fixed array compiled into the library
+// instead of from the caller.
 //
 // The array is file-scope device memory of CSA_STATIC_SCRATCH_BYTES: every GPU that loads the
 // library holds it until the process exits. In host code its name is only a host-side

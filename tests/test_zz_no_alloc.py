@@ -1,7 +1,8 @@
 """The allocation-free decode entry point (csa_decode_static_scratch), on the GPU.
 
-Some callers cannot allocate device memory (CUDA-graph capture, allocator-free serving
-loops), so the library offers csa_decode with its scratch in a fixed array inside the
+Some callers cannot allocate device memory (their device memory belongs to another
+framework's allocator, or a real-time loop must not call cudaMalloc because it can synchronise
+the device), so the library offers csa_decode with its scratch in a fixed array inside the
 library. These tests call it through the C ABI twice in a row and compare it with
 csa_decode given a caller workspace; they also check that a layer too large for the array is
 refused. This file is collected last so that a failure here comes after every other test.
