@@ -330,24 +330,26 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 }
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_base + sb * kSStride;
-                // pass 1: tile maximum of the valid scores
+                // the row's scores in registers: one TMEM load of 128 columns (+16 for the window)
+                float sv[128], sx[16];
+                tmem_ld128_sync(s_addr, sv);
+                if (nk > 128) tmem_ld16_sync(s_addr + 128, sx);
                 float tmax = -INFINITY;
-#pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    float v[32];
-                    tmem_ld32_sync(s_addr + c0, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (c0 + e >= lo && c0 + e < hi) tmax = fmaxf(tmax, v[e]);
+                for (int e = 0; e < 128; ++e) {
+                    sv[e] = (e >= lo && e < hi) ? sv[e] * P.scale_log2 : -INFINITY;
+                    tmax = fmaxf(tmax, sv[e]);
                 }
                 if (nk > 128) {
-                    float v[16];
-                    tmem_ld16_sync(s_addr + 128, v);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (128 + e >= lo && 128 + e < hi) tmax = fmaxf(tmax, v[e]);
+                    for (int e = 0; e < 16; ++e) {
+                        sx[e] = (128 + e >= lo && 128 + e < hi) ? sx[e] * P.scale_log2 : -INFINITY;
+                        tmax = fmaxf(tmax, sx[e]);
+                    }
                 }
-                tmax *= P.scale_log2;
+                // S(n) is in registers: the MMA may write S(n + 2) into this slot
+                tc_fence_before();
+                mbar_arrive(smem_u32(&b_sfree[sb]));
                 const bool upd = tmax > m_run + kOver;
                 if (__any_sync(0xffffffffu, upd)) {
                     // (warp-uniform branch) rows whose maximum moved rescale by f, the others by 1
@@ -373,33 +375,44 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     }
                     if (upd) m_run = tmax;
                 }
+                // P = exp2(scale * s - max) as BF16; masked keys are -inf and give 0
+#pragma unroll
+                for (int e = 0; e < 128; ++e) sv[e] = sv[e] == -INFINITY ? 0.0f : fast_exp2(sv[e] - m_run);
+                if (nk > 128) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sx[e] = sx[e] == -INFINITY ? 0.0f : fast_exp2(sx[e] - m_run);
+                }
                 // the P buffer is free once the previous tile's P V has read it
                 if (n >= 1 &&
                     !__all_sync(0xffffffffu, mbar_wait(smem_u32(&b_pvdone), (n - 1) & 1, kWaitNs, &g_abort))) {
                     ok = false;
                     break;
                 }
-                // pass 2: P = exp2(scale * s - max) as BF16 into shared memory (row r, 16 keys at a time)
-                for (int c0 = 0; c0 < nk; c0 += 16) {
-                    float v[16];
-                    tmem_ld16_sync(s_addr + c0, v);
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 16) {
                     uint32_t pk[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
-                        const float p0 = (c0 + e >= lo && c0 + e < hi) ? fast_exp2(v[e] * P.scale_log2 - m_run) : 0.0f;
-                        const float p1 =
-                            (c0 + e + 1 >= lo && c0 + e + 1 < hi) ? fast_exp2(v[e + 1] * P.scale_log2 - m_run) : 0.0f;
-                        l_run += p0 + p1;
-                        pk[e >> 1] = pack_bf16x2(p0, p1);
+                        l_run += sv[c0 + e] + sv[c0 + e + 1];
+                        pk[e >> 1] = pack_bf16x2(sv[c0 + e], sv[c0 + e + 1]);
                     }
                     const int sub = c0 >> 6, ch = (c0 & 63) >> 3;
                     uint8_t *base = sm + kPOff + sub * 16384;
                     *reinterpret_cast<uint4 *>(base + sw128_off(r, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     *reinterpret_cast<uint4 *>(base + sw128_off(r, ch + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
+                if (nk > 128) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        l_run += sx[e] + sx[e + 1];
+                        pk[e >> 1] = pack_bf16x2(sx[e], sx[e + 1]);
+                    }
+                    uint8_t *base = sm + kPOff + 2 * 16384;
+                    *reinterpret_cast<uint4 *>(base + sw128_off(r, 0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(base + sw128_off(r, 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
                 fence_async_smem();
-                tc_fence_before();
-                mbar_arrive(smem_u32(&b_sfree[sb]));
                 mbar_arrive(smem_u32(&b_pfull));
             }
             if (!ok) break;

@@ -374,3 +374,83 @@ def test_decode(lib, csa):
 def test_device_status_clean(lib):
     torch.cuda.synchronize()
     assert lib.csa_device_status() == 0
+
+
+# ---------------------------------------------------------------------------------------
+# Full-size workloads, in the configuration bench.py times, checked on sampled rows
+# ---------------------------------------------------------------------------------------
+
+def _check_prefill_rows(wl, inp, out, topk, b, rows, csa, layer_no=0):
+    res = oracle_prefill(wl, inp, b, rows, csa=csa)
+    if csa:
+        gidx = topk.cpu().numpy()[b][rows]
+        frac = check_topk_by_score(gidx, res["scores"], rows, wl.m, wl.topk)
+        assert frac >= 0.95, frac
+        same = np.array([np.array_equal(gidx[r], res["idx"][r]) for r in range(len(rows))])
+        assert rel_l2(np64(out[b][rows])[same], res["o"][same]) <= 2e-2
+    else:
+        assert rel_l2(np64(out[b][rows]), res["o"]) <= 2e-2
+
+
+def test_csa_bf16_4x32768_full_size_sampled(lib):
+    # 4 sequences x 32768 tokens, 64 heads, FP8 indexer, top-512: the whole layer on the GPU,
+    # 96 sampled rows of the first and the last sequence against the oracle
+    wl = synth.WORKLOADS["csa_bf16_4x32768"]
+    from long_context_compressed_14_b300.pipeline import PrefillLayer
+    inp = synth.prefill_layer(wl, csa=True)
+    layer = PrefillLayer.create(wl, csa=True)
+    out = layer.run(_dev(inp))
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
+    for b in (0, wl.B - 1):
+        rows = synth.sample_rows(wl.L, 96, seed=b, first=16, last=16).numpy()
+        _check_prefill_rows(wl, inp, out, layer.topk, b, rows, csa=True)
+
+
+def test_pair_mixed_L262144_full_size_sampled(lib):
+    # the layer-pair workload as bench.py runs it (CSA layer then HCA layer, 262144 tokens,
+    # mixed-precision entries, FP8 indexer, top-1024), 48 sampled rows per layer
+    wl = synth.WORKLOADS["pair_mixed_L262144"]
+    from long_context_compressed_14_b300.pipeline import PrefillLayer
+    rows = synth.sample_rows(wl.L, 48, seed=4, first=8, last=8).numpy()
+    for layer_no, csa in ((0, True), (1, False)):
+        inp = synth.prefill_layer(wl, layer_no, csa=csa)
+        layer = PrefillLayer.create(wl, csa=csa)
+        out = layer.run(_dev(inp))
+        torch.cuda.synchronize()
+        assert lib.csa_device_status() == 0
+        out_rows = out[0][torch.as_tensor(rows, device=out.device)].cpu()
+        topk_rows = layer.topk[0][torch.as_tensor(rows, device=out.device)].cpu() if csa else None
+        del layer, out
+        res = oracle_prefill(wl, inp, 0, rows, csa=csa)
+        if csa:
+            frac = check_topk_by_score(topk_rows.numpy(), res["scores"], rows, wl.m, wl.topk)
+            assert frac >= 0.95, frac
+            same = np.array([np.array_equal(topk_rows.numpy()[r], res["idx"][r]) for r in range(len(rows))])
+            assert rel_l2(np64(out_rows)[same], res["o"][same]) <= 2e-2
+        else:
+            assert rel_l2(np64(out_rows), res["o"]) <= 2e-2
+        del inp
+        torch.cuda.empty_cache()
+
+
+def test_decode_b16_ctx131072_full_size_sampled(lib):
+    # 16 sequences x 131072 cached tokens, one CSA and one HCA decode step; sequences 0 and 15
+    wl = synth.WORKLOADS["decode_b16_ctx131072"]
+    from long_context_compressed_14_b300.pipeline import DecodeLayer
+    for csa in (True, False):
+        inp = synth.decode_layer(wl, 0 if csa else 1, csa=csa)
+        layer = DecodeLayer.create(wl, csa=csa)
+        d = _dev(inp)
+        layer.load_caches(d)
+        out = layer.run(d)
+        torch.cuda.synchronize()
+        assert lib.csa_device_status() == 0
+        for b in (0, wl.B - 1):
+            res = _oracle_decode(wl, inp, b, csa)
+            if csa:
+                frac = check_topk_by_score(layer.topk.cpu().numpy()[b][None], res["scores"][None],
+                                           [int(inp["ctx"][b]) - 1], wl.m, wl.topk)
+                if frac < 1.0:
+                    continue  # a near-tie changed the set; the selection itself was checked above
+            assert rel_l2(np64(out[b]), res["o"]) <= 2e-2, b
