@@ -334,22 +334,30 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 float sv[128], sx[16];
                 tmem_ld128_sync(s_addr, sv);
                 if (nk > 128) tmem_ld16_sync(s_addr + 128, sx);
-                float tmax = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < 128; ++e) {
-                    sv[e] = (e >= lo && e < hi) ? sv[e] * P.scale_log2 : -INFINITY;
-                    tmax = fmaxf(tmax, sv[e]);
-                }
-                if (nk > 128) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        sx[e] = (128 + e >= lo && 128 + e < hi) ? sx[e] * P.scale_log2 : -INFINITY;
-                        tmax = fmaxf(tmax, sx[e]);
-                    }
-                }
                 // S(n) is in registers: the MMA may write S(n + 2) into this slot
                 tc_fence_before();
                 mbar_arrive(smem_u32(&b_sfree[sb]));
+                // masked keys become -inf; a warp whose rows all see the whole tile skips the masks
+                const bool full = __all_sync(0xffffffffu, lo == 0 && hi >= 128 && nk == 128);
+                if (!full) {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e) sv[e] = (e >= lo && e < hi) ? sv[e] : -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sx[e] = (nk > 128 && 128 + e >= lo && 128 + e < hi) ? sx[e] : -INFINITY;
+                }
+                // tile maximum with eight independent partial maxima (short dependency chains)
+                float mx8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx8[q] = full ? sv[q] : fmaxf(sv[q], sx[q]);
+#pragma unroll
+                for (int e = 8; e < 128; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
+                if (!full) {
+#pragma unroll
+                    for (int e = 8; e < 16; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], sx[e]);
+                }
+                float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                tmax *= P.scale_log2;  // the scale is positive: max(s) * scale = max(s * scale)
                 const bool upd = tmax > m_run + kOver;
                 if (__any_sync(0xffffffffu, upd)) {
                     // (warp-uniform branch) rows whose maximum moved rescale by f, the others by 1
@@ -375,12 +383,21 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     }
                     if (upd) m_run = tmax;
                 }
-                // P = exp2(scale * s - max) as BF16; masked keys are -inf and give 0
+                // P = exp2(scale * s - max) as BF16; masked keys are -inf and give exp2(-inf) = 0
+                // (m_run is finite whenever the row has a valid key; a row with none in this
+                // tile and m_run = -inf would give NaN, so such a row is zeroed explicitly)
+                const float neg_m = -m_run;
+                const bool row_live = m_run != -INFINITY;
+                if (__all_sync(0xffffffffu, row_live)) {
 #pragma unroll
-                for (int e = 0; e < 128; ++e) sv[e] = sv[e] == -INFINITY ? 0.0f : fast_exp2(sv[e] - m_run);
+                    for (int e = 0; e < 128; ++e) sv[e] = fast_exp2(fmaf(sv[e], P.scale_log2, neg_m));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e) sv[e] = row_live ? fast_exp2(fmaf(sv[e], P.scale_log2, neg_m)) : 0.0f;
+                }
                 if (nk > 128) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) sx[e] = sx[e] == -INFINITY ? 0.0f : fast_exp2(sx[e] - m_run);
+                    for (int e = 0; e < 16; ++e) sx[e] = row_live ? fast_exp2(fmaf(sx[e], P.scale_log2, neg_m)) : 0.0f;
                 }
                 // the P buffer is free once the previous tile's P V has read it
                 if (n >= 1 &&
@@ -388,12 +405,13 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     ok = false;
                     break;
                 }
+                float ls8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int c0 = 0; c0 < 128; c0 += 16) {
                     uint32_t pk[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
-                        l_run += sv[c0 + e] + sv[c0 + e + 1];
+                        ls8[e >> 1] += sv[c0 + e] + sv[c0 + e + 1];
                         pk[e >> 1] = pack_bf16x2(sv[c0 + e], sv[c0 + e + 1]);
                     }
                     const int sub = c0 >> 6, ch = (c0 & 63) >> 3;
@@ -405,13 +423,14 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     uint32_t pk[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
-                        l_run += sx[e] + sx[e + 1];
+                        ls8[e >> 1] += sx[e] + sx[e + 1];
                         pk[e >> 1] = pack_bf16x2(sx[e], sx[e + 1]);
                     }
                     uint8_t *base = sm + kPOff + 2 * 16384;
                     *reinterpret_cast<uint4 *>(base + sw128_off(r, 0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     *reinterpret_cast<uint4 *>(base + sw128_off(r, 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
+                l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
                 fence_async_smem();
                 mbar_arrive(smem_u32(&b_pfull));
             }
