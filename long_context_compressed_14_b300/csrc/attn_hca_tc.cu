@@ -13,17 +13,19 @@
 // Per key tile: S = Q K^T (M = 128, N = 128 or 144, K = 128) into TMEM; one thread per query row
 // reads its S row, masks it (visibility / window), keeps a running row maximum in the log2
 // domain (moved lazily, only when the tile maximum exceeds it by more than 8; O is then
-// rescaled in TMEM), writes P = exp2(s - max) as BF16 into shared memory, and O += P V
-// (M = 128, N = 128, K = keys) accumulates in TMEM, V being the same key tile read through an
-// MN-major descriptor.
+// rescaled in TMEM), and writes P = exp2(s - max) as BF16 back into the first columns of the
+// same TMEM slot (two values per 32-bit column); O += P V (M = 128, N = 128, K = keys)
+// accumulates in TMEM with P read from TMEM as the A operand and V (the same key tile) from
+// shared memory through an MN-major descriptor.
 //
 // Roles (192 threads, persistent over work items):
 //   warps 0-3  softmax + epilogue (thread = query row = TMEM lane);
 //   warp 4     MMA issue (one thread);
 //   warp 5     producer: query rows by TMA (and RoPE on them, all 32 lanes), key tiles by TMA.
-// S is double-buffered in TMEM, so the MMA computes the next tile's scores while the softmax
-// works on this one; key tiles flow through three buffers; query rows are double-buffered and
-// fetched one item ahead. Mixed-precision entries are widened
+// S/P is double-buffered in TMEM, so the MMA computes the next tile's scores and the previous
+// tile's P V while the softmax works on this one; a slot is rewritten by S(n + 2) only after
+// P V(n) has read it, which the in-order tensor pipe guarantees (P V(n) is issued first). Key
+// tiles flow through four buffers; query rows are double-buffered and fetched one item ahead. Mixed-precision entries are widened
 // to BF16 once per call (caller workspace) before this kernel runs. Every wait is bounded.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -38,15 +40,14 @@ constexpr int kRows = 128;                 // query rows per work item
 constexpr int kMmaWarp = 4;
 constexpr int kProdWarp = 5;
 constexpr int kThreads = 192;
-constexpr int kNB = 3;                     // key-tile buffers
+constexpr int kNB = 4;                     // key-tile buffers
 constexpr int kMaxKeys = 144;              // rows of a key-tile buffer (the window tile needs <= 144)
 constexpr int kSub = kMaxKeys * 128;       // bytes of one 64-dim half of a key-tile buffer (18 KB)
 constexpr int kQOff = 0;                   // Q: 2 buffers of two 64-dim halves of 16 KB
 constexpr int kKOff = 65536;               // key tiles: kNB buffers of 2 * kSub
-constexpr int kPOff = kKOff + kNB * 2 * kSub;  // P: three 64-key sub-tiles of 16 KB
-constexpr int kSmemBytes = kPOff + 3 * 16384 + 1024;
+constexpr int kSmemBytes = kKOff + kNB * 2 * kSub + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSStride = 160;         // S slots at columns [0, 144) and [160, 304)
+constexpr uint32_t kSStride = 160;         // S/P slots at columns [0, 144) and [160, 304)
 constexpr uint32_t kOCol = 320;            // O: columns [320, 448)
 constexpr float kOver = 8.0f;              // log2 of the largest unnormalised weight allowed
 }  // namespace hca_tc
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t b_qraw[2], b_qfull[2], b_qempty[2];
     __shared__ __align__(8) uint64_t b_kfull[kNB], b_kempty[kNB];
-    __shared__ __align__(8) uint64_t b_sfull[2], b_sfree[2], b_pfull, b_pvdone, b_ofull, b_oempty;
+    __shared__ __align__(8) uint64_t b_sfull[2], b_pfull[2], b_pvdone, b_ofull, b_oempty;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -115,9 +116,8 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&b_sfull[i]), 1);
-            mbar_init(smem_u32(&b_sfree[i]), kRows);
+            mbar_init(smem_u32(&b_pfull[i]), kRows);
         }
-        mbar_init(smem_u32(&b_pfull), kRows);
         mbar_init(smem_u32(&b_pvdone), 1);
         mbar_init(smem_u32(&b_ofull), 1);
         mbar_init(smem_u32(&b_oempty), kRows);
@@ -235,17 +235,17 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
             int pv_n = -1, pv_kb = 0, pv_nkeys = 0;  // the tile whose P V is still to issue
             bool pv_first = false, pv_last = false;
             int pv_it = 0;
-            const uint32_t idesc_pv = idesc_bf16(128, 128, 0, 1);  // A = P K-major, B = V MN-major
+            const uint32_t idesc_pv = idesc_bf16(128, 128, 0, 1);  // A = P (TMEM), B = V MN-major
             auto issue_pv = [&]() -> bool {
-                if (!mbar_wait(smem_u32(&b_pfull), pv_n & 1, kWaitNs, &g_abort)) return false;
+                const int psb = pv_n & 1;
+                if (!mbar_wait(smem_u32(&b_pfull[psb]), (pv_n >> 1) & 1, kWaitNs, &g_abort)) return false;
                 if (pv_first && pv_it >= 1 && !mbar_wait(smem_u32(&b_oempty), (pv_it - 1) & 1, kWaitNs, &g_abort))
                     return false;
                 tc_fence_after();
                 const uint32_t kt = s_base + kKOff + pv_kb * 2 * kSub;
                 for (int kk = 0; kk < pv_nkeys / 16; ++kk) {
-                    const uint64_t ad = sdesc_sw128(s_base + kPOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(kt + kk * 2048, kSub, 1024);
-                    mma_bf16(tmem + kOCol, ad, bd, idesc_pv, (!pv_first || kk > 0) ? 1u : 0u);
+                    mma_bf16_ts(tmem + kOCol, tmem + psb * kSStride + kk * 8, bd, idesc_pv, (!pv_first || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&b_kempty[pv_kb]));
                 mma_commit(smem_u32(&b_pvdone));
@@ -261,11 +261,8 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     const int kb = n % kNB, sb = n & 1;
                     const int nkeys = c < I.n_ct ? 128 : P.n_swa;
                     if (!mbar_wait(smem_u32(&b_kfull[kb]), (n / kNB) & 1, kWaitNs, &g_abort)) { ok = false; break; }
-                    // S slot sb is free once the softmax has read S(n - 2)
-                    if (n >= 2 && !mbar_wait(smem_u32(&b_sfree[sb]), ((n >> 1) - 1) & 1, kWaitNs, &g_abort)) {
-                        ok = false;
-                        break;
-                    }
+                    // slot sb last held S(n - 2) / P(n - 2): the softmax had written P(n - 2) before
+                    // P V(n - 2) was issued, and that P V was issued before this S on the same pipe
                     tc_fence_after();
                     const uint32_t kt = s_base + kKOff + kb * 2 * kSub;
                     const uint32_t idesc_s = idesc_bf16(128, nkeys, 0, 0);
@@ -334,9 +331,6 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 float sv[128], sx[16];
                 tmem_ld128_sync(s_addr, sv);
                 if (nk > 128) tmem_ld16_sync(s_addr + 128, sx);
-                // S(n) is in registers: the MMA may write S(n + 2) into this slot
-                tc_fence_before();
-                mbar_arrive(smem_u32(&b_sfree[sb]));
                 // masked keys become -inf; a warp whose rows all see the whole tile skips the masks
                 const bool full = __all_sync(0xffffffffu, lo == 0 && hi >= 128 && nk == 128);
                 if (!full) {
@@ -399,40 +393,33 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
 #pragma unroll
                     for (int e = 0; e < 16; ++e) sx[e] = row_live ? fast_exp2(fmaf(sx[e], P.scale_log2, neg_m)) : 0.0f;
                 }
-                // the P buffer is free once the previous tile's P V has read it
-                if (n >= 1 &&
-                    !__all_sync(0xffffffffu, mbar_wait(smem_u32(&b_pvdone), (n - 1) & 1, kWaitNs, &g_abort))) {
-                    ok = false;
-                    break;
-                }
+                // P as BF16 pairs into the first columns of the slot (its scores are in registers)
                 float ls8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int c0 = 0; c0 < 128; c0 += 16) {
-                    uint32_t pk[8];
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    float w[16];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        ls8[e >> 1] += sv[c0 + e] + sv[c0 + e + 1];
-                        pk[e >> 1] = pack_bf16x2(sv[c0 + e], sv[c0 + e + 1]);
+                    for (int e = 0; e < 32; e += 2) {
+                        ls8[(e >> 1) & 7] += sv[c0 + e] + sv[c0 + e + 1];
+                        w[e >> 1] = __uint_as_float(pack_bf16x2(sv[c0 + e], sv[c0 + e + 1]));
                     }
-                    const int sub = c0 >> 6, ch = (c0 & 63) >> 3;
-                    uint8_t *base = sm + kPOff + sub * 16384;
-                    *reinterpret_cast<uint4 *>(base + sw128_off(r, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(base + sw128_off(r, ch + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    tmem_st16(s_addr + (c0 >> 1), w);
                 }
                 if (nk > 128) {
-                    uint32_t pk[8];
+                    float w[16];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
                         ls8[e >> 1] += sx[e] + sx[e + 1];
-                        pk[e >> 1] = pack_bf16x2(sx[e], sx[e + 1]);
+                        w[e >> 1] = __uint_as_float(pack_bf16x2(sx[e], sx[e + 1]));
                     }
-                    uint8_t *base = sm + kPOff + 2 * 16384;
-                    *reinterpret_cast<uint4 *>(base + sw128_off(r, 0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(base + sw128_off(r, 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+                    for (int e = 8; e < 16; ++e) w[e] = 0.0f;  // columns 72..79: beyond the 144 keys' P
+                    tmem_st16(s_addr + 64, w);
                 }
                 l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-                fence_async_smem();
-                mbar_arrive(smem_u32(&b_pfull));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&b_pfull[sb]));
             }
             if (!ok) break;
             // ---- epilogue of the item: O / (sum + exp(sink)), inverse RoPE, BF16 store ----
