@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
     __shared__ float s_red[8][32];            // cross-warp reduction scratch
     __shared__ __align__(16) float s_fo[kH];  // final output factor per head
     __shared__ int s_cnt[3];                  // producer warps' counts of valid top-k entries
+    __shared__ float4 s_rope[16];             // RoPE (cos, sin) pairs of the current token
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t s_base = smem_u32(sm);
@@ -266,6 +267,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             landed = it + 1;
             // count the valid prefix of the top-k row (ascending, -1 padded) in parallel
             const int32_t *sidx = reinterpret_cast<const int32_t *>(sm + kIdxOff) + qs * P.topk;
+            if (ptid < 16)  // the token's row of the RoPE table, staged for the query rotation below
+                s_rope[ptid] = pos_ok ? __ldg(reinterpret_cast<const float4 *>(P.rope + (int64_t)t * 32) + ptid)
+                                      : make_float4(1.0f, 0.0f, 1.0f, 0.0f);
             int cnt = 0;
             if (!P.dense)
                 for (int i = ptid; i < P.topk; i += kProducers) cnt += (pos_ok && sidx[i] >= 0) ? 1 : 0;
@@ -285,10 +289,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 uint8_t *q1 = sm + kQOff + qs * 16384 + 8192;
                 for (int u = ptid; u < kH * 4; u += kProducers) {
                     const int h = u >> 2, c = u & 3;
-                    const float4 *rp = reinterpret_cast<const float4 *>(P.rope + (int64_t)t * 32 + 8 * c);
                     float4 rc[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) rc[e] = __ldg(rp + e);  // (cos, sin) of pairs 8c .. 8c+7
+                    for (int e = 0; e < 4; ++e) rc[e] = s_rope[4 * c + e];  // (cos, sin) of pairs 8c .. 8c+7
                     uint4 *pa = reinterpret_cast<uint4 *>(q1 + sw128_off(h, c));
                     uint4 *pb = reinterpret_cast<uint4 *>(q1 + sw128_off(h, c + 4));
                     uint4 va = *pa, vb = *pb;

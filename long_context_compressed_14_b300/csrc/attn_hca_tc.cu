@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
     __shared__ __align__(8) uint64_t b_kfull[kNB], b_kempty[kNB];
     __shared__ __align__(8) uint64_t b_sfull[2], b_pfull[2], b_pvdone, b_ofull, b_oempty;
     __shared__ uint32_t tmem_slot;
+    __shared__ float4 s_rope[16][16];  // RoPE (cos, sin) pairs of the item's tokens (T <= 16)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t s_base = smem_u32(sm);
@@ -160,17 +161,24 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 break;
             }
             landed = it + 1;
-            // RoPE on dims 64..127 of every query row at its token's position
+            // RoPE on dims 64..127 of every query row at its token's position; the item's T rows of
+            // the table are staged in shared memory first (one load per lane, no dependent chains)
             if (P.d_rope == 64) {
+                for (int i = lane; i < P.T * 16; i += 32) {
+                    const int t = I.t0 + (i >> 4);
+                    s_rope[i >> 4][i & 15] =
+                        t < P.L ? __ldg(reinterpret_cast<const float4 *>(P.rope + (int64_t)t * 32) + (i & 15))
+                                : make_float4(1.0f, 0.0f, 1.0f, 0.0f);
+                }
+                __syncwarp();
                 uint8_t *q1 = sm + kQOff + qs * 32768 + 16384;
                 for (int u = lane; u < kRows * 4; u += 32) {
                     const int r = u >> 2, c = u & 3;
                     const int t = I.t0 + r / P.H;
                     if (t >= P.L) continue;
-                    const float4 *rp = reinterpret_cast<const float4 *>(P.rope + (int64_t)t * 32 + 8 * c);
                     float4 rc[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) rc[e] = __ldg(rp + e);
+                    for (int e = 0; e < 4; ++e) rc[e] = s_rope[r / P.H][4 * c + e];
                     uint4 *pa = reinterpret_cast<uint4 *>(q1 + sw128_off(r, c));
                     uint4 *pb = reinterpret_cast<uint4 *>(q1 + sw128_off(r, c + 4));
                     uint4 va = *pa, vb = *pb;
@@ -187,6 +195,7 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     *pa = va;
                     *pb = vb;
                 }
+                __syncwarp();  // s_rope is rewritten for the next item
             }
             fence_async_smem();
             mbar_arrive(smem_u32(&b_qfull[qs]));
