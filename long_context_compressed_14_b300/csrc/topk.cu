@@ -8,34 +8,39 @@
 // increasing addresses), padded with -1 when n < k. Deterministic: the selection is a
 // function of the score bits only.
 //
-// Scores map to order-preserving 32-bit keys (score_key). One CTA per query row:
-//  1. histogram of the top 11 key bits (2048 bins) over the row, read once;
-//  2. the bin holding the k-th largest key is found by a suffix scan; every key in a higher
-//     bin is kept (a bit in a shared-memory bitmap), the keys of the threshold bin are
-//     collected with their indices (second read of the row, normally served by L2);
-//  3. an exact radix select over the low 21 bits of the collected keys gives K*, the k-th
-//     largest key, and how many keys equal to K* are taken; they are marked in a second
-//     bitmap (ties: lowest indices first, applied at emission);
-//  4. emission in index order from the two bitmaps with block-wide prefix sums.
-// A threshold bin too large for shared memory (heavy exact ties) is resolved by exact radix
-// passes over the row in global memory instead. Rows of more than kMaxBitmapN entries use the
-// plain four-pass radix select with an ordered compaction.
+// Scores map to order-preserving 32-bit keys (-0 folded onto +0). One CTA of 256 threads per
+// query row, four CTAs per SM:
+//  1. a threshold from a sample of the row (the first 128-byte line of every eight): two
+//     2048-bin histograms of the sampled keys (top 11 bits, then the next 11 inside the chosen
+//     bin) give a 22-bit key that, with a 4-sigma margin on the sampled count, lies below the
+//     k-th largest key;
+//  2. one pass over the row, four float4 loads per thread in flight, collects every key at or
+//     above the threshold (normally ~1.4 k keys) into shared memory;
+//  3. an exact radix select over the collected keys, offset by the threshold, gives K*, the
+//     k-th largest key, and how many keys equal to K* are taken; keys > K* and keys == K* are
+//     marked in two bitmaps;
+//  4. emission in index order from the bitmaps with block-wide prefix sums (ties: lowest
+//     indices first).
+// When the sample misjudges (fewer than k or more than kCandCap keys collected) the exact full
+// path runs instead: a histogram of the whole row, the threshold bin's keys collected (or, when
+// that bin is too large for shared memory, radix passes over the row), then steps 3-4. Rows of
+// more than kMaxBitmapN entries use the plain four-pass radix select with an ordered compaction.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace csa {
 
 namespace tk {
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;            // top 11 key bits
 constexpr int kBinShift = 21;
-constexpr int kCandCap = 4096;         // keys of the threshold bin kept in shared memory
+constexpr int kCandCap = 3584;         // candidate keys kept in shared memory
 constexpr int kMaxBitmapN = 1 << 18;   // rows up to this many entries use the bitmap kernel
 }  // namespace tk
 
 // ---------------------------------------------------------------------------------------
-// block-wide scans (512 threads)
+// block-wide scans
 // ---------------------------------------------------------------------------------------
 
 // Exclusive prefix sum of v across the CTA in thread order; *total = sum. Uses s_tmp[kWarps].
@@ -147,48 +152,35 @@ __device__ __forceinline__ void find_threshold_bin(const uint32_t *hist, int nbi
 // bitmap kernel
 // ---------------------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(tk::kThreads) topk_bitmap_kernel(TopkArgs a) {
+// Canonical order key of a score: -0 folded onto +0 by adding +0 (x + 0 = x otherwise), then
+// the sign-magnitude bits mapped to an unsigned order (larger score -> larger key).
+__device__ __forceinline__ uint32_t key_of(float s) {
+    const uint32_t u = __float_as_uint(s + 0.0f);
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
+// Exact k-th largest key among the n scores of the row, by the full histogram path: keys in
+// higher bins than the k-th are marked in bm_gt, the threshold bin's keys are collected and
+// selected exactly (or, when that bin is too large for shared memory, by radix passes over the
+// row). On return bm_gt holds every key > K*, bm_eq every key == K*; the result is the number
+// of keys == K* to take (lowest indices first).
+__device__ int select_full(const float *S, int n, int k, uint32_t *hist, uint32_t *cand_key, int32_t *cand_idx,
+                           uint32_t *bm_gt, uint32_t *bm_eq, int *s_tmp, int *s_res, int *s_ncand) {
     using namespace tk;
-    extern __shared__ uint32_t dyn[];
-    uint32_t *hist = dyn;                              // [kBins]
-    uint32_t *cand_key = hist + kBins;                 // [kCandCap]
-    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + kCandCap);  // [kCandCap]
-    uint32_t *bm_gt = reinterpret_cast<uint32_t *>(cand_idx + kCandCap);  // [nw]
-    __shared__ int s_tmp[kWarps];
-    __shared__ int s_res[2];
-    __shared__ int s_ncand;
-
-    int64_t t;
-    const float *S;
-    int32_t *out;
-    if (!topk_row(a, blockIdx.x, &t, &S, &out)) return;
-    const int k = a.k;
-    const int n = visible_entries(t, a.m, a.ncap);
-    if (n <= k) {
-        for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
-        return;
-    }
-    const int nw = (n + 31) >> 5;
-    uint32_t *bm_eq = bm_gt + nw;
     for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
-    for (int i = threadIdx.x; i < 2 * nw; i += kThreads) bm_gt[i] = 0;
-    if (threadIdx.x == 0) s_ncand = 0;
+    if (threadIdx.x == 0) *s_ncand = 0;
     __syncthreads();
-
-    // 1. histogram of the top 11 bits
     for_each_key(S, n, [&](int, uint32_t key) { atomicAdd(&hist[key >> kBinShift], 1u); });
     __syncthreads();
     int bstar, above;
     find_threshold_bin(hist, kBins, k, s_tmp, s_res, &bstar, &above);
-    int need = k - above;  // keys still to take from bin bstar (>= 1)
-
-    // 2. keys above the bin are kept; keys of the bin are collected
+    int need = k - above;
     for_each_key(S, n, [&](int i, uint32_t key) {
         const int bin = (int)(key >> kBinShift);
         if (bin > bstar) {
             atomicOr(&bm_gt[i >> 5], 1u << (i & 31));
         } else if (bin == bstar) {
-            const int pos = atomicAdd(&s_ncand, 1);
+            const int pos = atomicAdd(s_ncand, 1);
             if (pos < kCandCap) {
                 cand_key[pos] = key;
                 cand_idx[pos] = i;
@@ -196,11 +188,9 @@ __global__ void __launch_bounds__(tk::kThreads) topk_bitmap_kernel(TopkArgs a) {
         }
     });
     __syncthreads();
-    const int nc = s_ncand;
-    uint32_t kstar;
+    const int nc = *s_ncand;
+    uint32_t prefix = (uint32_t)bstar << kBinShift, mask = ~0u << kBinShift;
     if (nc <= kCandCap) {
-        // 3. exact select inside the bin: low 21 bits in rounds of 7 bits (128 bins)
-        uint32_t prefix = (uint32_t)bstar << kBinShift, mask = ~0u << kBinShift;
         for (int round = 0; round < 3; ++round) {
             const int shift = 14 - 7 * round;
             for (int i = threadIdx.x; i < kThreads; i += kThreads) hist[i] = 0;
@@ -216,7 +206,7 @@ __global__ void __launch_bounds__(tk::kThreads) topk_bitmap_kernel(TopkArgs a) {
             mask |= 127u << shift;
             need -= ab2;
         }
-        kstar = prefix;
+        const uint32_t kstar = prefix;
         for (int c = threadIdx.x; c < nc; c += kThreads) {
             const uint32_t key = cand_key[c];
             const int i = cand_idx[c];
@@ -225,7 +215,6 @@ __global__ void __launch_bounds__(tk::kThreads) topk_bitmap_kernel(TopkArgs a) {
         }
     } else {
         // heavy bin: exact radix rounds over the row in global memory (8 + 8 + 5 bits)
-        uint32_t prefix = (uint32_t)bstar << kBinShift, mask = ~0u << kBinShift;
         const int shifts[3] = {13, 5, 0};
         const int widths[3] = {8, 8, 5};
         for (int round = 0; round < 3; ++round) {
@@ -243,7 +232,7 @@ __global__ void __launch_bounds__(tk::kThreads) topk_bitmap_kernel(TopkArgs a) {
             mask |= wmask << shift;
             need -= ab2;
         }
-        kstar = prefix;
+        const uint32_t kstar = prefix;
         for_each_key(S, n, [&](int i, uint32_t key) {
             if ((key >> kBinShift) != (uint32_t)bstar) return;
             if (key > kstar) atomicOr(&bm_gt[i >> 5], 1u << (i & 31));
@@ -251,8 +240,12 @@ __global__ void __launch_bounds__(tk::kThreads) topk_bitmap_kernel(TopkArgs a) {
         });
     }
     __syncthreads();
+    return need;
+}
 
-    // 4. emission in index order: every gt bit, and the first `need` eq bits
+// Emission in index order from the bitmaps: every gt bit and the first `need` eq bits.
+__device__ void emit_selection(uint32_t *bm_gt, uint32_t *bm_eq, int nw, int need, int k, int32_t *out, int *s_tmp) {
+    using namespace tk;
     const int per = (nw + kThreads - 1) / kThreads;
     const int w0 = threadIdx.x * per, w1 = min(nw, w0 + per);
     int my_eq = 0;
@@ -277,16 +270,210 @@ __global__ void __launch_bounds__(tk::kThreads) topk_bitmap_kernel(TopkArgs a) {
     int tot_sel;
     int pos = block_excl_sum(my_sel, s_tmp, &tot_sel);
     for (int w = w0; w < w1; ++w) {
-        uint32_t s = bm_gt[w] | bm_eq[w];
-        while (s) {
-            const int bit = __ffs(s) - 1;
-            s &= s - 1u;
+        uint32_t sl = bm_gt[w] | bm_eq[w];
+        while (sl) {
+            const int bit = __ffs(sl) - 1;
+            sl &= sl - 1u;
             if (pos < k) out[pos] = 32 * w + bit;
             ++pos;
         }
     }
     if (tot_sel != k) set_status(CSA_ERR_BOUNDS);  // cannot happen: the select keeps exactly k
     for (int i = tot_sel + threadIdx.x; i < k; i += kThreads) out[i] = -1;
+}
+
+// Appends the kept scores of one float4 per lane (up to four each) to the candidate list; one
+// shared atomic per warp. Positions beyond kCandCap are counted but not stored.
+__device__ __forceinline__ void warp_append4(const bool p[4], const uint32_t key[4], int i0, int *s_ncand,
+                                             uint32_t *cand_key, int32_t *cand_idx, int lane) {
+    unsigned b[4];
+    int tot = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        b[e] = __ballot_sync(0xffffffffu, p[e]);
+        tot += __popc(b[e]);
+    }
+    if (tot == 0) return;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(s_ncand, tot);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if (p[e]) {
+            const int pos = base + __popc(b[e] & lt);
+            if (pos < tk::kCandCap) {
+                cand_key[pos] = key[e];
+                cand_idx[pos] = i0 + e;
+            }
+        }
+        base += __popc(b[e]);
+    }
+}
+
+// Visits the sampled float4s of a row: the first 128-byte line of every 8 (one eighth of the
+// row, whole lines so that the sample costs one eighth of the row's DRAM sectors).
+template <typename F>
+__device__ __forceinline__ void for_each_sample(const float4 *S4, int n4, F &&fn) {
+    for (int s = threadIdx.x;; s += tk::kThreads) {
+        const int j = ((s >> 3) << 6) | (s & 7);
+        if (j >= n4) break;
+        fn(__ldcg(S4 + j));
+    }
+}
+__device__ __forceinline__ int sample_count(int n4) {  // float4s visited by for_each_sample
+    return 8 * (n4 >> 6) + min(8, n4 & 63);
+}
+
+// Main kernel, one CTA per row.
+// A. (rows longer than kCandCap) threshold from the sample: histograms of the sampled keys'
+//    top 11 bits and then of the next 11 bits inside the chosen bin give the 22-bit key prefix
+//    where the sampled count from the top reaches the scaled k plus a 4-sigma margin.
+// B. one pass over the row (four float4 per thread in flight) collects every key at or above
+//    the threshold, with its index, into shared memory.
+// C. when at least k and at most kCandCap keys were collected, the k-th largest key K* is among
+//    them: radix rounds over d = key - threshold (the first round spans the collected range,
+//    the next ones the remaining low bits, at most 11 per round) give K* and the number of keys
+//    equal to it to take; keys above and equal to K* are marked in two bitmaps. Otherwise the
+//    sample misjudged and the exact full path runs.
+// D. emission in index order.
+__global__ void __launch_bounds__(tk::kThreads, 4) topk_bitmap_kernel(TopkArgs a) {
+    using namespace tk;
+    extern __shared__ uint32_t dyn[];
+    uint32_t *hist = dyn;                              // [kBins]
+    uint32_t *cand_key = hist + kBins;                 // [kCandCap]
+    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + kCandCap);  // [kCandCap]
+    uint32_t *bm_gt = reinterpret_cast<uint32_t *>(cand_idx + kCandCap);  // [nw]
+    __shared__ int s_tmp[kWarps];
+    __shared__ int s_res[2];
+    __shared__ int s_ncand;
+
+    int64_t t;
+    const float *S;
+    int32_t *out;
+    if (!topk_row(a, blockIdx.x, &t, &S, &out)) return;
+    const int k = a.k;
+    const int n = visible_entries(t, a.m, a.ncap);
+    if (n <= k) {
+        for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    const int nw = (n + 31) >> 5;
+    uint32_t *bm_eq = bm_gt + nw;
+    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+    for (int i = threadIdx.x; i < 2 * nw; i += kThreads) bm_gt[i] = 0;
+    if (threadIdx.x == 0) s_ncand = 0;
+    __syncthreads();
+
+    const int n4 = n >> 2;
+    const float4 *S4 = reinterpret_cast<const float4 *>(S);
+    // A. threshold
+    uint32_t thr = 0;
+    if (n > kCandCap) {
+        for_each_sample(S4, n4, [&](float4 v) {
+            atomicAdd(&hist[key_of(v.x) >> kBinShift], 1u);
+            atomicAdd(&hist[key_of(v.y) >> kBinShift], 1u);
+            atomicAdd(&hist[key_of(v.z) >> kBinShift], 1u);
+            atomicAdd(&hist[key_of(v.w) >> kBinShift], 1u);
+        });
+        __syncthreads();
+        const int ns = 4 * sample_count(n4);
+        const float expect = (float)k * (float)ns / (float)n;
+        const int ks = min(ns, (int)ceilf(expect + 4.0f * sqrtf(expect) + 4.0f));
+        int bin, above;
+        find_threshold_bin(hist, kBins, ks, s_tmp, s_res, &bin, &above);
+        for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        for_each_sample(S4, n4, [&](float4 v) {
+            const uint32_t q[4] = {key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if ((int)(q[e] >> kBinShift) == bin) atomicAdd(&hist[(q[e] >> 10) & (kBins - 1)], 1u);
+        });
+        __syncthreads();
+        int bin2, above2;
+        find_threshold_bin(hist, kBins, ks - above, s_tmp, s_res, &bin2, &above2);
+        thr = ((uint32_t)bin << kBinShift) | ((uint32_t)bin2 << 10);
+    }
+    // B. collection
+    constexpr int kU = 4;
+    for (int i0 = 0; i0 < n4; i0 += kU * kThreads) {
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i4 = i0 + u * kThreads + threadIdx.x;
+            v[u] = i4 < n4 ? __ldcs(S4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i4 = i0 + u * kThreads + threadIdx.x;
+            const bool live = i4 < n4;
+            const uint32_t q[4] = {key_of(v[u].x), key_of(v[u].y), key_of(v[u].z), key_of(v[u].w)};
+            const bool p[4] = {live && q[0] >= thr, live && q[1] >= thr, live && q[2] >= thr, live && q[3] >= thr};
+            if (__any_sync(0xffffffffu, p[0] || p[1] || p[2] || p[3]))
+                warp_append4(p, q, 4 * i4, &s_ncand, cand_key, cand_idx, lane);
+        }
+    }
+    if (threadIdx.x < 32) {  // the last n % 4 scores
+        const int i = 4 * n4 + lane;
+        const bool live = i < n;
+        const uint32_t key = live ? key_of(__ldcg(S + i)) : 0u;
+        const bool p[4] = {live && key >= thr, false, false, false};
+        const uint32_t q[4] = {key, 0u, 0u, 0u};
+        if (__any_sync(0xffffffffu, p[0])) warp_append4(p, q, i, &s_ncand, cand_key, cand_idx, lane);
+    }
+    __syncthreads();
+    const int nc = s_ncand;
+    __syncthreads();  // every thread has read the count before the full path may reset it
+    int need;
+    if (nc >= k && nc <= kCandCap) {
+        // C. exact K* among the candidates, on d = key - thr (every candidate has key >= thr)
+        uint32_t dmax = 0;
+        for (int c = threadIdx.x; c < nc; c += kThreads) dmax = max(dmax, cand_key[c] - thr);
+        dmax = __reduce_max_sync(0xffffffffu, dmax);
+        if (lane == 0) s_tmp[threadIdx.x >> 5] = (int)dmax;
+        __syncthreads();
+        dmax = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) dmax = max(dmax, (uint32_t)s_tmp[w]);
+        __syncthreads();
+        // round 1 bins d >> shift (< kBins); later rounds take the next <= 11 bits below
+        int shift = dmax == 0u ? 0 : max(0, 32 - __clz(dmax) - 11);
+        uint32_t prefix = 0, mask = 0, wmask = ~0u;
+        need = k;
+        while (true) {
+            for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+            __syncthreads();
+            for (int c = threadIdx.x; c < nc; c += kThreads) {
+                const uint32_t d = cand_key[c] - thr;
+                if ((d & mask) == prefix) atomicAdd(&hist[(d >> shift) & wmask], 1u);
+            }
+            __syncthreads();
+            int b2, ab2;
+            find_threshold_bin(hist, kBins, need, s_tmp, s_res, &b2, &ab2);
+            prefix |= (uint32_t)b2 << shift;
+            mask |= wmask << shift;
+            need -= ab2;
+            if (shift == 0) break;
+            const int next = max(0, shift - 11);
+            wmask = (1u << (shift - next)) - 1u;
+            shift = next;
+        }
+        const uint32_t dstar = prefix;
+        for (int c = threadIdx.x; c < nc; c += kThreads) {
+            const uint32_t d = cand_key[c] - thr;
+            const int i = cand_idx[c];
+            if (d > dstar) atomicOr(&bm_gt[i >> 5], 1u << (i & 31));
+            else if (d == dstar) atomicOr(&bm_eq[i >> 5], 1u << (i & 31));
+        }
+        __syncthreads();
+    } else {
+        // the sample misjudged (too few or too many candidates): exact full path
+        need = select_full(S, n, k, hist, cand_key, cand_idx, bm_gt, bm_eq, s_tmp, s_res, &s_ncand);
+    }
+    // D. emission in index order
+    emit_selection(bm_gt, bm_eq, nw, need, k, out, s_tmp);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -375,6 +562,7 @@ void launch_topk(const TopkArgs &a, cudaStream_t st) {
         const int nw = (a.ncap + 31) / 32;
         const size_t smem = sizeof(uint32_t) * ((size_t)kBins + 2 * kCandCap + 2 * (size_t)nw);
         cudaFuncSetAttribute(topk_bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(topk_bitmap_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         topk_bitmap_kernel<<<a.nrows, kThreads, smem, st>>>(a);
     } else {
         topk_radix_kernel<<<a.nrows, kThreads, 0, st>>>(a);
