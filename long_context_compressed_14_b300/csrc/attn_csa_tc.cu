@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 }
                 // fetch the next token's rows once its slot is free (never blocking here)
                 if (ptid == 0 && fetched == it + 1 && it + 1 < n_tok_cta &&
-                    (it + 1 < 2 || mbar_try_wait(smem_u32(&b_qempty[(it + 1) & 1]), (((it + 1) >> 1) - 1) & 1))) {
+                    (it + 1 < 2 || mbar_test_wait(smem_u32(&b_qempty[(it + 1) & 1]), (((it + 1) >> 1) - 1) & 1))) {
                     fetch(it + 1);
                     fetched = it + 2;
                 }

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     }
                     // prefetch the next item's query rows once its slot is free (never blocking)
                     if (fetched == it + 1 && it + 1 < n_it_cta &&
-                        (it + 1 < 2 || mbar_try_wait(smem_u32(&b_qempty[(it + 1) & 1]), (((it + 1) >> 1) - 1) & 1))) {
+                        (it + 1 < 2 || mbar_test_wait(smem_u32(&b_qempty[(it + 1) & 1]), (((it + 1) >> 1) - 1) & 1))) {
                         fetch_q(it + 1);
                         fetched = it + 2;
                     }

@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
             mbar_init(smem_u32(&b_qfull[i]), 1);
             mbar_init(smem_u32(&b_qempty[i]), 1);
             mbar_init(smem_u32(&b_dfull[i]), 1);
-            mbar_init(smem_u32(&b_dempty[i]), kEpi);
+            mbar_init(smem_u32(&b_dempty[i]), kEpi / 32);  // one arrival per epilogue warp
         }
         for (int i = 0; i < kNK; ++i) {
             mbar_init(smem_u32(&b_kfull[i]), 1);
@@ -120,13 +120,25 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
             while (mq < P.n_qt && ok) {
                 while (lq < P.n_qt && ln - mn < kNK) {
                     const int net = n_et_of(lq);
+                    const int kb = ln % kNK;
+                    if (ln >= kNK) {
+                        // the slot's last reader is MMA ln - kNK: block only when no MMA is
+                        // pending, otherwise issue MMAs first and come back (checked before the
+                        // query load so that nothing is issued twice)
+                        const uint32_t par = ((ln / kNK) - 1) & 1;
+                        if (ln == mn) {
+                            if (!mbar_wait(smem_u32(&b_kempty[kb]), par, kWaitNs, &g_abort)) { ok = false; break; }
+                        } else if (!mbar_test_wait(smem_u32(&b_kempty[kb]), par)) {
+                            break;
+                        }
+                    }
                     if (le == 0) {
                         const int qb = lqn & 1;
                         if (lqn >= 2) {
                             const uint32_t par = ((lqn >> 1) - 1) & 1;
                             if (ln == mn) {
                                 if (!mbar_wait(smem_u32(&b_qempty[qb]), par, kWaitNs, &g_abort)) { ok = false; break; }
-                            } else if (!mbar_try_wait(smem_u32(&b_qempty[qb]), par)) {
+                            } else if (!mbar_test_wait(smem_u32(&b_qempty[qb]), par)) {
                                 break;  // do MMA work first
                             }
                         }
@@ -134,8 +146,6 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
                         tma_load_3d(s_base + kQOff + qb * kQBytes, &P.mq, smem_u32(&b_qfull[qb]), 0,
                                     (int)(((int64_t)P.b * P.L + P.t0 + lq * TQ) * HI), 0);
                     }
-                    const int kb = ln % kNK;
-                    if (ln >= kNK && !mbar_wait(smem_u32(&b_kempty[kb]), ((ln / kNK) - 1) & 1, kWaitNs, &g_abort)) { ok = false; break; }
                     mbar_expect_tx(smem_u32(&b_kfull[kb]), kKBytes);
                     tma_load_3d(s_base + kKOff + kb * kKBytes, &P.mk, smem_u32(&b_kfull[kb]), 0, P.b * P.ncap + le * kJ, 0);
                     ++ln;
@@ -170,14 +180,20 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
         }
     } else {
         // ---- epilogue: warpgroup g = warp / 4 takes the columns [g*C, (g+1)*C) of D, i.e.
-        // tokens [g*C/HI, (g+1)*C/HI) of the query tile; thread = one entry of the tile ----
+        // tokens [g*C/HI, (g+1)*C/HI) of the query tile; thread = one entry of the tile. The C
+        // columns are read as two halves of 32: the second half's TMEM load and the next tile's
+        // first half are in flight while the tokens of the half already in registers are
+        // computed, and the entry scales are fetched one tile ahead. Warps only meet at the end
+        // of a query tile; a failed wait is a warp-uniform decision ----
         constexpr int C = kN / kEpiWG;  // 64 columns
         constexpr int TW = C / HI;      // tokens per warpgroup
+        constexpr int TH = TW / 2;      // tokens per 32-column half
         const int g = warp >> 2;
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        auto ewait = [&](uint32_t bar, uint32_t par) -> bool {
-            const bool w = mbar_wait(bar, par, kWaitNs, &g_abort);
-            return !named_sync_or(kBarEpi, kEpi, !w);
+        const uint32_t tcol = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + g * C;
+        const float *kscale = P.k_scale + (int64_t)P.b * P.ncap;
+        const int jl = 32 * (warp & 3) + lane;  // this thread's entry within a tile
+        auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, par, kWaitNs, &g_abort));
         };
         int n = 0;
         for (int qt = blockIdx.x; qt < P.n_qt && ok; qt += gridDim.x) {
@@ -197,36 +213,69 @@ __global__ void __launch_bounds__(idx_tc::kThreads, 1) indexer_tc_kernel(const _
             named_sync(kBarEpi, kEpi);
             const int t_g = tq0 + g * TW;  // first token of this warpgroup
             float *srow0 = P.S + (int64_t)(t_g - P.t0) * P.ldS;
-            for (int et = 0; et < n_et; ++et, ++n) {
-                const int db = n & 1;
-                if (!ewait(smem_u32(&b_dfull[db]), (n >> 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                float v[C];
-                tmem_ld64_sync(tmem + lane_base + db * kN + g * C, v);
-                // the accumulators are in registers: hand the TMEM buffer back to the MMA
-                tc_fence_before();
-                mbar_arrive(smem_u32(&b_dempty[db]));
-                const int j = et * kJ + 32 * (warp & 3) + lane;  // this thread's entry
-                const int t_first = (j + 1) * P.m - 1;            // first token that sees entry j
-                const float sk = j < P.ncap ? P.k_scale[(int64_t)P.b * P.ncap + j] : 0.0f;
+            const float4 *wq4 = reinterpret_cast<const float4 *>(s_wq + g * TW * HI);
+            // scores of tokens [q0, q0 + TH) of entry j from one 32-column half; the heads are
+            // summed as two interleaved partial sums (even and odd heads) in packed FP32 pairs.
+            // `full`: every token of the warpgroup sees the whole tile and lies in the chunk
+            auto tokens = [&](const uint32_t (&r)[32], int q0, int j, float sk, bool full) {
+                const int t_first = (j + 1) * P.m - 1;  // first token that sees entry j
+                float *dst = srow0 + (int64_t)q0 * P.ldS + j;
 #pragma unroll
-                for (int q = 0; q < TW; ++q) {
-                    const int t = t_g + q;
-                    const float4 *wq = reinterpret_cast<const float4 *>(s_wq + (g * TW + q) * HI);
-                    float s = 0.0f;
+                for (int q = 0; q < TH; ++q) {
+                    const int t = t_g + q0 + q;
+                    uint64_t acc = 0;
 #pragma unroll
                     for (int h4 = 0; h4 < HI / 4; ++h4) {
-                        const float4 w4 = wq[h4];
-                        s = fmaf(w4.x, fmaxf(v[q * HI + 4 * h4 + 0], 0.0f), s);
-                        s = fmaf(w4.y, fmaxf(v[q * HI + 4 * h4 + 1], 0.0f), s);
-                        s = fmaf(w4.z, fmaxf(v[q * HI + 4 * h4 + 2], 0.0f), s);
-                        s = fmaf(w4.w, fmaxf(v[q * HI + 4 * h4 + 3], 0.0f), s);
+                        const float4 w4 = wq4[((q0 + q) * HI) / 4 + h4];
+                        const uint32_t *x = r + q * HI + 4 * h4;
+                        acc = f2_fma(f2_pack(w4.x, w4.y),
+                                     f2_pack(fmaxf(__uint_as_float(x[0]), 0.0f), fmaxf(__uint_as_float(x[1]), 0.0f)), acc);
+                        acc = f2_fma(f2_pack(w4.z, w4.w),
+                                     f2_pack(fmaxf(__uint_as_float(x[2]), 0.0f), fmaxf(__uint_as_float(x[3]), 0.0f)), acc);
                     }
-                    s = s * sk + 0.0f;  // + 0 turns -0 into +0
-                    if (t >= t_first && t <= last_row) srow0[(int64_t)q * P.ldS + j] = s;
+                    const float2 a2 = f2_unpack(acc);
+                    const float s = fmaf(a2.x + a2.y, sk, 0.0f);  // + 0 turns -0 into +0
+                    if (full || (t >= t_first && t <= last_row)) *dst = s;
+                    dst += P.ldS;
                 }
+            };
+            uint32_t ra[32], rb[32];
+            float sk_next = jl < P.ncap ? kscale[jl] : 0.0f;
+            if (wwait(smem_u32(&b_dfull[n & 1]), (n >> 1) & 1)) {
+                tc_fence_after();
+                tmem_ld32_async(tcol + (n & 1) * kN, ra);
+            } else {
+                ok = false;
+                if (lane == 0) set_timeout();
             }
-            named_sync(kBarEpi, kEpi);  // s_wq is rewritten for the next query tile
+            for (int et = 0; et < n_et && ok; ++et, ++n) {
+                const int db = n & 1;
+                const int j = et * kJ + jl;
+                const float sk = sk_next;
+                // the last entry of the tile is visible to the warpgroup's first token
+                const bool full = ((et + 1) * kJ) * P.m - 1 <= t_g && t_g + TW - 1 <= last_row;
+                if (et + 1 < n_et) sk_next = j + kJ < P.ncap ? kscale[j + kJ] : 0.0f;
+                tmem_wait_hold32(ra);
+                tmem_ld32_async(tcol + db * kN + 32, rb);
+                tokens(ra, 0, j, sk, full);
+                tmem_wait_hold32(rb);
+                // both halves are in registers: hand the TMEM buffer back to the MMA
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&b_dempty[db]));
+                if (et + 1 < n_et) {
+                    if (wwait(smem_u32(&b_dfull[db ^ 1]), ((n + 1) >> 1) & 1)) {
+                        tc_fence_after();
+                        tmem_ld32_async(tcol + (db ^ 1) * kN, ra);
+                    } else {
+                        ok = false;
+                        if (lane == 0) set_timeout();
+                    }
+                }
+                tokens(rb, TH, j, sk, full);
+            }
+            // s_wq is rewritten for the next query tile; a failure anywhere stops every warp
+            ok = !named_sync_or(kBarEpi, kEpi, !ok);
         }
         if (!ok && tid == 0) set_timeout();
     }
