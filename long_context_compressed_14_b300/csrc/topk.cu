@@ -14,11 +14,12 @@
 //     2048-bin histograms of the sampled keys (top 11 bits, then the next 11 inside the chosen
 //     bin) give a 22-bit key that, with a 4-sigma margin on the sampled count, lies below the
 //     k-th largest key;
-//  2. one pass over the row, four float4 loads per thread in flight, collects every key at or
-//     above the threshold (normally ~1.4 k keys) into shared memory;
-//  3. an exact radix select over the collected keys, offset by the threshold, gives K*, the
-//     k-th largest key, and how many keys equal to K* are taken; keys > K* and keys == K* are
-//     marked in two bitmaps;
+//  2. one pass over the row, four float4 loads per thread in flight, compares every score with
+//     the threshold and writes the indices of those at or above it (normally ~1.4 k) to shared
+//     memory;
+//  3. an exact radix select over the collected keys (gathered from the row, still in L2),
+//     offset by the threshold, gives K*, the k-th largest key, and how many keys equal to K*
+//     are taken; keys > K* and keys == K* are marked in two bitmaps;
 //  4. emission in index order from the bitmaps with block-wide prefix sums (ties: lowest
 //     indices first).
 // When the sample misjudges (fewer than k or more than kCandCap keys collected) the exact full
@@ -159,6 +160,13 @@ __device__ __forceinline__ uint32_t key_of(float s) {
     return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
+// The smallest float whose key (key_of) is at least `key`: a float v (not NaN) has
+// key_of(v) >= key exactly when v >= key_floor_value(key). Keys up to that of -inf give -inf.
+__device__ __forceinline__ float key_floor_value(uint32_t key) {
+    if (key <= 0x007FFFFFu) return -INFINITY;
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 // Exact k-th largest key among the n scores of the row, by the full histogram path: keys in
 // higher bins than the k-th are marked in bm_gt, the threshold bin's keys are collected and
 // selected exactly (or, when that bin is too large for shared memory, by radix passes over the
@@ -282,35 +290,6 @@ __device__ void emit_selection(uint32_t *bm_gt, uint32_t *bm_eq, int nw, int nee
     for (int i = tot_sel + threadIdx.x; i < k; i += kThreads) out[i] = -1;
 }
 
-// Appends the kept scores of one float4 per lane (up to four each) to the candidate list; one
-// shared atomic per warp. Positions beyond kCandCap are counted but not stored.
-__device__ __forceinline__ void warp_append4(const bool p[4], const uint32_t key[4], int i0, int *s_ncand,
-                                             uint32_t *cand_key, int32_t *cand_idx, int lane) {
-    unsigned b[4];
-    int tot = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        b[e] = __ballot_sync(0xffffffffu, p[e]);
-        tot += __popc(b[e]);
-    }
-    if (tot == 0) return;
-    int base = 0;
-    if (lane == 0) base = atomicAdd(s_ncand, tot);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        if (p[e]) {
-            const int pos = base + __popc(b[e] & lt);
-            if (pos < tk::kCandCap) {
-                cand_key[pos] = key[e];
-                cand_idx[pos] = i0 + e;
-            }
-        }
-        base += __popc(b[e]);
-    }
-}
-
 // Visits the sampled float4s of a row: the first 128-byte line of every 8 (one eighth of the
 // row, whole lines so that the sample costs one eighth of the row's DRAM sectors).
 template <typename F>
@@ -329,8 +308,8 @@ __device__ __forceinline__ int sample_count(int n4) {  // float4s visited by for
 // A. (rows longer than kCandCap) threshold from the sample: histograms of the sampled keys'
 //    top 11 bits and then of the next 11 bits inside the chosen bin give the 22-bit key prefix
 //    where the sampled count from the top reaches the scaled k plus a 4-sigma margin.
-// B. one pass over the row (four float4 per thread in flight) collects every key at or above
-//    the threshold, with its index, into shared memory.
+// B. one pass over the row (four float4 per thread in flight) collects the indices of the
+//    scores at or above the threshold into shared memory.
 // C. when at least k and at most kCandCap keys were collected, the k-th largest key K* is among
 //    them: radix rounds over d = key - threshold (the first round spans the collected range,
 //    the next ones the remaining low bits, at most 11 per round) give K* and the number of keys
@@ -396,41 +375,71 @@ __global__ void __launch_bounds__(tk::kThreads, 4) topk_bitmap_kernel(TopkArgs a
         find_threshold_bin(hist, kBins, ks - above, s_tmp, s_res, &bin2, &above2);
         thr = ((uint32_t)bin << kBinShift) | ((uint32_t)bin2 << 10);
     }
-    // B. collection
+    // B. collection of the candidate indices. The threshold is compared as a float (the
+    // smallest float whose key is thr); each lane covers four float4s per batch as a 16-bit
+    // mask, one warp scan of the mask counts gives the positions and only the kept indices are
+    // written. Keys are gathered for the candidates afterwards.
+    const float thr_f = key_floor_value(thr);
     constexpr int kU = 4;
     for (int i0 = 0; i0 < n4; i0 += kU * kThreads) {
         float4 v[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int i4 = i0 + u * kThreads + threadIdx.x;
-            v[u] = i4 < n4 ? __ldcs(S4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[u] = i4 < n4 ? __ldcs(S4 + i4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
+        uint32_t mask = 0;
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            const int i4 = i0 + u * kThreads + threadIdx.x;
-            const bool live = i4 < n4;
-            const uint32_t q[4] = {key_of(v[u].x), key_of(v[u].y), key_of(v[u].z), key_of(v[u].w)};
-            const bool p[4] = {live && q[0] >= thr, live && q[1] >= thr, live && q[2] >= thr, live && q[3] >= thr};
-            if (__any_sync(0xffffffffu, p[0] || p[1] || p[2] || p[3]))
-                warp_append4(p, q, 4 * i4, &s_ncand, cand_key, cand_idx, lane);
+            const uint32_t live = (i0 + u * kThreads + threadIdx.x < n4) ? 0xFu : 0u;
+            const uint32_t m4 = (v[u].x >= thr_f ? 1u : 0u) | (v[u].y >= thr_f ? 2u : 0u) |
+                                (v[u].z >= thr_f ? 4u : 0u) | (v[u].w >= thr_f ? 8u : 0u);
+            mask |= (m4 & live) << (4 * u);
+        }
+        const int c = __popc(mask);
+        if (__any_sync(0xffffffffu, c != 0)) {
+            int x = c;  // inclusive warp scan of the counts
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            int base = 0;
+            if (lane == 31) base = atomicAdd(&s_ncand, x);
+            int pos = __shfl_sync(0xffffffffu, base, 31) + x - c;
+            const int ibase = 4 * (i0 + threadIdx.x);
+            while (mask) {
+                const int bit = __ffs(mask) - 1;
+                mask &= mask - 1u;
+                if (pos < kCandCap) cand_idx[pos] = ibase + (bit >> 2) * (4 * kThreads) + (bit & 3);
+                ++pos;
+            }
         }
     }
     if (threadIdx.x < 32) {  // the last n % 4 scores
         const int i = 4 * n4 + lane;
-        const bool live = i < n;
-        const uint32_t key = live ? key_of(__ldcg(S + i)) : 0u;
-        const bool p[4] = {live && key >= thr, false, false, false};
-        const uint32_t q[4] = {key, 0u, 0u, 0u};
-        if (__any_sync(0xffffffffu, p[0])) warp_append4(p, q, i, &s_ncand, cand_key, cand_idx, lane);
+        const bool keep = i < n && __ldcg(S + i) >= thr_f;
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (m != 0u) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&s_ncand, __popc(m));
+            const int pos = __shfl_sync(0xffffffffu, base, 0) + __popc(m & ((1u << lane) - 1u));
+            if (keep && pos < kCandCap) cand_idx[pos] = i;
+        }
     }
     __syncthreads();
     const int nc = s_ncand;
     __syncthreads();  // every thread has read the count before the full path may reset it
     int need;
     if (nc >= k && nc <= kCandCap) {
-        // C. exact K* among the candidates, on d = key - thr (every candidate has key >= thr)
+        // C. exact K* among the candidates, on d = key - thr (every candidate has key >= thr);
+        // the candidates' keys are gathered from the row (still in L2)
         uint32_t dmax = 0;
-        for (int c = threadIdx.x; c < nc; c += kThreads) dmax = max(dmax, cand_key[c] - thr);
+        for (int c = threadIdx.x; c < nc; c += kThreads) {
+            const uint32_t key = key_of(__ldcg(S + cand_idx[c]));
+            cand_key[c] = key;
+            dmax = max(dmax, key - thr);
+        }
         dmax = __reduce_max_sync(0xffffffffu, dmax);
         if (lane == 0) s_tmp[threadIdx.x >> 5] = (int)dmax;
         __syncthreads();
