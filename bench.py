@@ -349,7 +349,7 @@ def run_mine(args, rank, world, local_rank):
         t = stage_ms[dom] / args.steps / 1e3
         ach = amount / t / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_sus"], "traffic": None,
+                "frac": ach / pk["bf16_sus"], "traffic": measured_traffic(dom, wl.B * wl.L),
                 "peak_note": f"bf16 dense sustained ({pk['src']}); the kernel is timed inside a long step"}
     elif wl.kind == "decode":
         dom = max(stage_ms, key=lambda n: stage_ms[n])
@@ -394,6 +394,47 @@ def decode_bytes(wl, csa):
     else:
         by += B * (wl.L // wl.m_hca) * d * act
     return by
+
+
+# DRAM traffic of the dominant kernel, from an ncu capture summarised under profiles/: the file
+# records the bytes read + written by one launch, the query tokens that launch processed and a
+# SHA-256 over the kernel's sources at capture time. The figure is scaled to the timed launch by
+# tokens and reported only while the sources still hash the same (otherwise null).
+TRAFFIC_RECORDS = {
+    "csa.attention": ("ncu_csa_tc_pair_mixed_L32768.md",
+                      ("attn_csa_tc.cu", "umma.cuh", "common.cuh", "kernels.cuh", "tma_host.cuh")),
+}
+
+
+def kernel_source_hash(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "long_context_compressed_14_b300", "csrc")
+    for f in files:
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(stage: str, tokens: int):
+    rec = TRAFFIC_RECORDS.get(stage)
+    if rec is None:
+        return None
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", rec[0])
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and line.strip().startswith("- `"):
+                k, v = line.strip()[3:].split("`:", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    try:
+        if fields["source_sha256"] != kernel_source_hash(rec[1]):
+            return None
+        return float(fields["traffic_bytes_per_launch"]) * tokens / float(fields["tokens_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def workload_config(wl, big_inputs):

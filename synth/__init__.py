@@ -54,7 +54,7 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads of the method's benchmark set.
+# The five workloads of the method's benchmark set, plus a profiler-sized copy of the pair.
 WORKLOADS = {
     # CSA prefill, one sequence, fp32 end to end (bit-exact top-k workload).
     "csa_f32_L2048": Workload("csa_f32_L2048", "csa", B=1, L=2048, H=8, seed=0, H_I=4, topk=32,
@@ -68,6 +68,10 @@ WORKLOADS = {
     # Interleaved CSA + HCA layer pair, L = 262144, mixed-precision KV entries, top-1024.
     "pair_mixed_L262144": Workload("pair_mixed_L262144", "pair", B=1, L=262144, H=64, seed=4,
                                    topk=1024, c_t="mixed"),
+    # The same layer pair at one eighth of the length: a profiler-sized case of the same kernels
+    # (identical per-token configuration; the compressed caches fit L2 at both lengths).
+    "pair_mixed_L32768": Workload("pair_mixed_L32768", "pair", B=1, L=32768, H=64, seed=4,
+                                  topk=1024, c_t="mixed"),
 }
 
 
