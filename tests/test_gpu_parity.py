@@ -166,6 +166,32 @@ def test_index_topk_f32_long_rows(lib, L, m, k):
     np.testing.assert_array_equal(out.cpu().numpy()[0][rows], oracle.topk(s, m, rows, k))
 
 
+def test_index_topk_sample_misjudged(lib):
+    # Rows longer than the shared-memory candidate store estimate their threshold from a sample
+    # made of the first 32 entries of every 256. Here exactly those entries score high and all
+    # others near zero, so the sample overrates the row: fewer than k scores reach its
+    # threshold and the exact full path must take over. Bit-exact against the oracle.
+    L, m, H_I, k = 9000, 1, 2, 1024
+    g = torch.Generator().manual_seed(23)
+    u = torch.randn((64,), generator=g)
+    qI = torch.zeros((1, L, H_I, 64))
+    qI[0, :, 0, :] = u
+    KI = 0.01 * torch.randn((1, L, 64), generator=g)
+    hot = (torch.arange(L) % 256) < 32
+    KI[0, hot] += 4.0 * u + 0.1 * torch.randn((int(hot.sum()), 64), generator=g)
+    w = torch.zeros((1, L, H_I))
+    w[0, :, 0] = 1.0
+    p = lib.make_params(B=1, L=L, H=8, m=m, topk=k, H_I=H_I, act="f32", kv="f32", idx="f32")
+    out = torch.empty((1, L, k), dtype=torch.int32, device=DEV)
+    lib.csa_index_topk(p, (qI.to(DEV), None), (KI.to(DEV), None), w.to(DEV), out,
+                       lib.alloc_workspace(p, lib.OP_INDEX_TOPK))
+    rows = np.concatenate([np.arange(L - 20, L), np.arange(3600, 3620), np.arange(6000, 6010)])
+    s = oracle.index_scores_f32(qI[0].numpy()[rows], KI[0].numpy(), w[0].numpy()[rows], m, rows)
+    np.testing.assert_array_equal(out.cpu().numpy()[0][rows], oracle.topk(s, m, rows, k))
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
+
+
 def test_index_topk_heavy_ties(lib):
     # Rows whose weights are all zero score 0 everywhere: the threshold bin holds every entry
     # (more than fits in shared memory), and the lowest indices must win. Rows with a single
