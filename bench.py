@@ -416,11 +416,13 @@ def kernel_source_hash(files) -> str:
     return h.hexdigest()
 
 
-def measured_traffic(stage: str, tokens: int):
+def measured_traffic(stage: str, tokens: int, profiles_dir: str | None = None):
     rec = TRAFFIC_RECORDS.get(stage)
     if rec is None:
         return None
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", rec[0])
+    if profiles_dir is None:
+        profiles_dir = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
+    path = os.path.join(profiles_dir, rec[0])
     if not os.path.exists(path):
         return None
     fields = {}
