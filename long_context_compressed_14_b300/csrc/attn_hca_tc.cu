@@ -25,8 +25,10 @@
 // S/P is double-buffered in TMEM, so the MMA computes the next tile's scores and the previous
 // tile's P V while the softmax works on this one; a slot is rewritten by S(n + 2) only after
 // P V(n) has read it, which the in-order tensor pipe guarantees (P V(n) is issued first). Key
-// tiles flow through four buffers; query rows are double-buffered and fetched one item ahead. Mixed-precision entries are widened
-// to BF16 once per call (caller workspace) before this kernel runs. Every wait is bounded.
+// tiles flow through four buffers; query rows are double-buffered and fetched one item ahead.
+// Mixed-precision entries are widened to BF16 once per call (caller workspace) before this
+// kernel runs. Every wait is bounded, and every TMEM access and every wait whose result guards
+// one sits in a warp-uniform branch (tcgen05.ld / st are .sync.aligned).
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tma_host.cuh"

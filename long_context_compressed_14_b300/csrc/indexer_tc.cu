@@ -16,10 +16,12 @@
 // each token and stores the token's score -- the 128 threads of a warpgroup write 128
 // consecutive entries of one score row at a time.
 //
-// CTA (persistent): warps 0-15 epilogue (four warpgroups, one per quarter of the tokens of a
-// query tile), warp 16 lane 0 loads tiles by TMA and issues the MMAs. Query tiles are dealt round-robin; each walks
-// only the entry tiles its last token can see (causal skipping). D is double-buffered in TMEM
-// (2 x 256 columns), entry tiles flow through a 4-deep ring, query tiles through 2 buffers.
+// CTA (persistent, one per SM): warps 0-15 epilogue (four warpgroups, one per quarter of the
+// tokens of a query tile), warp 16 lane 0 loads tiles by TMA and issues the MMAs. Query tiles
+// are dealt round-robin; each walks only the entry tiles its last token can see (causal
+// skipping). D is double-buffered in TMEM (2 x 256 columns), entry tiles flow through a 4-deep
+// ring, query tiles through 2 buffers. The load cursor runs ahead of the MMA cursor and only
+// blocks on a buffer when no MMA is pending; its other checks are non-blocking.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tma_host.cuh"
