@@ -229,6 +229,21 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(x: float, device: str) -> float:
+    """The maximum of x over all ranks of the process group (x itself without one)."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_step: float) -> float:
+    """Whole-job units per second: the units of every rank over the slowest rank's step time."""
+    return units_per_rank * world / (ms_step / 1e3)
+
+
 def run_mine(args, rank, world, local_rank):
     import long_context_compressed_14_b300 as lib
     wl = synth.WORKLOADS[args.workload]
@@ -278,13 +293,8 @@ def run_mine(args, rank, world, local_rank):
             t = ev[k][i].elapsed_time(ev[k][i + 1])
             stage_ms[name] += t
             total_ms += t
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    units = units_per_step(wl) * world
-    value = units / (ms_step / 1e3)
+    ms_step = max_over_ranks(total_ms / args.steps, "cuda")
+    value = job_throughput(units_per_step(wl), world, ms_step)
 
     # e2e: host buffers through the public API, copies inside the timed region
     e2e = None
@@ -310,12 +320,9 @@ def run_mine(args, rank, world, local_rank):
                 h.copy_(o, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = e0.elapsed_time(e1) / nsteps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": units / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / nsteps, "cuda")
+        e2e = {"value": job_throughput(units_per_step(wl), world, ms_e2e), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
 
     if rank != 0:
