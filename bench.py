@@ -286,6 +286,10 @@ def run_mine(args, rank, world, local_rank):
     torch.cuda.synchronize()
     launches = lib.csa_launch_count() - launches0
     clk = clocks.stop() if clocks else None
+    # a bounded wait that gave up makes every later kernel return early: a step timed over
+    # aborted kernels would be fast and wrong, so the run fails instead of printing it
+    status_timed = lib.csa_device_status(reset=False)
+    assert status_timed == 0, f"device status {status_timed} after the timed steps"
     stage_ms = {name: 0.0 for name, _ in stages}
     total_ms = 0.0
     for k in range(args.steps):
@@ -320,6 +324,8 @@ def run_mine(args, rank, world, local_rank):
                 h.copy_(o, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
+        status_e2e = lib.csa_device_status(reset=False)
+        assert status_e2e == 0, f"device status {status_e2e} after the end-to-end steps"
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / nsteps, "cuda")
         e2e = {"value": job_throughput(units_per_step(wl), world, ms_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d,
@@ -382,6 +388,7 @@ def run_mine(args, rank, world, local_rank):
         "roofline": roof,
         "stages": stage_report,
         "gpu_launches": launches,
+        "device_status": status_timed,
         "clocks": clk,
         "e2e": e2e,
     }

@@ -233,7 +233,11 @@ int csa_decode_static_scratch(const csa_params *p, const void *q, const int32_t 
                               const float *sink, const float *rope_tab, int32_t *topk_out,
                               void *out, float *lse_out, csa_stream_t stream);
 
-/* HCA decode step: every visible cached entry plus the window, arguments as csa_decode. */
+/* HCA decode step ([P2] 提案手法 §1 HCA: m' = 128, dense attention over every compressed entry,
+ * plus the sliding window and sink; 訓練インフラの革新 §5: state cache of recent raw tokens +
+ * compressed KV cache). Key set of the new token at p = ctx_len[b] - 1: every cached entry j with
+ * (j+1)m - 1 <= p, in order, then the window rows of the ring. Arguments as csa_decode (no
+ * indexer operands, no workspace: ws may be NULL). */
 int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
                const void *swa_ring, const float *sink, const float *rope_tab, void *out,
                float *lse_out, void *ws, size_t ws_bytes, csa_stream_t stream);
@@ -241,9 +245,21 @@ int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
 /* Number of kernels this library has launched in the process so far (host counter). */
 uint64_t csa_launch_count(void);
 
-/* Synchronises the device, returns the device status word (CSA_OK or the first device-side
- * code recorded since the last reset) in *status, and clears it when reset != 0. */
-int csa_device_status(int *status, int reset);
+/* Waits for the work queued on `stream`, then returns the device status word in *status:
+ * CSA_OK or the first device-side code recorded since the last reset (CSA_ERR_TIMEOUT: a bounded
+ * wait gave up and the kernel returned early, so its outputs are incomplete; CSA_ERR_BOUNDS: an
+ * out-of-range index or decode position was skipped). The word is shared by every stream of the
+ * device; it is cleared, together with the abort flag that makes every later bounded wait give
+ * up at once, when reset != 0 (a stream-ordered reset on `stream`). A timeout therefore stays
+ * visible, and keeps later kernels from waiting, until the caller resets it. */
+int csa_device_status(int *status, int reset, csa_stream_t stream);
+
+/* Diagnostic, no counterpart on the pages: launches one CTA that waits on an mbarrier that
+ * never receives its arrival, through the same bounded wait the library's kernels use, with a
+ * limit of limit_ns nanoseconds (1 .. 1e9). The wait gives up, records CSA_ERR_TIMEOUT in the
+ * device status word and raises the abort flag, which csa_device_status(reset = 1) clears.
+ * It exists so that the error path of a stalled pipeline can be exercised without a fault. */
+int csa_selftest_wait_timeout(uint64_t limit_ns, csa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -80,7 +80,8 @@ def _load():
             "csa_sparse_attention": (I, [PP, P, P, PE, P, P, P, P, P, P, ctypes.c_size_t, P]),
             "csa_decode_static_scratch": (I, [PP, P, P, PE, PI, PI, P, P, P, P, P, P, P, P]),
             "csa_launch_count": (ctypes.c_uint64, []),
-            "csa_device_status": (I, [ctypes.POINTER(ctypes.c_int), I]),
+            "csa_device_status": (I, [ctypes.POINTER(ctypes.c_int), I, P]),
+            "csa_selftest_wait_timeout": (I, [ctypes.c_uint64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -235,10 +236,15 @@ def hca_decode(p: Params, q, ctx_len, C, swa_ring, sink, rope_tab, out, lse_out,
         "hca_decode")
 
 
-def csa_device_status(reset: bool = True) -> int:
+def csa_device_status(reset: bool = True, stream=None) -> int:
+    """Device status word after the work queued on `stream` (0 = ok); cleared when reset."""
     v = ctypes.c_int(0)
-    _ok(_load().csa_device_status(ctypes.byref(v), int(reset)), "csa_device_status")
+    _ok(_load().csa_device_status(ctypes.byref(v), int(reset), _stream(stream)), "csa_device_status")
     return v.value
+
+
+def csa_selftest_wait_timeout(limit_ns: int, stream=None):
+    _ok(_load().csa_selftest_wait_timeout(int(limit_ns), _stream(stream)), "csa_selftest_wait_timeout")
 
 
 # ---------------------------------------------------------------------------------------

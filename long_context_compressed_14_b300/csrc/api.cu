@@ -81,14 +81,20 @@ size_t widen_bytes(const csa_params *p) {
     return p->kv_t == CSA_MIXED ? align_up((size_t)p->B * (size_t)ncap_of(p) * kD * 2) : 0;
 }
 
+// Workspace of the prefill indexer + top-k: the FP8 path keeps per-row candidate lists (the
+// fused selection), the exact FP32 path a chunk of full score rows.
+size_t index_ws_bytes(const csa_params *p) {
+    if (p->idx_t == CSA_FP8E4M3) return align_up(isel_workspace_bytes(p->L, (int)ncap_of(p)));
+    return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
+}
+
 size_t ws_bytes(const csa_params *p, int op) {
     switch (op) {
     case CSA_OP_INDEX_TOPK:
-        return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
+        return index_ws_bytes(p);
     case CSA_OP_CSA_PREFILL:
         if (p->topk == 0) return 0;
-        return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p)) +
-               align_up(sizeof(int32_t) * (size_t)p->B * p->L * p->topk) + widen_bytes(p);
+        return index_ws_bytes(p) + align_up(sizeof(int32_t) * (size_t)p->B * p->L * p->topk) + widen_bytes(p);
     case CSA_OP_SPARSE_ATTENTION:
         return p->topk > 0 ? widen_bytes(p) : 0;
     case CSA_OP_HCA_PREFILL:
@@ -121,11 +127,20 @@ bool index_rows_ok(const csa_params *p, const csa_index_rows *r) {
     return true;
 }
 
-// indexer + top-k over all prefill rows, chunked through the score workspace
+// indexer + top-k over all prefill rows: FP8 through the fused selection, FP32 (exact, the
+// bit-exact workload) chunked through a workspace of full score rows
 int run_index_topk(const csa_params *p, const csa_index_rows *qI, const csa_index_rows *KI,
                    const float *w, int32_t *idx_out, float *S, cudaStream_t st) {
-    const int64_t chunk = score_chunk_rows(p);
     const int ncap = (int)ncap_of(p);
+    if (p->idx_t == CSA_FP8E4M3) {
+        IselArgs ia{};
+        ia.qI = qI->data; ia.qI_scale = qI->scale; ia.KI = KI->data; ia.KI_scale = KI->scale; ia.w = w;
+        ia.out = idx_out; ia.ws = S;
+        ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap; ia.k = p->topk;
+        const int s = launch_index_select(ia, st);
+        return s ? s : launch_status();
+    }
+    const int64_t chunk = score_chunk_rows(p);
     for (int b = 0; b < p->B; ++b) {
         for (int64_t t0 = 0; t0 < p->L; t0 += chunk) {
             const int nrows = (int)((p->L - t0) < chunk ? (p->L - t0) : chunk);
@@ -174,6 +189,27 @@ AttnArgs attn_args(const csa_params *p, const void *q, const void *kvr, const cs
     a.d_rope = p->d_rope; a.ncap = (int)ncap_of(p); a.scale = p->scale;
     a.decode = decode; a.act_t = p->act_t; a.kv_t = p->kv_t;
     return a;
+}
+
+// Attention kernel choice (no silent second backend): FP32 activations run the CUDA-core
+// kernel (the exact FP32 workload); BF16 activations run the tensor-core kernels, and a BF16
+// layer those do not take is refused with CSA_ERR_UNSUPPORTED before anything is launched.
+int run_csa_attention(const AttnArgs &a, cudaStream_t st) {
+    if (a.act_t == CSA_F32) {
+        launch_attn_simple(a, st);
+        return launch_status();
+    }
+    if (!launch_csa_tc(a, st)) return CSA_ERR_UNSUPPORTED;
+    return launch_status();
+}
+
+int run_hca_attention(const AttnArgs &a, cudaStream_t st) {
+    if (a.act_t == CSA_F32) {
+        launch_attn_simple(a, st);
+        return launch_status();
+    }
+    if (!(a.decode ? launch_csa_tc(a, st) : launch_hca_tc(a, st))) return CSA_ERR_UNSUPPORTED;
+    return launch_status();
 }
 
 }  // namespace
@@ -270,7 +306,7 @@ int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
     void *wide = nullptr;
     if (p->topk > 0) {
         float *S = reinterpret_cast<float *>(ws);
-        const size_t sbytes = align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
+        const size_t sbytes = index_ws_bytes(p);
         const size_t ibytes = align_up(sizeof(int32_t) * (size_t)p->B * p->L * p->topk);
         idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
         wide = reinterpret_cast<char *>(ws) + sbytes + ibytes;
@@ -279,9 +315,11 @@ int csa_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
     }
     AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, idx, nullptr, sink, rope_tab, out,
                            lse_out, 0, p->topk, wide, widen_bytes(p));
-    if (p->topk == 0) a.ncap = 0;
-    if (!launch_csa_tc(a, st)) launch_attn_simple(a, st);
-    return launch_status();
+    if (p->topk == 0) {
+        a.ncap = 0;
+        a.dense = 1;  // no compressed branch: the key list is the window alone
+    }
+    return run_csa_attention(a, st);
 }
 
 int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope,
@@ -297,9 +335,11 @@ int csa_sparse_attention(const csa_params *p, const void *q, const void *kv_rope
     if (need > 0 && (wsb < need || !ws || !aligned16(ws))) return CSA_ERR_WORKSPACE;
     AttnArgs a = attn_args(p, q, kv_rope, p->topk > 0 ? C : nullptr, p->topk > 0 ? topk_idx : nullptr, nullptr, sink,
                            rope_tab, out, lse_out, 0, p->topk, ws, wsb);
-    if (p->topk == 0) a.ncap = 0;
-    if (!launch_csa_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
-    return launch_status();
+    if (p->topk == 0) {
+        a.ncap = 0;
+        a.dense = 1;
+    }
+    return run_csa_attention(a, cs(stream));
 }
 
 int hca_prefill(const csa_params *p, const void *q, const void *kv_rope, const csa_entries *C,
@@ -314,8 +354,7 @@ int hca_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
     const size_t need = ws_bytes(p, CSA_OP_HCA_PREFILL);
     if (need > 0 && (wsb < need || !ws || !aligned16(ws))) return CSA_ERR_WORKSPACE;
     AttnArgs a = attn_args(p, q, kv_rope, C, nullptr, nullptr, sink, rope_tab, out, lse_out, 0, 0, ws, wsb);
-    if (!launch_hca_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
-    return launch_status();
+    return run_hca_attention(a, cs(stream));
 }
 
 int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
@@ -351,9 +390,11 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     }
     AttnArgs a = attn_args(p, q, swa_ring, p->topk > 0 ? C : nullptr, idx, ctx_len, sink, rope_tab, out,
                            lse_out, 1, p->topk);
-    if (p->topk == 0) a.ncap = 0;
-    if (!launch_csa_tc(a, st)) launch_attn_simple(a, st);
-    return launch_status();
+    if (p->topk == 0) {
+        a.ncap = 0;
+        a.dense = 1;
+    }
+    return run_csa_attention(a, st);
 }
 
 int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
@@ -369,24 +410,31 @@ int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
     AttnArgs a = attn_args(p, q, swa_ring, C, nullptr, ctx_len, sink, rope_tab, out, lse_out, 1, 0);
     a.dense = 1;  // every visible entry, in order
-    if (!launch_csa_tc(a, cs(stream))) launch_attn_simple(a, cs(stream));
-    return launch_status();
+    return run_hca_attention(a, cs(stream));
 }
 
 uint64_t csa_launch_count(void) { return launch_counter(); }
 
-int csa_device_status(int *status, int reset) {
+int csa_device_status(int *status, int reset, csa_stream_t stream) {
     if (!status) return CSA_ERR_INVALID;
-    if (cudaDeviceSynchronize() != cudaSuccess) return CSA_ERR_CUDA;
+    cudaStream_t st = cs(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return CSA_ERR_CUDA;
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return CSA_ERR_CUDA;
     *status = v;
     if (reset) {
-        const int zero = 0;
-        if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
-        if (cudaMemcpyToSymbol(g_abort, &zero, sizeof(int)) != cudaSuccess) return CSA_ERR_CUDA;
+        launch_status_reset(st);
+        if (cudaStreamSynchronize(st) != cudaSuccess) return CSA_ERR_CUDA;
     }
     return CSA_OK;
+}
+
+int csa_selftest_wait_timeout(uint64_t limit_ns, csa_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return CSA_ERR_INVALID;
+    launch_wait_selftest(limit_ns, cs(stream));
+    return launch_status();
 }
 
 }  // extern "C"

@@ -759,7 +759,7 @@ bool csa_tc_supported(const AttnArgs &a) {
     if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED) return false;
     if (a.H != csa_tc::kH || a.n_win != 128) return false;
     if (!a.dense && (a.topk < 4 || a.topk > kMaxTopk || a.topk % 4 != 0)) return false;
-    if (a.dense && !a.decode) return false;
+    if (a.dense && !a.decode && a.ncap != 0) return false;  // prefill: dense only as window-only (no entries)
     if (a.d_rope != 0 && a.d_rope != 64) return false;
     if (csa_widen_bytes(a) > a.ws_bytes || (csa_widen_bytes(a) > 0 && !a.ws)) return false;
     // outputs are stored with a bulk copy, top-k rows fetched with one: 16-byte aligned
@@ -783,7 +783,7 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.c_rope = reinterpret_cast<const __nv_bfloat16 *>(a.c_rope);
     P.c_scale = a.c_scale;
     P.mixed = a.kv_t == CSA_MIXED;
-    if (P.mixed && !a.decode) {
+    if (P.mixed && !a.decode && a.ncap > 0) {
         // widen every entry once; the attention then gathers BF16 rows
         P.c_data = launch_widen_mixed(a, st);
         P.c_rope = nullptr;

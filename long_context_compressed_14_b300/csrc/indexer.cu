@@ -13,7 +13,8 @@
 // FP8 operands: s = sk_j * sum_h (w_h * sq_h) * ReLU(sum_c qcode_c * kcode_c) -- the row
 //   scales factor out of the ReLU because they are positive.
 // This file holds the CUDA-core kernels: the exact FP32 path and the decode scan (one query
-// per sequence, HBM-bound). The FP8 prefill indexer on tensor cores is in indexer_tc.cu.
+// per sequence, HBM-bound). The FP8 prefill indexer, with the selection fused in, runs on the
+// tensor cores (index_select.cu).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -163,7 +164,6 @@ void launch_indexer(const IndexArgs &a, cudaStream_t st) {
     }
     const int last_vis = visible_entries((int64_t)a.t0 + a.nrows - 1, a.m, a.ncap);
     if (last_vis <= 0) return;
-    if (a.idx_t == CSA_FP8E4M3 && launch_indexer_tc(a, st)) return;  // tensor-core FP8 path
     dim3 grid((unsigned)ceil_div64(last_vis, kIdxTJ), (unsigned)ceil_div64(a.nrows, kIdxTQ));
     const size_t smem = sizeof(float) * ((size_t)kIdxTQ * a.H_I * kDI + kIdxTQ * a.H_I +
                                          kIdxTJ * (kDI + 1) + kIdxTJ);

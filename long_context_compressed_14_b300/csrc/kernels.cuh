@@ -66,10 +66,30 @@ struct AttnArgs {
     int dense;             // 1: the key list is every visible entry in order (HCA decode), no idx
 };
 
+// FP8 prefill indexer with the top-k selection fused in (index_select.cu).
+constexpr int kIselCap = 4096;         // candidates kept per query row
+constexpr int kIselSampleStride = 16;  // the threshold sample holds every 16th entry tile
+struct IselArgs {
+    const void *qI;        // FP8 codes [B, L, H_I, d_I]
+    const float *qI_scale; // [B, L, H_I]
+    const void *KI;        // FP8 codes [B, ncap, d_I]
+    const float *KI_scale; // [B, ncap]
+    const float *w;        // [B, L, H_I]
+    int32_t *out;          // [B, L, k]
+    void *ws;              // isel_workspace_bytes(L, ncap) bytes, 256-byte aligned
+    int B, L, H_I, m, ncap, k;
+};
+size_t isel_workspace_bytes(int L, int ncap);
+int64_t isel_chunk_rows(int L, int ncap);
+bool isel_supported(const IselArgs &a);
+int launch_index_select(const IselArgs &a, cudaStream_t st);  // returns a csa_status
+
 // host-side count of kernel launches (every launch_* adds the kernels it launched)
 void count_launches(int n);
 uint64_t launch_counter();
 
+void launch_status_reset(cudaStream_t st);
+void launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 void launch_rope_table(float *tab, int rope_len, int d_rope, float theta, cudaStream_t st);
 void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
                        cudaStream_t st);
@@ -81,7 +101,6 @@ void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
 // what they handle
 bool launch_hca_tc(const AttnArgs &a, cudaStream_t st);
 bool launch_csa_tc(const AttnArgs &a, cudaStream_t st);
-bool launch_indexer_tc(const IndexArgs &a, cudaStream_t st);
 // Mixed-precision entries (prefill) widened to BF16 rows [B, ncap, 128] in a.ws (csa_widen_bytes
 // bytes); returns the widened array.
 size_t csa_widen_bytes(const AttnArgs &a);

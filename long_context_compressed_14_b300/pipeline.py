@@ -14,7 +14,7 @@ from typing import Optional
 
 import torch
 
-from . import (FP8E4M3, OP_CSA_DECODE, OP_CSA_PREFILL, OP_HCA_DECODE, OP_HCA_PREFILL, Params,
+from . import (FP8E4M3, MIXED, OP_CSA_DECODE, OP_CSA_PREFILL, OP_HCA_DECODE, OP_HCA_PREFILL, Params,
                alloc_entries, alloc_index_rows, alloc_workspace, csa_decode, csa_prefill,
                csa_quant_fp8_rows, hca_decode, hca_prefill, kv_compress, make_params, rope_table,
                torch_dtype)
@@ -107,7 +107,17 @@ class DecodeLayer:
 
     def load_caches(self, inp: dict, stream=None):
         """Cache set-up (not part of a decode step): the FP8 indexer-key cache is quantised
-        from the float keys; the entry cache and ring are used as given."""
+        from the float keys; a mixed-precision entry cache is stored from the given rows (the
+        first d - d_rope dims as FP8 codes with one scale per entry, the RoPE dims as they are);
+        other entry caches and the ring are used as given."""
+        self.C = None
+        if self.p.kv_t == MIXED:
+            C = inp["C"]
+            nope = self.p.d - self.p.d_rope
+            codes = torch.empty(C.shape[:-1] + (nope,), dtype=torch.uint8, device=C.device)
+            scales = torch.empty(C.shape[:-1], dtype=torch.float32, device=C.device)
+            csa_quant_fp8_rows(C[..., :nope].float().contiguous(), codes, scales, stream)
+            self.C = (codes, C[..., nope:].to(torch.bfloat16).contiguous(), scales)
         if self.csa:
             if self.p.idx_t == FP8E4M3:
                 csa_quant_fp8_rows(inp["KI"], self.KI[0], self.KI[1], stream)
@@ -117,7 +127,10 @@ class DecodeLayer:
     def run(self, inp: dict, stream=None, want_lse: bool = False, want_topk: bool = True) -> torch.Tensor:
         p = self.p
         lse = self.lse if want_lse else None
-        C = inp["C"] if isinstance(inp["C"], (tuple, list)) else (inp["C"], None, None)
+        if getattr(self, "C", None) is not None:
+            C = self.C
+        else:
+            C = inp["C"] if isinstance(inp["C"], (tuple, list)) else (inp["C"], None, None)
         if self.csa:
             if p.idx_t == FP8E4M3:
                 csa_quant_fp8_rows(inp["qI"], self.qI[0], self.qI[1], stream)

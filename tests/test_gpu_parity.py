@@ -1,10 +1,18 @@
 """GPU vs oracle parity through the C ABI (needs a B300).
 
-Tolerances (fixed here, derived in the design doc):
+Tolerances (fixed here):
   * FP32 workloads: top-k indices bit-exact on identical indexer inputs; outputs max-abs <= 1e-4.
-  * BF16 / FP8 / mixed workloads: outputs relative-L2 <= 2e-2; top-k by score (every selected
-    entry within 1e-3 * max|score| of the oracle's k-th score) with >= 95% of rows identical.
+  * BF16 / FP8 / mixed workloads: outputs relative-L2 <= 2e-2, checked twice on every compared
+    row -- against the oracle's attention run on the GPU's own top-k selection (which isolates
+    the attention kernel) and end to end against the oracle's own selection; top-k by score
+    (every selected entry within 1e-3 * max|score| of the oracle's k-th score, mean set overlap
+    >= 99%, >= 95% of rows identical: near-ties may legitimately resolve either way when the
+    GPU and the oracle sum the same products in different orders).
   * FP8 codes and row scales from the same float inputs: bit-exact.
+  * 2e-2 comes from the arithmetic: BF16 operands and BF16 weights P carry 2^-9 relative
+    rounding each, FP8 entry halves up to 2^-4 per element; averaged over 128-dim dot products
+    and the softmax the expected relative L2 error is ~5e-3, so 2e-2 leaves a 4x margin while a
+    structural error (a missing key set, a wrong rotation) moves the output by O(1).
 """
 import math
 
@@ -14,7 +22,8 @@ import torch
 
 import oracle
 import synth
-from _helpers import check_topk_by_score, np32, np64, oracle_prefill, rel_l2
+from _helpers import (attention_on_gpu_selection, check_csa_rows, check_topk_by_score, np32, np64,
+                      oracle_prefill, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -241,6 +250,82 @@ def test_index_topk_fp8(lib):
     assert frac >= 0.95, frac
 
 
+def _fp8_index_case(lib, L, m, H_I, k, qI, KI, w):
+    """Runs the FP8 indexer + top-k on float operands (quantised by the library) and returns
+    (GPU selection [L, k], dequantised oracle keys)."""
+    N = math.ceil(L / m)
+    p = lib.make_params(B=1, L=L, H=64, m=m, topk=k, H_I=H_I, act="bf16", kv="bf16", idx="fp8")
+    qd = lib.alloc_index_rows(p, (1, L, H_I))
+    kd = lib.alloc_index_rows(p, (1, N))
+    lib.csa_quant_fp8_rows(qI.to(DEV), qd[0], qd[1])
+    lib.csa_quant_fp8_rows(KI.to(DEV), kd[0], kd[1])
+    out = torch.full((1, L, k), -7, dtype=torch.int32, device=DEV)
+    lib.csa_index_topk(p, qd, kd, w.to(DEV), out, lib.alloc_workspace(p, lib.OP_INDEX_TOPK))
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
+    ok_, osk = oracle.quant_rows_fp8(KI[0].numpy())
+    return out.cpu().numpy()[0], oracle.dequant_fp8(ok_, osk)
+
+
+def test_index_topk_fp8_sampled_threshold(lib):
+    # Rows past 4 x 4096 see more than 4096 entries: their threshold comes from the sample of
+    # every 16th entry tile and only candidates above it are kept. Rows on both sides of that
+    # boundary, random rows and the last rows, by score against the oracle.
+    L, m, H_I, k = 40000, 4, 8, 512
+    g = torch.Generator().manual_seed(41)
+    N = L // m
+    qI = torch.randn((1, L, H_I, 64), generator=g)
+    KI = torch.randn((1, N, 64), generator=g)
+    w = torch.randn((1, L, H_I), generator=g)
+    got, kd = _fp8_index_case(lib, L, m, H_I, k, qI, KI, w)
+    rows = np.unique(np.concatenate([np.arange(16376, 16392), np.arange(L - 24, L),
+                                     np.random.default_rng(5).integers(0, L, 40), np.arange(0, 40)]))
+    s, _ = oracle.indexer_topk(qI[0].numpy()[rows], kd, w[0].numpy()[rows], m, k, rows, "fp8")
+    frac = check_topk_by_score(got[rows], s, rows, m, k)
+    assert frac >= 0.95, frac
+
+
+def test_index_topk_fp8_sample_misjudged(lib):
+    # The sampled entry tiles (entries [2048 s, 2048 s + 128)) score high and every other entry
+    # near zero, so the threshold taken from the sample lets fewer than k candidates through;
+    # those rows must be redone by the exact full-row path.
+    L, m, H_I, k = 9000, 1, 4, 1024
+    g = torch.Generator().manual_seed(29)
+    u = torch.randn((64,), generator=g)
+    qI = torch.zeros((1, L, H_I, 64))
+    qI[0, :, 0, :] = u
+    KI = 0.01 * torch.randn((1, L, 64), generator=g)
+    hot = (torch.arange(L) % 2048) < 128
+    KI[0, hot] += 4.0 * u + 0.1 * torch.randn((int(hot.sum()), 64), generator=g)
+    w = torch.zeros((1, L, H_I))
+    w[0, :, 0] = 1.0
+    got, kd = _fp8_index_case(lib, L, m, H_I, k, qI, KI, w)
+    rows = np.concatenate([np.arange(L - 20, L), np.arange(4090, 4110), np.arange(6000, 6010)])
+    s, _ = oracle.indexer_topk(qI[0].numpy()[rows], kd, w[0].numpy()[rows], m, k, rows, "fp8")
+    frac = check_topk_by_score(got[rows], s, rows, m, k)
+    assert frac >= 0.95, frac
+
+
+def test_index_topk_fp8_heavy_ties(lib):
+    # Odd rows weigh every head 0, so all their scores are exactly 0: every entry is a
+    # candidate (more than the list holds once a row sees more than 4096 entries) and the
+    # lowest indices must win. Exact on those rows; the other rows by score.
+    L, m, H_I, k = 12000, 1, 4, 300
+    g = torch.Generator().manual_seed(31)
+    qI = torch.randn((1, L, H_I, 64), generator=g)
+    KI = torch.randn((1, L, 64), generator=g)
+    w = torch.randn((1, L, H_I), generator=g)
+    w[0, 1::2] = 0.0
+    got, kd = _fp8_index_case(lib, L, m, H_I, k, qI, KI, w)
+    rows = np.concatenate([np.arange(L - 30, L), np.arange(5000, 5030), np.arange(290, 310)])
+    odd = rows % 2 == 1
+    assert np.all(got[rows[odd & (rows + 1 > k)]] == np.arange(k)[None, :])
+    ev = rows[~odd]
+    s, _ = oracle.indexer_topk(qI[0].numpy()[ev], kd, w[0].numpy()[ev], m, k, ev, "fp8")
+    frac = check_topk_by_score(got[ev], s, ev, m, k)
+    assert frac >= 0.95, frac
+
+
 # ---------------------------------------------------------------------------------------
 # Prefill layers
 # ---------------------------------------------------------------------------------------
@@ -287,18 +372,19 @@ def test_csa_prefill_f32_pipeline(lib):
     gidx = layer.topk.cpu().numpy()[0]
     frac = check_topk_by_score(gidx, res["scores"], rows, wl.m, wl.topk, rel_eps=1e-5)
     assert frac >= 0.99, frac
-    same = np.array([np.array_equal(gidx[r], res["idx"][r]) for r in rows])
-    err = np.abs(np64(out[0])[same] - res["o"][same]).max()
+    # every row against the oracle's attention on the GPU's own selection
+    o_own = attention_on_gpu_selection(wl, res, np64(inp["q"][0]), gidx, rows, np64(inp["sink"]))
+    err = np.abs(np64(out[0]) - o_own).max()
     assert err <= 1e-4, err
 
 
 @pytest.mark.parametrize("B,L,H,c_t,sink", [
-    (1, 2000, 16, "bf16", True), (1, 127, 16, "bf16", True), (1, 129, 4, "bf16", True),
+    (1, 2000, 16, "bf16", True), (1, 127, 16, "bf16", True), (1, 129, 32, "bf16", True),
     (2, 1001, 64, "bf16", True), (1, 1001, 64, "mixed", True), (2, 300, 32, "mixed", False),
     (1, 70, 64, "bf16", False), (1, 515, 128 // 2, "mixed", True),
 ])
 def test_hca_prefill_bf16(lib, B, L, H, c_t, sink):
-    # H in {16, 32, 64} runs the tensor-core kernel; H = 4 the CUDA-core kernel
+    # BF16 HCA prefill runs the tensor-core kernel (H in {16, 32, 64})
     wl = synth.WORKLOADS["hca_bf16_L16384"].replace(B=B, L=L, H=H, c_t=c_t)
     from long_context_compressed_14_b300.pipeline import PrefillLayer
     inp = synth.prefill_layer(wl, csa=False)
@@ -340,8 +426,25 @@ def test_csa_prefill_bf16_fp8(lib, B, L, k, c_t):
         gidx = layer.topk.cpu().numpy()[b][rows]
         frac = check_topk_by_score(gidx, res["scores"], rows, wl.m, k)
         assert frac >= 0.95, frac
-        same = np.array([np.array_equal(gidx[r], res["idx"][r]) for r in range(len(rows))])
-        assert rel_l2(np64(out[b][rows])[same], res["o"][same]) <= 2e-2
+        check_csa_rows(wl, inp, b, rows, np64(out[b][rows]), gidx, res)
+
+
+def test_bf16_head_counts_without_a_tensor_core_kernel_are_refused(lib):
+    # BF16 layers run on the tensor-core kernels only; a head count they do not take is refused
+    # before anything is launched (no silent CUDA-core fallback)
+    from long_context_compressed_14_b300.pipeline import PrefillLayer
+    wl = synth.WORKLOADS["hca_bf16_L16384"].replace(L=300, H=4)
+    inp = synth.prefill_layer(wl, csa=False)
+    with pytest.raises(lib.CsaError) as e:
+        PrefillLayer.create(wl, csa=False).run(_dev(inp))
+    assert e.value.status == lib.ERR_UNSUPPORTED
+    wl2 = synth.WORKLOADS["csa_bf16_4x32768"].replace(B=1, L=300, H=32, topk=64)
+    inp2 = synth.prefill_layer(wl2, csa=True)
+    with pytest.raises(lib.CsaError) as e:
+        PrefillLayer.create(wl2, csa=True).run(_dev(inp2))
+    assert e.value.status == lib.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
 
 
 def test_csa_topk_zero_and_tiny(lib):
@@ -364,22 +467,40 @@ def test_csa_topk_zero_and_tiny(lib):
 # Decode
 # ---------------------------------------------------------------------------------------
 
-def _oracle_decode(wl, inp, b, csa):
+def _oracle_decode(wl, inp, b, csa, gpu_idx=None):
+    """Oracle decode of sequence b; with gpu_idx, the attention runs on that selection."""
     m = wl.m if csa else wl.m_hca
     kw = dict(d_rope=wl.d_rope, theta=wl.theta, n_win=wl.n_win, scale=wl.scale)
     ctx = int(inp["ctx"][b])
-    C = np64(inp["C"][b])
+    C, _ = oracle.store_rows(np64(inp["C"][b]), wl.c_t if wl.c_t == "mixed" else "f64", wl.d_rope)
     if csa:
         kc, ks = oracle.quant_rows_fp8(np32(inp["KI"][b]))
-        return oracle.csa_decode(np64(inp["q"][b]), ctx, C, np32(inp["qI"][b]), oracle.dequant_fp8(kc, ks),
-                                 np32(inp["w"][b]), np64(inp["ring"][b]), np64(inp["sink"]), m=m, k=wl.topk,
-                                 idx_store=wl.idx_t, **kw)
+        res = oracle.csa_decode(np64(inp["q"][b]), ctx, C, np32(inp["qI"][b]), oracle.dequant_fp8(kc, ks),
+                                np32(inp["w"][b]), np64(inp["ring"][b]), np64(inp["sink"]), m=m, k=wl.topk,
+                                idx_store=wl.idx_t, **kw)
+        if gpu_idx is not None:
+            res["o_own"], _ = oracle.decode_one(np64(inp["q"][b]), ctx, C, np.asarray(gpu_idx, np.int32), wl.topk, m,
+                                                np64(inp["ring"][b]), sink=np64(inp["sink"]), **kw)
+        return res
     return oracle.hca_decode(np64(inp["q"][b]), ctx, C, np64(inp["ring"][b]), np64(inp["sink"]), m=m, **kw)
 
 
+def _check_decode(wl, inp, layer, out, csa, seqs):
+    for b in seqs:
+        if csa:
+            gidx = layer.topk.cpu().numpy()[b]
+            res = _oracle_decode(wl, inp, b, csa, gpu_idx=gidx)
+            check_topk_by_score(gidx[None], res["scores"][None], [int(inp["ctx"][b]) - 1], wl.m, wl.topk)
+            assert rel_l2(np64(out[b]), res["o_own"]) <= 2e-2, ("attention on the GPU selection", b)
+        else:
+            res = _oracle_decode(wl, inp, b, csa)
+        assert rel_l2(np64(out[b]), res["o"]) <= 2e-2, ("end to end", b)
+
+
 @pytest.mark.parametrize("csa", [True, False])
-def test_decode(lib, csa):
-    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=8192, topk=256)
+@pytest.mark.parametrize("c_t", ["bf16", "mixed"])
+def test_decode(lib, csa, c_t):
+    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=8192, topk=256, c_t=c_t)
     from long_context_compressed_14_b300.pipeline import DecodeLayer
     inp = synth.decode_layer(wl, csa=csa)
     inp["ctx"] = torch.tensor([8192, 1, 77, 5001], dtype=torch.int32)
@@ -387,14 +508,9 @@ def test_decode(lib, csa):
     d = _dev(inp)
     layer.load_caches(d)
     out = layer.run(d)
-    for b in range(4):
-        res = _oracle_decode(wl, inp, b, csa)
-        if csa:
-            frac = check_topk_by_score(layer.topk.cpu().numpy()[b][None], res["scores"][None],
-                                       [int(inp["ctx"][b]) - 1], wl.m, wl.topk)
-            if frac < 1.0:
-                continue  # a near-tie changed the set; the selection itself was checked above
-        assert rel_l2(np64(out[b]), res["o"]) <= 2e-2, b
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
+    _check_decode(wl, inp, layer, out, csa, range(4))
 
 
 def test_device_status_clean(lib):
@@ -412,8 +528,7 @@ def _check_prefill_rows(wl, inp, out, topk, b, rows, csa, layer_no=0):
         gidx = topk.cpu().numpy()[b][rows]
         frac = check_topk_by_score(gidx, res["scores"], rows, wl.m, wl.topk)
         assert frac >= 0.95, frac
-        same = np.array([np.array_equal(gidx[r], res["idx"][r]) for r in range(len(rows))])
-        assert rel_l2(np64(out[b][rows])[same], res["o"][same]) <= 2e-2
+        check_csa_rows(wl, inp, b, rows, np64(out[b][rows]), gidx, res)
     else:
         assert rel_l2(np64(out[b][rows]), res["o"]) <= 2e-2
 
@@ -452,8 +567,7 @@ def test_pair_mixed_L262144_full_size_sampled(lib):
         if csa:
             frac = check_topk_by_score(topk_rows.numpy(), res["scores"], rows, wl.m, wl.topk)
             assert frac >= 0.95, frac
-            same = np.array([np.array_equal(topk_rows.numpy()[r], res["idx"][r]) for r in range(len(rows))])
-            assert rel_l2(np64(out_rows)[same], res["o"][same]) <= 2e-2
+            check_csa_rows(wl, inp, 0, rows, np64(out_rows), topk_rows.numpy(), res)
         else:
             assert rel_l2(np64(out_rows), res["o"]) <= 2e-2
         del inp
@@ -472,11 +586,4 @@ def test_decode_b16_ctx131072_full_size_sampled(lib):
         out = layer.run(d)
         torch.cuda.synchronize()
         assert lib.csa_device_status() == 0
-        for b in (0, wl.B - 1):
-            res = _oracle_decode(wl, inp, b, csa)
-            if csa:
-                frac = check_topk_by_score(layer.topk.cpu().numpy()[b][None], res["scores"][None],
-                                           [int(inp["ctx"][b]) - 1], wl.m, wl.topk)
-                if frac < 1.0:
-                    continue  # a near-tie changed the set; the selection itself was checked above
-            assert rel_l2(np64(out[b]), res["o"]) <= 2e-2, b
+        _check_decode(wl, inp, layer, out, csa, (0, wl.B - 1))

@@ -90,6 +90,30 @@ def test_visibility_rule():
     assert list(oracle.entry_pos(3, 4)) == [3, 7, 11]
 
 
+@pytest.mark.parametrize("m", [4, 128])
+def test_entry_rotation_position_is_its_last_raw_row(m):
+    # An entry whose weights all sit on the last raw row u = (j+1)m-1 of its block (a +60
+    # set-a logit there, every other logit 0) is that raw row; rotated at the entry position it
+    # must equal the sliding-window copy of row u, which is rotated at u itself. So its logit
+    # against any query equals row u's window logit. Rotating entries at jm (the block start)
+    # or at (j+1)m (one past it) breaks this.
+    L, d, d_rope, theta = 5 * m + 3, 128, 64, 1.0e4
+    rng = np.random.default_rng(m)
+    kv = rng.standard_normal((L, d))
+    N = oracle.num_entries(L, m)
+    for j in range(N - 1):  # complete blocks
+        u = (j + 1) * m - 1
+        z = np.zeros((L, 2))
+        z[u, 0] = 60.0
+        comp = oracle.kv_compress(kv, z, None, m, d_rope, theta)
+        np.testing.assert_allclose(comp["C"][j], comp["kv_rope"][u], rtol=0, atol=1e-12)
+        q = rng.standard_normal((3, d))
+        np.testing.assert_allclose(q @ comp["C"][j], q @ comp["kv_rope"][u], rtol=0, atol=1e-10)
+        # a rotation at the block start would not agree (the RoPE half moves)
+        wrong = oracle.rope(kv[u:u + 1], np.array([j * m]), d_rope, theta)[0]
+        assert np.abs(wrong[d - d_rope:] - comp["C"][j][d - d_rope:]).max() > 1e-3
+
+
 # ---------------------------------------------------------------------------------------
 # RoPE
 # ---------------------------------------------------------------------------------------
