@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode record of the default line")
+    ap.add_argument("--no-probes", action="store_true", help="skip the FP8 / FFMA / L2 peak probes")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
     return ap.parse_args()
 
@@ -244,10 +246,63 @@ def job_throughput(units_per_rank: float, world: int, ms_step: float) -> float:
     return units_per_rank * world / (ms_step / 1e3)
 
 
-def run_mine(args, rank, world, local_rank):
-    import long_context_compressed_14_b300 as lib
-    wl = synth.WORKLOADS[args.workload]
-    torch.cuda.set_device(local_rank)
+def measure_probes(lib):
+    """Roofline denominators MEASURED_PEAKS.json does not hold, measured in this run on this GPU:
+    FP8 E4M3 dense tensor rate (torch._scaled_mm 8192^3, the library GEMM), FP32 FMA rate of the
+    CUDA cores and L2 read bandwidth (the library's probe kernels). Best of 5."""
+    res = {"fp8_tflops": None, "ffma_tflops": None, "l2_read_gbs": None}
+    stream = torch.cuda.current_stream()
+
+    def best(fn, reps=5):
+        t = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1) / 1e3)
+        return min(t)
+    try:
+        n = 8192
+        a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn).t()
+        one = torch.tensor(1.0, device="cuda")
+        mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)  # noqa: E731
+        for _ in range(3):
+            mm()
+        res["fp8_tflops"] = 2 * n ** 3 / best(lambda: [mm() for _ in range(5)]) * 5 / 1e12
+        del a, b
+    except Exception:
+        pass
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    blocks, iters = sms * 16, 8192
+    out = torch.empty(blocks * 256, device="cuda")
+    lib.csa_probe_ffma(blocks, 64, out)
+    res["ffma_tflops"] = blocks * 256 * iters * 32 / best(lambda: lib.csa_probe_ffma(blocks, iters, out)) / 1e12
+    buf = torch.ones(48 * 2 ** 20 // 4, device="cuda")  # 48 MiB: resident in the 126 MB L2
+    sums = torch.zeros(sms * 4, device="cuda")
+    reps = 20
+    lib.csa_probe_read(buf, 2, sms * 4, sums)
+    res["l2_read_gbs"] = buf.numel() * 4 * reps / best(lambda: lib.csa_probe_read(buf, reps, sms * 4, sums)) / 1e9
+    return res
+
+
+def stage_peak(name, kind, pk, probes):
+    """(peak, unit, note) a stage's roofline fraction is taken against."""
+    if kind == "hbm":
+        return pk["hbm"], "GB/s", f"HBM copy ({pk['src']})"
+    if name.endswith("index_topk"):
+        if probes.get("fp8_tflops"):
+            return probes["fp8_tflops"], "TFLOP/s", "FP8 dense (torch._scaled_mm 8192^3, measured in this run)"
+        return 2 * pk["bf16_sus"], "TFLOP/s", f"FP8 = 2 x BF16 sustained ({pk['src']}, nominal ratio)"
+    return pk["bf16_sus"], "TFLOP/s", f"BF16 dense sustained ({pk['src']}); the kernel is timed inside a long step"
+
+
+def time_workload(lib, wl, args, graph=False, e2e=False, world=1, rank=0, local_rank=0):
+    """Times K steps of workload wl after W warm-up steps (CUDA events on the launching stream,
+    L2 flushed between steps unless the inputs are larger than L2). graph=True captures one
+    step in a CUDA graph and times its replays (the per-stage times then come from eager steps)."""
     dev_inputs = [{k: v.cuda() if isinstance(v, torch.Tensor) else v for k, v in inp.items()}
                   for inp in make_inputs(wl)]
     steps = build_steps(lib, wl, dev_inputs)
@@ -269,10 +324,10 @@ def run_mine(args, rank, world, local_rank):
         if flush is not None:
             flush.zero_()
     torch.cuda.synchronize()
-    assert lib.csa_device_status() == 0, "device status after warm-up"
+    assert lib.csa_device_status(reset=False) == 0, "device status after warm-up"
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
-    clocks = Clocks(local_rank) if rank == 0 else None
+    clocks = Clocks(local_rank) if (rank == 0 and not graph) else None
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -288,8 +343,8 @@ def run_mine(args, rank, world, local_rank):
     clk = clocks.stop() if clocks else None
     # a bounded wait that gave up makes every later kernel return early: a step timed over
     # aborted kernels would be fast and wrong, so the run fails instead of printing it
-    status_timed = lib.csa_device_status(reset=False)
-    assert status_timed == 0, f"device status {status_timed} after the timed steps"
+    status = lib.csa_device_status(reset=False)
+    assert status == 0, f"device status {status} after the timed steps"
     stage_ms = {name: 0.0 for name, _ in stages}
     total_ms = 0.0
     for k in range(args.steps):
@@ -297,14 +352,41 @@ def run_mine(args, rank, world, local_rank):
             t = ev[k][i].elapsed_time(ev[k][i + 1])
             stage_ms[name] += t
             total_ms += t
-    ms_step = max_over_ranks(total_ms / args.steps, "cuda")
-    value = job_throughput(units_per_step(wl), world, ms_step)
-
-    # e2e: host buffers through the public API, copies inside the timed region
-    e2e = None
-    if not args.no_e2e:
-        # per-step inputs: every prefill input; for decode, the new token's q, qI and w (the
-        # caches are state that stays resident between steps)
+    rec = {"stage_ms": {n: v / args.steps for n, v in stage_ms.items()}, "ms_step": total_ms / args.steps,
+           "launches": launches, "clocks": clk, "flush": flush is not None, "status": status}
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            one_step()  # warm the capture stream
+            side.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                one_step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        clocks = Clocks(local_rank) if rank == 0 else None
+        if clocks:
+            clocks.start()
+        for k in range(args.steps):
+            gev[k][0].record(stream)
+            g.replay()
+            gev[k][1].record(stream)
+            if flush is not None:
+                flush.zero_()
+        torch.cuda.synchronize()
+        rec["clocks"] = clocks.stop() if clocks else None
+        status = lib.csa_device_status(reset=False)
+        assert status == 0, f"device status {status} after the graph replays"
+        rec["ms_step_graph"] = sum(a.elapsed_time(b) for a, b in gev) / args.steps
+    if e2e:
+        # host buffers through the public API, copies inside the timed region. Per-step inputs:
+        # every prefill input; for decode, the new token's q, qI and w (the caches are state
+        # that stays resident between steps)
         per_step = (lambda key: key in ("q", "qI", "w")) if wl.kind == "decode" else (lambda key: key != "ctx")
         host_inputs = [{k: v for k, v in inp.items() if per_step(k)} for inp in make_inputs(wl, pin=True)]
         host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for st in steps for o in st.outputs()]
@@ -324,17 +406,49 @@ def run_mine(args, rank, world, local_rank):
                 h.copy_(o, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        status_e2e = lib.csa_device_status(reset=False)
-        assert status_e2e == 0, f"device status {status_e2e} after the end-to-end steps"
-        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / nsteps, "cuda")
-        e2e = {"value": job_throughput(units_per_step(wl), world, ms_e2e), "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+        status = lib.csa_device_status(reset=False)
+        assert status == 0, f"device status {status} after the end-to-end steps"
+        rec["e2e"] = {"ms": e0.elapsed_time(e1) / nsteps, "h2d": h2d, "d2h": d2h}
+    del steps, dev_inputs
+    torch.cuda.empty_cache()
+    return rec
 
+
+def measure_decode(lib, args, pk, name="decode_b16_ctx131072"):
+    """The decode workload (one CSA and one HCA decode step of 16 sequences x 131072 cached
+    tokens), timed as a CUDA-graph-captured step with L2 flushed between steps; HBM roofline of
+    the whole step from the bytes it must move."""
+    wl = synth.WORKLOADS[name]
+    rec = time_workload(lib, wl, args, graph=True)
+    byts = decode_bytes(wl, True) + decode_bytes(wl, False)
+    ms = rec["ms_step_graph"]
+    ach = byts / (ms / 1e3) / 1e9
+    return {"workload": wl.name, "B": wl.B, "ctx": wl.L, "ms_per_step": ms, "tokens_per_s": wl.B / (ms / 1e3),
+            "ms_per_step_eager": rec["ms_step"], "stages_eager_ms": rec["stage_ms"], "cuda_graph": True,
+            "l2": "L2 flushed between steps (2x126 MiB write)" if rec["flush"] else "inputs larger than L2",
+            "gpu_launches_per_step": rec["launches"] / args.steps, "clocks": rec["clocks"],
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s", "frac": ach / pk["hbm"],
+                         "bytes_per_step": byts, "peak_note": f"HBM copy ({pk['src']}); whole step, both layers"}}
+
+
+def run_mine(args, rank, world, local_rank):
+    import long_context_compressed_14_b300 as lib
+    wl = synth.WORKLOADS[args.workload]
+    torch.cuda.set_device(local_rank)
+    rec = time_workload(lib, wl, args, graph=wl.kind == "decode", e2e=not args.no_e2e, world=world, rank=rank,
+                        local_rank=local_rank)
+    ms_step = max_over_ranks(rec["ms_step_graph"] if wl.kind == "decode" else rec["ms_step"], "cuda")
+    value = job_throughput(units_per_step(wl), world, ms_step)
+    e2e = None
+    if "e2e" in rec:
+        ms_e2e = max_over_ranks(rec["e2e"]["ms"], "cuda")
+        e2e = {"value": job_throughput(units_per_step(wl), world, ms_e2e), "unit": "tokens/s",
+               "h2d_bytes_per_step": rec["e2e"]["h2d"], "d2h_bytes_per_step": rec["e2e"]["d2h"], "ms_per_step": ms_e2e}
     if rank != 0:
         return None
     pk = peaks()
-    # algorithmic work per stage, and the roofline of the dominant single-kernel stage
+    probes = measure_probes(lib) if not args.no_probes else {}
+    # algorithmic work per stage, each stage's roofline fraction, and the dominant kernel's
     act_bytes = 4 if wl.q_t == "f32" else 2
     work = {}
     if wl.kind == "pair":
@@ -343,34 +457,32 @@ def run_mine(args, rank, world, local_rank):
                 work[tag + kname] = v
     elif wl.kind != "decode":
         work = stage_work(wl, wl.kind == "csa", act_bytes)
+    stage_ms = rec["stage_ms"]
+    total_ms = sum(stage_ms.values())
     stage_report = {}
-    for name in stage_ms:
-        per_launch_ms = stage_ms[name] / args.steps
-        rec = {"ms": per_launch_ms, "share": stage_ms[name] / total_ms}
+    for name, per_launch_ms in stage_ms.items():
+        r = {"ms": per_launch_ms, "share": per_launch_ms / total_ms}
         if name in work:
             kind, amount = work[name]
-            if kind == "hbm":
-                rec["GB/s"] = amount / (per_launch_ms / 1e3) / 1e9
-            else:
-                rec["TFLOP/s"] = amount / (per_launch_ms / 1e3) / 1e12
-        stage_report[name] = rec
+            peak, unit, _ = stage_peak(name, kind, pk, probes)
+            ach = amount / (per_launch_ms / 1e3) / (1e9 if kind == "hbm" else 1e12)
+            r[unit] = ach
+            r["frac"] = ach / peak
+        stage_report[name] = r
     roof = None
     attn_names = [n for n in stage_ms if n.endswith("attention")]
     if attn_names:
         dom = max(attn_names, key=lambda n: stage_ms[n])
         kind, amount = work[dom]
-        t = stage_ms[dom] / args.steps / 1e3
-        ach = amount / t / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_sus"], "traffic": measured_traffic(dom, wl.B * wl.L),
-                "peak_note": f"bf16 dense sustained ({pk['src']}); the kernel is timed inside a long step"}
+        peak, unit, note = stage_peak(dom, kind, pk, probes)
+        ach = amount / (stage_ms[dom] / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": unit,
+                "frac": ach / peak, "traffic": measured_traffic(dom, wl.B * wl.L), "peak_note": note}
     elif wl.kind == "decode":
-        dom = max(stage_ms, key=lambda n: stage_ms[n])
-        byts = decode_bytes(wl, csa=dom.startswith("csa"))
-        t = stage_ms[dom] / args.steps / 1e3
-        ach = byts / t / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": ach / pk["hbm"], "traffic": None, "peak_note": f"HBM copy ({pk['src']})"}
+        byts = decode_bytes(wl, True) + decode_bytes(wl, False)
+        ach = byts / (ms_step / 1e3) / 1e9
+        roof = {"kernel": "decode step (CSA + HCA layer)", "bound": "hbm", "achieved": ach, "peak": pk["hbm"],
+                "unit": "GB/s", "frac": ach / pk["hbm"], "traffic": None, "peak_note": f"HBM copy ({pk['src']})"}
     line = {
         "metric": METRIC,
         "value": value,
@@ -384,14 +496,19 @@ def run_mine(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f32" if wl.q_t == "f32" else "bf16",
         "data": "synthetic",
-        "config": workload_config(wl, flush is None),
+        "config": workload_config(wl, not rec["flush"]),
         "roofline": roof,
         "stages": stage_report,
-        "gpu_launches": launches,
-        "device_status": status_timed,
-        "clocks": clk,
+        "gpu_launches": rec["launches"],
+        "device_status": rec["status"],
+        "clocks": rec["clocks"],
         "e2e": e2e,
+        "probes": probes,
     }
+    if wl.kind == "decode":
+        line["cuda_graph"] = True
+    if wl.kind == "pair" and not args.no_decode:
+        line["decode"] = measure_decode(lib, args, pk)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     return line
@@ -473,8 +590,21 @@ def _np64(t):
     return t.detach().float().numpy().astype(np.float64)
 
 
-def _oracle_prefill_sample(wl, layer, csa, n_rows):
+def systematic_rows(L: int, n: int, seed: int):
+    """n query rows of a length-L sequence at evenly spaced positions (i + u) * L / n with one
+    seeded random offset u: every region of the sequence is represented in proportion, so the
+    mean cost of the sampled rows estimates the mean cost of all rows without bias whatever n
+    is (the CPU baseline and the reference arm use different n and agree)."""
     import numpy as np
+    n = max(1, min(n, L))
+    u = np.random.default_rng(seed).random()
+    return np.unique(np.minimum(((np.arange(n) + u) * L / n).astype(np.int64), L - 1))
+
+
+def _oracle_prefill_sample(wl, layer, csa, n_rows):
+    """Seconds per token of one prefill layer of the oracle: compression of the whole sequence
+    (timed in full) plus the mean per-row time of the indexer, top-k and attention over n_rows
+    systematically sampled query rows. Returns (seconds per token, rows, seconds spent)."""
     import oracle
     inp = synth.prefill_layer(wl.replace(B=1), layer, csa=csa)
     m = wl.m if csa else wl.m_hca
@@ -483,7 +613,7 @@ def _oracle_prefill_sample(wl, layer, csa, n_rows):
                               _np64(inp["kI_raw"][0]) if csa and wl.topk > 0 else None, m, wl.d_rope, wl.theta,
                               c_store=wl.c_t, idx_store=wl.idx_t if csa else "f64", q_store=wl.q_t)
     t_comp = time.perf_counter() - t0
-    rows = synth.sample_rows(wl.L, n_rows, seed=wl.seed, first=min(n_rows // 4, 64), last=min(n_rows // 4, 64)).numpy()
+    rows = systematic_rows(wl.L, n_rows, seed=wl.seed + 7 * layer)
     kw = dict(d_rope=wl.d_rope, theta=wl.theta, n_win=wl.n_win, scale=wl.scale)
     q = _np64(inp["q"][0][rows])
     sink = _np64(inp["sink"])
@@ -496,12 +626,10 @@ def _oracle_prefill_sample(wl, layer, csa, n_rows):
     else:
         oracle.hca_rows(q, comp["kv_rope"], comp["C"], sink, rows, m=m, **kw)
     t_rows = time.perf_counter() - t1
-    # rows are sampled with the stratification above; scale by the mean cost per row
     return t_comp / wl.L + t_rows / len(rows), len(rows), t_comp + t_rows
 
 
 def _oracle_decode_sample(wl, layer, csa, n_seq):
-    import numpy as np
     import oracle
     sub = wl.replace(B=n_seq)
     inp = synth.decode_layer(sub, layer, csa=csa)
@@ -521,48 +649,66 @@ def _oracle_decode_sample(wl, layer, csa, n_seq):
     return dt / n_seq, n_seq, dt
 
 
+def oracle_sample(wl, n_rows):
+    """One bounded sample of the workload on the oracle: (seconds per token, description,
+    seconds spent). Prefill: per layer, compression in full plus n_rows sampled query rows;
+    decode: n_rows sequences (at least 1) of one CSA and one HCA decode step."""
+    if wl.kind == "decode":
+        n = max(1, min(wl.B, n_rows))
+        spt_c, _, dc = _oracle_decode_sample(wl, 0, True, n)
+        spt_h, _, dh = _oracle_decode_sample(wl, 1, False, n)
+        return spt_c + spt_h, f"{n} of {wl.B} sequences, one CSA and one HCA decode step each", dc + dh
+    layers = [(0, True), (1, False)] if wl.kind == "pair" else [(0, wl.kind == "csa")]
+    spt, secs = 0.0, 0.0
+    for layer, csa in layers:
+        p, _, dt = _oracle_prefill_sample(wl, layer, csa, n_rows)
+        spt += p
+        secs += dt
+    desc = (f"sequence 0 of {wl.B}, per layer ({len(layers)}): compression in full, then {n_rows} query rows at "
+            f"evenly spaced positions (seeded offset); seconds per token = compression / L + mean per sampled row")
+    return spt, desc, secs
+
+
+def sample_rows_for(wl, target_s):
+    """Rows per layer of a sample that takes about target_s seconds (sized from a 4-row probe)."""
+    if wl.kind == "decode":
+        _, _, dt = oracle_sample(wl, 1)
+        return max(1, min(wl.B, int(target_s / max(dt, 1e-3))))
+    spt, _, dt = oracle_sample(wl, 4)
+    per_row = max(dt / 4.0, 1e-4)  # compression included: a conservative per-row figure
+    return int(max(4, min(wl.L, target_s / per_row)))
+
+
 def cpu_baseline(wl, target_s=15.0):
     import oracle
     threads = oracle.num_threads()
-    if wl.kind == "decode":
-        n = 2
-        spt_c, _, _ = _oracle_decode_sample(wl, 0, True, n)
-        spt_h, _, _ = _oracle_decode_sample(wl, 1, False, n)
-        spt = spt_c + spt_h
-        sample = f"{n} of {wl.B} sequences, one CSA and one HCA decode step each (the cache quantisation included)"
-    else:
-        layers = [(0, True), (1, False)] if wl.kind == "pair" else [(0, wl.kind == "csa")]
-        # a first small sample sizes the row count to the time target
-        spt, rows_used, secs = 0.0, 0, 0.0
-        for layer, csa in layers:
-            probe_spt, nr, dt = _oracle_prefill_sample(wl, layer, csa, 16)
-            per_row = max(dt / max(nr, 1), 1e-4)
-            n_rows = int(max(16, min(wl.L, (target_s / len(layers)) / per_row)))
-            if n_rows > 16:
-                probe_spt, nr, dt = _oracle_prefill_sample(wl, layer, csa, n_rows)
-            spt += probe_spt
-            rows_used += nr
-            secs += dt
-        sample = (f"sequence 0 of {wl.B}: compression in full, then {rows_used} sampled query rows over "
-                  f"{len(layers)} layer(s) (first/last/random), per-token time extrapolated linearly")
-    return {"value": 1.0 / spt, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
+    n = sample_rows_for(wl, target_s)
+    spt, desc, secs = oracle_sample(wl, n)
+    return {"value": 1.0 / spt, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc,
+            "sample_seconds": secs, "extrapolated": True}
 
 
 def run_reference(args, rank):
+    """The reference arm: the CPU oracle, as it stands, on this workload. A step is one bounded
+    sample (sized so that warm-up and timed steps end within a few minutes); ms_per_step is the
+    measured time of one such step and value the tokens/s extrapolated from it."""
     if rank != 0:
         return None
+    import oracle
     wl = synth.WORKLOADS[args.workload]
+    per_step_s = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    n = sample_rows_for(wl, per_step_s)
     for _ in range(args.warmup):
-        cpu_baseline(wl, target_s=2.0)
-    vals = []
-    t0 = time.perf_counter()
-    base = None
+        oracle_sample(wl, n)
+    spts, walls = [], []
+    desc = ""
     for _ in range(args.steps):
-        base = cpu_baseline(wl, target_s=args.cpu_seconds / max(args.steps, 1))
-        vals.append(base["value"])
-    elapsed = time.perf_counter() - t0
-    value = statistics.median(vals)
-    base["value"] = value
+        t0 = time.perf_counter()
+        spt, desc, _ = oracle_sample(wl, n)
+        walls.append(time.perf_counter() - t0)
+        spts.append(spt)
+    value = 1.0 / statistics.median(spts)
+    ms_step = 1e3 * statistics.median(walls)
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -571,16 +717,17 @@ def run_reference(args, rank):
         "n_gpus": 1,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": 1e3 * units_per_step(wl) / value,
+        "ms_per_step": ms_step,
+        "step": "one bounded oracle sample of the workload (timed); value extrapolated from it to tokens/s",
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(wl, True),
-        "cpu_baseline": base,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": desc, "extrapolated": True},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "wall_s": elapsed,
     }
 
 

@@ -215,7 +215,8 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
  * the device and take unbounded time; a caller held to a fixed device-memory budget. This
  * entry point has no counterpart in the paper; it exists only for such callers.
  * It computes exactly what csa_decode computes, with the same arguments minus the workspace:
- * the scratch it needs (indexer scores and selected indices) comes from one fixed array of
+ * the scratch it needs (indexer scores, selected indices and the split-KV partial results)
+ * comes from one fixed array of
  * CSA_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads the library holds
  * until the process exits. It allocates nothing.
  *  - A layer whose scratch (csa_workspace_bytes(p, CSA_OP_CSA_DECODE)) exceeds the array is
@@ -226,7 +227,7 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
  *  - All calls on a device share the array: calls that overlap on the GPU (unordered streams)
  *    race on it. Nothing in it needs to start at zero: each call writes the scores and indices
  *    before it reads them. */
-#define CSA_STATIC_SCRATCH_BYTES (4u << 20)
+#define CSA_STATIC_SCRATCH_BYTES (8u << 20)
 int csa_decode_static_scratch(const csa_params *p, const void *q, const int32_t *ctx_len,
                               const csa_entries *C, const csa_index_rows *qI,
                               const csa_index_rows *KI, const float *w, const void *swa_ring,
@@ -260,6 +261,17 @@ int csa_device_status(int *status, int reset, csa_stream_t stream);
  * device status word and raises the abort flag, which csa_device_status(reset = 1) clears.
  * It exists so that the error path of a stalled pipeline can be exercised without a fault. */
 int csa_selftest_wait_timeout(uint64_t limit_ns, csa_stream_t stream);
+
+/* Measurement kernels, no counterpart on the pages: roofline denominators for the library's
+ * kernels, timed by the caller with CUDA events on `stream`.
+ * csa_probe_ffma: `blocks` CTAs of 256 threads, each thread 16 independent FP32 FMA chains of
+ *   `iters` steps (32 * iters FLOP per thread); out [blocks * 256] float receives the results.
+ * csa_probe_read: `blocks` CTAs of 512 threads read the device buffer buf (`bytes`, a multiple
+ *   of 16, 16-byte aligned) `reps` times with 16-byte loads that may hit L2 (smaller than L2:
+ *   the L2 read bandwidth; larger: HBM); out [blocks] float (zeroed by the caller) receives one
+ *   sum per CTA. */
+int csa_probe_ffma(int blocks, int iters, float *out, csa_stream_t stream);
+int csa_probe_read(const void *buf, int64_t bytes, int reps, int blocks, float *out, csa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -82,6 +82,8 @@ def _load():
             "csa_launch_count": (ctypes.c_uint64, []),
             "csa_device_status": (I, [ctypes.POINTER(ctypes.c_int), I, P]),
             "csa_selftest_wait_timeout": (I, [ctypes.c_uint64, P]),
+            "csa_probe_ffma": (I, [I, I, P, P]),
+            "csa_probe_read": (I, [P, I64, I, I, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -216,7 +218,7 @@ def csa_decode(p: Params, q, ctx_len, C, qI, KI, w, swa_ring, sink, rope_tab, to
         "csa_decode")
 
 
-STATIC_SCRATCH_BYTES = 4 << 20  # CSA_STATIC_SCRATCH_BYTES in include/csa.h
+STATIC_SCRATCH_BYTES = 8 << 20  # CSA_STATIC_SCRATCH_BYTES in include/csa.h
 
 
 def csa_decode_static_scratch(p: Params, q, ctx_len, C, qI, KI, w, swa_ring, sink, rope_tab, topk_out, out, lse_out,
@@ -241,6 +243,14 @@ def csa_device_status(reset: bool = True, stream=None) -> int:
     v = ctypes.c_int(0)
     _ok(_load().csa_device_status(ctypes.byref(v), int(reset), _stream(stream)), "csa_device_status")
     return v.value
+
+
+def csa_probe_ffma(blocks: int, iters: int, out: torch.Tensor, stream=None):
+    _ok(_load().csa_probe_ffma(blocks, iters, _ptr(out), _stream(stream)), "csa_probe_ffma")
+
+
+def csa_probe_read(buf: torch.Tensor, reps: int, blocks: int, out: torch.Tensor, stream=None):
+    _ok(_load().csa_probe_read(_ptr(buf), _nbytes(buf), reps, blocks, _ptr(out), _stream(stream)), "csa_probe_read")
 
 
 def csa_selftest_wait_timeout(limit_ns: int, stream=None):

@@ -88,6 +88,14 @@ size_t index_ws_bytes(const csa_params *p) {
     return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
 }
 
+// Partial results of the split-KV decode attention (BF16 activations, the tensor-core path).
+size_t decode_split_bytes(const csa_params *p, int dense) {
+    if (p->act_t != CSA_BF16) return 0;
+    int S = 1, T = 1;
+    decode_split_plan(p->B, p->topk, (int)ncap_of(p), dense, &S, &T);
+    return align_up(decode_partial_bytes(p->B, S));
+}
+
 size_t ws_bytes(const csa_params *p, int op) {
     switch (op) {
     case CSA_OP_INDEX_TOPK:
@@ -100,9 +108,12 @@ size_t ws_bytes(const csa_params *p, int op) {
     case CSA_OP_HCA_PREFILL:
         return widen_bytes(p);
     case CSA_OP_CSA_DECODE:
-        if (p->topk == 0) return 0;
-        return align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) +
-               align_up(sizeof(int32_t) * (size_t)p->B * p->topk);
+        return (p->topk == 0 ? 0
+                             : align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) +
+                                   align_up(sizeof(int32_t) * (size_t)p->B * p->topk)) +
+               decode_split_bytes(p, 0);
+    case CSA_OP_HCA_DECODE:
+        return decode_split_bytes(p, 1);
     default:
         return 0;
     }
@@ -203,12 +214,28 @@ int run_csa_attention(const AttnArgs &a, cudaStream_t st) {
     return launch_status();
 }
 
+// Decode: BF16 runs split-KV on the tensor cores (work items over the key tiles, partial results
+// in the workspace at `part`) followed by the combine step; FP32 the CUDA-core kernel.
+int run_decode_attention(AttnArgs a, void *part, cudaStream_t st) {
+    if (a.act_t == CSA_F32) {
+        launch_attn_simple(a, st);
+        return launch_status();
+    }
+    decode_split_plan(a.B, a.topk, a.ncap, a.dense, &a.split_S, &a.split_T);
+    a.part_o = reinterpret_cast<float *>(part);
+    a.part_ml = reinterpret_cast<float2 *>(reinterpret_cast<char *>(part) +
+                                           (size_t)a.B * a.split_S * 64 * 128 * sizeof(float));
+    if (!launch_csa_tc(a, st)) return CSA_ERR_UNSUPPORTED;
+    launch_decode_combine(a, st);
+    return launch_status();
+}
+
 int run_hca_attention(const AttnArgs &a, cudaStream_t st) {
     if (a.act_t == CSA_F32) {
         launch_attn_simple(a, st);
         return launch_status();
     }
-    if (!(a.decode ? launch_csa_tc(a, st) : launch_hca_tc(a, st))) return CSA_ERR_UNSUPPORTED;
+    if (!launch_hca_tc(a, st)) return CSA_ERR_UNSUPPORTED;
     return launch_status();
 }
 
@@ -366,16 +393,18 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     if (!q || !ctx_len || !swa_ring || !out || !aligned16(q) || !aligned16(swa_ring) || !aligned16(out))
         return CSA_ERR_INVALID;
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
-    if (p->topk > 0) {
-        if (!entries_ok(p, C) || !index_rows_ok(p, qI) || !index_rows_ok(p, KI) || !w) return CSA_ERR_INVALID;
-        if (wsb < ws_bytes(p, CSA_OP_CSA_DECODE) || !ws || !aligned16(ws)) return CSA_ERR_WORKSPACE;
-    }
+    if (p->topk > 0 && (!entries_ok(p, C) || !index_rows_ok(p, qI) || !index_rows_ok(p, KI) || !w))
+        return CSA_ERR_INVALID;
+    const size_t need = ws_bytes(p, CSA_OP_CSA_DECODE);
+    if (need > 0 && (wsb < need || !ws || !aligned16(ws))) return CSA_ERR_WORKSPACE;
     cudaStream_t st = cs(stream);
     int32_t *idx = nullptr;
     const int ncap = (int)ncap_of(p);
+    const size_t sbytes = p->topk > 0 ? align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) : 0;
+    const size_t ibytes = p->topk > 0 ? align_up(sizeof(int32_t) * (size_t)p->B * p->topk) : 0;
+    void *part = need > 0 ? reinterpret_cast<char *>(ws) + sbytes + ibytes : nullptr;
     if (p->topk > 0) {
         float *S = reinterpret_cast<float *>(ws);
-        const size_t sbytes = align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p));
         idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
         IndexArgs ia{};
         ia.qI = qI->data; ia.qI_scale = qI->scale; ia.KI = KI->data; ia.KI_scale = KI->scale;
@@ -394,23 +423,23 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
         a.ncap = 0;
         a.dense = 1;
     }
-    return run_csa_attention(a, st);
+    return run_decode_attention(a, part, st);
 }
 
 int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
                const void *swa_ring, const float *sink, const float *rope_tab, void *out,
                float *lse_out, void *ws, size_t wsb, csa_stream_t stream) {
-    (void)ws;
-    (void)wsb;
     int s = check(p, CSA_OP_HCA_DECODE);
     if (s) return s;
     if (!q || !ctx_len || !swa_ring || !out || !aligned16(q) || !aligned16(swa_ring) || !aligned16(out) ||
         !entries_ok(p, C))
         return CSA_ERR_INVALID;
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    const size_t need = ws_bytes(p, CSA_OP_HCA_DECODE);
+    if (need > 0 && (wsb < need || !ws || !aligned16(ws))) return CSA_ERR_WORKSPACE;
     AttnArgs a = attn_args(p, q, swa_ring, C, nullptr, ctx_len, sink, rope_tab, out, lse_out, 1, 0);
     a.dense = 1;  // every visible entry, in order
-    return run_hca_attention(a, cs(stream));
+    return run_decode_attention(a, ws, cs(stream));
 }
 
 uint64_t csa_launch_count(void) { return launch_counter(); }
@@ -429,6 +458,19 @@ int csa_device_status(int *status, int reset, csa_stream_t stream) {
         if (cudaStreamSynchronize(st) != cudaSuccess) return CSA_ERR_CUDA;
     }
     return CSA_OK;
+}
+
+int csa_probe_ffma(int blocks, int iters, float *out, csa_stream_t stream) {
+    if (blocks < 1 || iters < 1 || !out) return CSA_ERR_INVALID;
+    launch_probe_ffma(blocks, iters, out, cs(stream));
+    return launch_status();
+}
+
+int csa_probe_read(const void *buf, int64_t bytes, int reps, int blocks, float *out, csa_stream_t stream) {
+    if (!buf || !aligned16(buf) || bytes < 16 || bytes % 16 != 0 || reps < 1 || blocks < 1 || !out)
+        return CSA_ERR_INVALID;
+    launch_probe_read(buf, bytes, reps, blocks, out, cs(stream));
+    return launch_status();
 }
 
 int csa_selftest_wait_timeout(uint64_t limit_ns, csa_stream_t stream) {

@@ -90,6 +90,12 @@ struct CsaTcParams {
     int B, L, ncap, topk, n_win, d_rope, mixed, decode, rows;
     int dense, m;   // dense: keys are entries 0 .. visible(t) - 1 in order (no top-k row)
     float scale_log2;
+    // split-KV decode: work item r = (sequence r / S, split r % S) takes the key tiles
+    // [T * (r % S), T * (r % S) + T) of its sequence (compressed tiles, then the window tile) and
+    // writes its unnormalised partial O and per-head (max, sum) instead of the output
+    int split, S, T;
+    float *part_o;     // [items][64 heads][128 dims] float
+    float2 *part_ml;   // [items][64 heads] (running max in log2 units, sum of weights)
 };
 
 namespace {
@@ -97,6 +103,8 @@ namespace {
 struct TokenMeta {
     int n_sel;   // valid top-k entries
     int n_ct;    // compressed tiles
+    int c0;      // first key tile of this work item (the window tile is tile n_ct)
+    int n_tiles; // key tiles of this work item (>= 1)
     int t;       // query position
     int b;       // sequence
     int n_win_t; // window rows that exist (<= n_win)
@@ -227,7 +235,8 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         // Fetch of a token's top-k row (bulk copy) and query rows (TMA) into slot it & 1, issued
         // by one thread as early as the slot is free, so it overlaps the previous token.
         auto fetch = [&](int it2) {
-            const int row2 = (int)blockIdx.x + it2 * (int)gridDim.x;
+            const int item2 = (int)blockIdx.x + it2 * (int)gridDim.x;
+            const int row2 = P.split ? item2 / P.S : item2;  // query row (token) of the item
             const int qs2 = it2 & 1;
             const uint32_t qb = smem_u32(&b_qraw[qs2]);
             mbar_expect_tx(qb, 2 * kH * 128 + (P.dense ? 0 : P.topk * 4));
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             if (named_sync_or(kBarProd, kProducers, !ok)) { ok = false; break; }
             int b, t;
             if (P.decode) {
-                b = row;
+                b = P.split ? row / P.S : row;
                 t = P.ctx[b] - 1;
             } else {
                 b = row / P.L;
@@ -283,6 +292,19 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             mt.b = b;
             mt.n_win_t = pos_ok ? min(P.n_win, t + 1) : 0;
             mt.pos_ok = pos_ok;
+            mt.c0 = 0;
+            mt.n_tiles = mt.n_ct + 1;
+            if (P.split) {
+                const int c0 = (row % P.S) * P.T;
+                if (c0 < mt.n_ct + 1) {
+                    mt.c0 = c0;
+                    mt.n_tiles = min(P.T, mt.n_ct + 1 - c0);
+                } else {  // nothing left for this split: one fully masked tile (no key is valid)
+                    mt.c0 = mt.n_ct;
+                    mt.n_tiles = 1;
+                    mt.n_win_t = 0;
+                }
+            }
             if (ptid == 0) meta[qs] = mt;
             // RoPE on dims 64..127 at position t: head h, chunk pair (c, c+4) of the second half
             if (P.d_rope == 64 && pos_ok) {
@@ -311,9 +333,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             }
             fence_async_smem();
             mbar_arrive(smem_u32(&b_qfull[qs]));
-            // key tiles: compressed tiles, then the window tile
-            const int n_tiles = mt.n_ct + 1;
-            for (int c = 0; c < n_tiles; ++c, ++n) {
+            // key tiles of this item: compressed tiles, then the window tile
+            for (int cl = 0; cl < mt.n_tiles; ++cl, ++n) {
+                const int c = mt.c0 + cl;
                 const int kb = n % kNB;
                 if (n >= kNB && !pwait(smem_u32(&b_kempty[kb]), ((n / kNB) - 1) & 1)) {
                     ok = false;
@@ -454,7 +476,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             for (int it = 0; it < n_tok_cta && ok; ++it) {
                 const int qs = it & 1;
                 if (!mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kWaitNs, &g_abort)) { ok = false; break; }
-                const int n_tiles = meta[qs].n_ct + 1;
+                const int n_tiles = meta[qs].n_tiles;
                 for (int c = 0; c < n_tiles; ++c, ++n) {
                     const int kb = n % kNB, sb = n & 1;
                     if (!mbar_wait(smem_u32(&b_kfull[kb]), (n / kNB) & 1, kWaitNs, &g_abort)) { ok = false; break; }
@@ -507,11 +529,12 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
             const TokenMeta mt = meta[qs];
             mbar_arrive(smem_u32(&b_qempty[qs]));
-            const int n_tiles = mt.n_ct + 1;
+            const int n_tiles = mt.n_tiles;
 #pragma unroll
             for (int e = 0; e < 32; ++e) lpart[e] = 0.0f;
             bool failed = false;
-            for (int c = 0; c < n_tiles; ++c, ++n) {
+            for (int cl = 0; cl < n_tiles; ++cl, ++n) {
+                const int c = mt.c0 + cl;
                 const int sb = n & 1, pb = n & 1;
                 note(mbar_wait(smem_u32(&b_sfull[sb]), (n >> 1) & 1, kWaitNs, &g_abort));
                 tc_fence_after();
@@ -579,7 +602,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         lpart[e] *= f;
                         rescale_o |= f != 1.0f;
                     }
-                    rescale_o = c > 0 && named_sync_or(bar_wg, 128, rescale_o);
+                    rescale_o = cl > 0 && named_sync_or(bar_wg, 128, rescale_o);
                     if (rescale_o) {
                         // O^T holds the P V of the previous tiles of this token: wait for the last
                         note(mbar_wait(smem_u32(&b_pempty[(n - 1) & 1]), ((n - 1) >> 1) & 1, kWaitNs, &g_abort));
@@ -638,8 +661,11 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 const float l = (s_red[4 * wg][lane] + s_red[4 * wg + 1][lane]) +
                                 (s_red[4 * wg + 2][lane] + s_red[4 * wg + 3][lane]);
                 const float m = s_m[h];
-                float f;
-                if (P.sink) {
+                float f = 1.0f;
+                if (P.split) {
+                    // the combine step merges the items of the sequence and applies the sink
+                    P.part_ml[((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * kH + h] = make_float2(m, l);
+                } else if (P.sink) {
                     const float s2 = P.sink[h] * 1.4426950408889634f;
                     const float mf = fmaxf(m, s2);
                     f = exp2f(m - mf) / (l * exp2f(m - mf) + exp2f(s2 - mf));
@@ -647,7 +673,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     f = 1.0f / l;
                 }
                 s_fo[h] = f;
-                if (P.lse && mt.pos_ok)
+                if (P.lse && mt.pos_ok && !P.split)
                     P.lse[(int64_t)((P.decode ? mt.b : (int64_t)mt.b * P.L + mt.t)) * kH + h] =
                         (m + log2f(l)) * 0.6931471805599453f;
             }
@@ -658,6 +684,13 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             tmem_ld32_sync(tmem + lane_base + kOCol + ob * kH + h0, o);  // lane kl = output dim
             tc_fence_before();
             mbar_arrive(smem_u32(&b_oempty[ob]));
+            if (P.split) {
+                // unnormalised partial O of this item: [head][dim], dims across the warp's lanes
+                float *po = P.part_o + (((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * kH + h0) * 128 + kl;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) __stcg(po + e * 128, o[e]);
+                continue;
+            }
             {
                 const float4 *f4 = reinterpret_cast<const float4 *>(s_fo + h0);
 #pragma unroll
@@ -772,8 +805,10 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     if (!csa_tc_supported(a)) return false;
     CsaTcParams P;
     memset(&P, 0, sizeof(P));
-    const int rows = a.decode ? a.B : a.B * a.L;
-    bool ok = make_map_3d(&P.mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, 128, (uint64_t)rows * kH, 1, 64, kH,
+    const int qrows = a.decode ? a.B : a.B * a.L;  // query rows (tokens)
+    const bool split = a.decode && a.split_S > 0;
+    const int rows = split ? a.B * a.split_S : qrows;  // work items
+    bool ok = make_map_3d(&P.mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, 128, (uint64_t)qrows * kH, 1, 64, kH,
                           CU_TENSOR_MAP_SWIZZLE_128B);
     if (!a.decode)
         ok = ok && make_map_3d(&P.mkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kv_rope, 128, a.L, a.B, 64, kTile,
@@ -801,6 +836,11 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.decode = a.decode; P.rows = rows;
     P.dense = a.dense; P.m = a.m;
     P.scale_log2 = a.scale * 1.4426950408889634f;
+    P.split = split ? 1 : 0;
+    P.S = split ? a.split_S : 1;
+    P.T = split ? a.split_T : 1;
+    P.part_o = a.part_o;
+    P.part_ml = a.part_ml;
     int dev = 0, sms = 148, smem_max = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -820,6 +860,85 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     }
     count_launches(1);
     return true;
+}
+
+
+// ---------------------------------------------------------------------------------------
+// split-KV decode: the plan and the combine step
+// ---------------------------------------------------------------------------------------
+
+// Key tiles of a decode token at most (compressed tiles, then the window tile), items per
+// sequence S and tiles per item T, sized so that the B * S items fill about two waves of CTAs.
+void decode_split_plan(int B, int topk, int ncap, int dense, int *S, int *T) {
+    const int tiles = (dense ? (ncap + csa_tc::kTile - 1) / csa_tc::kTile
+                             : (topk + csa_tc::kTile - 1) / csa_tc::kTile) + 1;
+    int t = (int)ceil_div64((int64_t)tiles * B, 296);
+    if (t < 1) t = 1;
+    *T = t;
+    *S = (tiles + t - 1) / t;
+}
+
+size_t decode_partial_bytes(int B, int S) {
+    return (size_t)B * S * csa_tc::kH * (128 * sizeof(float) + sizeof(float2));
+}
+
+// One warp per (sequence, head): merges the S partial results of the sequence in a fixed order
+// (max of the running maxima, rescaled sums and outputs), adds the sink to the denominator,
+// normalises, rotates the RoPE half back by the query position and stores BF16. Lane i holds
+// dims i, 32 + i, 64 + i and 96 + i, so a RoPE pair (64 + i, 96 + i) sits in one lane.
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float *__restrict__ part_o,
+                                                             const float2 *__restrict__ part_ml,
+                                                             const int32_t *__restrict__ ctx,
+                                                             const float *__restrict__ sink,
+                                                             const float2 *__restrict__ rope,
+                                                             __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
+                                                             int B, int S, int L, int d_rope) {
+    constexpr int kH = csa_tc::kH;
+    const int lane = threadIdx.x & 31;
+    const int gw = (int)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (gw >= B * kH) return;
+    const int b = gw / kH, h = gw % kH;
+    const int t = ctx[b] - 1;
+    if (t < 0 || t >= L) return;  // reported by the attention kernel; nothing is stored
+    const float2 *ml = part_ml + (int64_t)b * S * kH + h;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[(int64_t)s * kH].x);
+    const float s2 = sink ? sink[h] * 1.4426950408889634f : -INFINITY;
+    const float Mf = fmaxf(M, s2);
+    float l = 0.0f, o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
+    for (int s = 0; s < S; ++s) {
+        const float2 v = ml[(int64_t)s * kH];
+        if (v.x == -INFINITY) continue;  // an item with no valid key
+        const float wgt = exp2f(v.x - Mf);
+        l = fmaf(v.y, wgt, l);
+        const float *po = part_o + (((int64_t)b * S + s) * kH + h) * 128;
+        o0 = fmaf(__ldcg(po + lane), wgt, o0);
+        o1 = fmaf(__ldcg(po + 32 + lane), wgt, o1);
+        o2 = fmaf(__ldcg(po + 64 + lane), wgt, o2);
+        o3 = fmaf(__ldcg(po + 96 + lane), wgt, o3);
+    }
+    const float f = 1.0f / (l + (sink ? exp2f(s2 - Mf) : 0.0f));
+    o0 *= f; o1 *= f; o2 *= f; o3 *= f;
+    if (d_rope == 64) {  // inverse RoPE of the pair (64 + lane, 96 + lane) at position t
+        const float2 cs = rope[(int64_t)t * 32 + lane];
+        const float x = o2, y = o3;
+        o2 = x * cs.x + y * cs.y;
+        o3 = -x * cs.y + y * cs.x;
+    }
+    __nv_bfloat16 *orow = out + ((int64_t)b * kH + h) * 128;
+    orow[lane] = __float2bfloat16_rn(o0);
+    orow[32 + lane] = __float2bfloat16_rn(o1);
+    orow[64 + lane] = __float2bfloat16_rn(o2);
+    orow[96 + lane] = __float2bfloat16_rn(o3);
+    if (lse && lane == 0) lse[(int64_t)b * kH + h] = (Mf + log2f(l)) * 0.6931471805599453f;
+}
+
+void launch_decode_combine(const AttnArgs &a, cudaStream_t st) {
+    const int warps = a.B * csa_tc::kH;
+    decode_combine_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
+        a.part_o, a.part_ml, a.ctx, a.sink, reinterpret_cast<const float2 *>(a.rope_tab),
+        reinterpret_cast<__nv_bfloat16 *>(a.out), a.lse, a.B, a.split_S, a.L, a.d_rope);
+    count_launches(1);
 }
 
 }  // namespace csa

@@ -23,14 +23,15 @@
 //     visible entries take all of them (threshold -inf);
 //  3. isel_tc_kernel<kFilter>: every visible score on the tensor cores, compared with its row's
 //     threshold in the epilogue; (entry, score) pairs at or above it are appended to the row's
-//     candidate list (at most kCap kept, all counted);
+//     candidates -- each epilogue warp to its own segment of the row (at most kSeg kept, all
+//     counted), in entry order, with the counts in registers (lane q counts token q);
 //  4. cand_select_kernel: exact top-k of each row's candidates (radix select on the order keys of
-//     the scores, ties to the lower index, emission in index order from bitmaps). A row whose
-//     list holds fewer than k or more than kCap candidates is queued instead;
+//     the scores, ties to the lower index, emission in index order from bitmaps). A row with
+//     fewer than k candidates, or a segment that overflowed, is queued instead;
 //  5. isel_fallback_kernel: each queued row's full score row on CUDA cores (float sums of the
 //     exact FP8 products) and the exact full-row select.
-// The result never depends on the sample being right: when a row's list holds at least k and at
-// most kCap candidates, every score above the threshold is in it, so its top k are.
+// The result never depends on the sample being right: when a row holds at least k candidates and
+// no segment overflowed, every score above the threshold is among them, so its top k are.
 //
 // Tensor-core kernel (persistent, one CTA per SM, 576 threads). One MMA tile: D[128 entries]
 // [128 columns = TQ tokens x H_I heads] = KI_tile (128 x 64 E4M3) times qI_tile^T, K = 64 as
@@ -81,8 +82,8 @@ struct IselTcParams {
     const float *thr;        // filter: [nrows] thresholds
     float *samp;             // sample: [nrows][ld_samp]
     int64_t ld_samp;
-    uint2 *cand;             // filter: [nrows][kIselCap] (entry, score bits)
-    int *cnt;                // filter: [nrows] candidates found (may exceed kIselCap)
+    uint2 *cand;             // filter: [nrows][16 warps][kIselSeg] (entry, score bits)
+    int *cnt;                // filter: [nrows][16 warps] candidates found (may exceed kIselSeg)
     int L, m, ncap, b, t0, nrows, n_qt;
 };
 
@@ -111,10 +112,9 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
     __shared__ __align__(8) uint64_t b_qfull[2], b_qempty[2], b_kfull[kNK], b_kempty[kNK], b_dfull[kWG],
         b_dempty[kWG];
     __shared__ uint32_t tmem_slot;
-    __shared__ __align__(16) float s_wq[2][kN];  // w * q_scale per (token, head) of a query slot
-    __shared__ float s_thr[2][TQ];               // per-token thresholds (filter)
-    __shared__ int s_nvis[2][TQ];                // entries visible to each token (0 past the chunk)
-    __shared__ int s_cnt[2][TQ];                 // candidates appended per token (filter)
+    __shared__ __align__(16) float s_wq[2][kN];  // w * q_scale / 2 per (token, head) of a query slot
+    __shared__ __align__(16) float s_thr[2][TQ]; // per-token thresholds (filter)
+    __shared__ __align__(16) int s_nvis[2][TQ];  // entries visible to each token (0 past the chunk)
     __shared__ int s_fin[2];                     // epilogue warps done with a query slot
     __shared__ int s_tq0[2];                     // first token of a query slot
 
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
                 float v = 0.0f;
                 if (tok <= last_row) {
                     const int64_t gr = ((int64_t)P.b * P.L + tok) * HI + rr % HI;
-                    v = P.w[gr] * P.q_scale[gr];
+                    v = 0.5f * (P.w[gr] * P.q_scale[gr]);  // exact halving: pairs with x + |x| = 2 ReLU(x)
                 }
                 s_wq[qs][rr] = v;
             }
@@ -185,7 +185,6 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
                 const bool in = tok <= last_row;
                 s_nvis[qs][lane] = in ? visible_entries(tok, P.m, P.ncap) : 0;
                 s_thr[qs][lane] = (MODE == kFilter && in) ? P.thr[tok - P.t0] : INFINITY;
-                s_cnt[qs][lane] = 0;
             }
             if (lane == 0) s_tq0[qs] = tq0;
             __syncwarp();
@@ -273,6 +272,9 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
             const int qs = iq & 1;
             if (!wwait(smem_u32(&b_qfull[qs]), (iq >> 1) & 1)) { ok = false; break; }
             const int tq0 = s_tq0[qs];
+            // filter: this warp's candidates of token q go to its own segment of row q, in entry
+            // order; lane q keeps the segment's count (no atomics, no shared state)
+            int my_cnt = 0;
             const float4 *wq4 = reinterpret_cast<const float4 *>(s_wq[qs]);
             for (int nn = n + ((g - n) & 3); nn < n + net; nn += kWG) {
                 const int e = nn - n;
@@ -281,8 +283,19 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
                 const float sk = j < P.ncap ? __ldg(kscale + j) : 0.0f;
                 if (!wwait(smem_u32(&b_dfull[g]), (nn >> 2) & 1)) { ok = false; break; }
                 tc_fence_after();
-                // scores of the CT tokens of one 16-column chunk from registers r
+                // scores of the CT tokens of one 16-column chunk from registers r. ReLU(x) * w is
+                // formed as (x + |x|) * (w / 2) -- exact, and on the FMA pipe rather than the
+                // half-rate ALU pipe that fmax would use. Tiles that every token of the query
+                // tile sees in full skip the per-token visibility test.
+                const bool full = (et + 1) * kJ * P.m - 1 <= tq0 && tq0 + TQ - 1 <= last_row;
                 auto chunk = [&](const uint32_t (&r)[16], int c) {
+                    float thr_c[CT];
+                    int nv_c[CT];
+#pragma unroll
+                    for (int qq = 0; qq < CT; ++qq) {
+                        thr_c[qq] = s_thr[qs][c * CT + qq];
+                        nv_c[qq] = s_nvis[qs][c * CT + qq];
+                    }
 #pragma unroll
                     for (int qq = 0; qq < CT; ++qq) {
                         const int q = c * CT + qq;
@@ -291,29 +304,26 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
                         for (int h4 = 0; h4 < HI / 4; ++h4) {
                             const float4 w4 = wq4[(q * HI) / 4 + h4];
                             const uint32_t *x = r + qq * HI + 4 * h4;
-                            acc = f2_fma(f2_pack(w4.x, w4.y),
-                                         f2_pack(fmaxf(__uint_as_float(x[0]), 0.0f), fmaxf(__uint_as_float(x[1]), 0.0f)),
-                                         acc);
-                            acc = f2_fma(f2_pack(w4.z, w4.w),
-                                         f2_pack(fmaxf(__uint_as_float(x[2]), 0.0f), fmaxf(__uint_as_float(x[3]), 0.0f)),
-                                         acc);
+                            const float x0 = __uint_as_float(x[0]), x1 = __uint_as_float(x[1]);
+                            const float x2 = __uint_as_float(x[2]), x3 = __uint_as_float(x[3]);
+                            acc = f2_fma(f2_pack(w4.x, w4.y), f2_pack(x0 + fabsf(x0), x1 + fabsf(x1)), acc);
+                            acc = f2_fma(f2_pack(w4.z, w4.w), f2_pack(x2 + fabsf(x2), x3 + fabsf(x3)), acc);
                         }
                         const float2 a2 = f2_unpack(acc);
                         const float s = fmaf(a2.x + a2.y, sk, 0.0f);  // + 0 turns -0 into +0
-                        const bool vis = j < s_nvis[qs][q];
+                        const bool vis = full || j < nv_c[qq];
                         const int64_t row = tq0 + q - P.t0;
                         if (MODE == kSample) {
                             if (vis) P.samp[row * P.ld_samp + e * kJ + jl] = s;
                         } else {
-                            const bool hit = vis && s >= s_thr[qs][q];
+                            const bool hit = vis && s >= thr_c[qq];
                             const unsigned bal = __ballot_sync(0xffffffffu, hit);
                             if (bal != 0u) {
-                                int base = 0;
-                                if (lane == 0) base = atomicAdd(&s_cnt[qs][q], __popc(bal));
-                                base = __shfl_sync(0xffffffffu, base, 0);
-                                const int pos = base + __popc(bal & lt_mask);
-                                if (hit && pos < kIselCap)
-                                    P.cand[row * kIselCap + pos] = make_uint2((uint32_t)j, __float_as_uint(s));
+                                const int pos = __shfl_sync(0xffffffffu, my_cnt, q) + __popc(bal & lt_mask);
+                                if (hit && pos < kIselSeg)
+                                    P.cand[(row * kEpiWarps + warp) * kIselSeg + pos] =
+                                        make_uint2((uint32_t)j, __float_as_uint(s));
+                                if (lane == q) my_cnt += __popc(bal);
                             }
                         }
                     }
@@ -339,8 +349,9 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
                 }
             }
             if (!ok) break;
-            // this warp is done with the query slot; the last of the 16 warps publishes the
-            // candidate counts and frees the slot
+            if (MODE == kFilter && lane < TQ && tq0 + lane <= last_row)
+                P.cnt[(int64_t)(tq0 + lane - P.t0) * kEpiWarps + warp] = my_cnt;
+            // this warp is done with the query slot; the last of the 16 warps frees it
             __syncwarp();
             int v = 0;
             if (lane == 0) {
@@ -349,9 +360,6 @@ __global__ void __launch_bounds__(isel::kThreads, 1) isel_tc_kernel(const __grid
             }
             v = __shfl_sync(0xffffffffu, v, 0);
             if (v == kEpiWarps - 1) {
-                __threadfence_block();
-                if (MODE == kFilter && lane < TQ && tq0 + lane <= last_row) P.cnt[tq0 + lane - P.t0] = s_cnt[qs][lane];
-                __syncwarp();
                 if (lane == 0) {
                     s_fin[qs] = 0;
                     mbar_arrive(smem_u32(&b_qempty[qs]));
@@ -429,9 +437,10 @@ __global__ void __launch_bounds__(tk::kThreads) sample_thr_kernel(IselRowArgs a)
 // exact top-k among a row's candidates
 // ---------------------------------------------------------------------------------------
 
-constexpr int kSelPer = kIselCap / tk::kThreads;  // candidates per thread (registers)
+constexpr int kSelPer = kIselCap / tk::kThreads;  // candidates per thread (registers): one per segment
+static_assert(kSelPer == 16 && kIselSeg == tk::kThreads, "thread t holds slot t of every segment");
 
-__global__ void __launch_bounds__(tk::kThreads) cand_select_kernel(IselRowArgs a) {
+__global__ void __launch_bounds__(tk::kThreads, 4) cand_select_kernel(IselRowArgs a) {
     using namespace tk;
     extern __shared__ uint32_t dyn[];
     uint32_t *hist = dyn;                 // [kBins]
@@ -447,8 +456,16 @@ __global__ void __launch_bounds__(tk::kThreads) cand_select_kernel(IselRowArgs a
         for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
         return;
     }
-    const int c = a.cnt[r];
-    if (c < k || c > kIselCap) {  // the threshold misjudged the row: queue it for the exact path
+    // the row's candidates: 16 segments (one per filter warp) of up to kIselSeg entries
+    const int *wc = a.cnt + (int64_t)r * 16;
+    int c = 0;
+    bool over = false;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        c += wc[u];
+        over |= wc[u] > kIselSeg;
+    }
+    if (c < k || over) {  // the threshold misjudged the row: queue it for the exact path
         if (threadIdx.x == 0) a.fb_rows[atomicAdd(a.fb_count, 1)] = r;
         return;
     }
@@ -460,10 +477,10 @@ __global__ void __launch_bounds__(tk::kThreads) cand_select_kernel(IselRowArgs a
     const uint2 *cl = a.cand + (int64_t)r * kIselCap;
 #pragma unroll
     for (int u = 0; u < kSelPer; ++u) {
-        const int i = threadIdx.x + u * kThreads;
-        const uint2 v = i < c ? __ldcs(cl + i) : make_uint2(0u, 0u);
-        key[u] = i < c ? key_of(__uint_as_float(v.y)) : 0u;
-        idx[u] = i < c ? (int32_t)v.x : -1;
+        const bool live = (int)threadIdx.x < wc[u];
+        const uint2 v = live ? __ldcs(cl + u * kIselSeg + threadIdx.x) : make_uint2(0u, 0u);
+        key[u] = live ? key_of(__uint_as_float(v.y)) : 0u;
+        idx[u] = live ? (int32_t)v.x : -1;
     }
     // radix rounds over the key bits 31..21, 20..10 and 9..0: the k-th largest key K* and how
     // many keys equal to it are taken
@@ -569,7 +586,7 @@ inline int64_t isel_ld_samp(int ncap) {
 }
 inline int64_t isel_ld_slot(int ncap) { return ((int64_t)ncap + 3) / 4 * 4; }
 inline size_t isel_row_bytes(int ncap) {
-    return sizeof(float) * (size_t)isel_ld_samp(ncap) + sizeof(uint2) * (size_t)kIselCap + 3 * sizeof(int);
+    return sizeof(float) * (size_t)isel_ld_samp(ncap) + sizeof(uint2) * (size_t)kIselCap + 18 * sizeof(int);
 }
 }  // namespace
 
@@ -583,7 +600,7 @@ int64_t isel_chunk_rows(int L, int ncap) {
 size_t isel_workspace_bytes(int L, int ncap) {
     const size_t R = (size_t)isel_chunk_rows(L, ncap);
     return al256(sizeof(float) * R * (size_t)isel_ld_samp(ncap)) + al256(sizeof(float) * R) +
-           al256(sizeof(uint2) * R * kIselCap) + 2 * al256(sizeof(int) * R) + al256(16) +
+           al256(sizeof(uint2) * R * kIselCap) + al256(sizeof(int) * R * 16) + al256(sizeof(int) * R) + al256(16) +
            al256(sizeof(float) * (size_t)isel::kFbCtas * (size_t)isel_ld_slot(ncap));
 }
 
@@ -602,7 +619,7 @@ int launch_index_select(const IselArgs &a, cudaStream_t st) {
     float *samp = reinterpret_cast<float *>(take(sizeof(float) * R * isel_ld_samp(a.ncap)));
     float *thr = reinterpret_cast<float *>(take(sizeof(float) * R));
     uint2 *cand = reinterpret_cast<uint2 *>(take(sizeof(uint2) * R * kIselCap));
-    int *cnt = reinterpret_cast<int *>(take(sizeof(int) * R));
+    int *cnt = reinterpret_cast<int *>(take(sizeof(int) * R * 16));
     int *fb_rows = reinterpret_cast<int *>(take(sizeof(int) * R));
     int *fb_count = reinterpret_cast<int *>(take(16));
     float *slots = reinterpret_cast<float *>(take(sizeof(float) * kFbCtas * isel_ld_slot(a.ncap)));

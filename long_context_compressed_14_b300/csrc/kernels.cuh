@@ -64,10 +64,16 @@ struct AttnArgs {
     float scale;
     int decode, act_t, kv_t;
     int dense;             // 1: the key list is every visible entry in order (HCA decode), no idx
+    // split-KV decode (0 = off): S work items per sequence, T key tiles per item; partial results
+    // in part_o [B*S, H, 128] float and part_ml [B*S, H] (max, sum), merged by the combine step
+    int split_S, split_T;
+    float *part_o;
+    float2 *part_ml;
 };
 
 // FP8 prefill indexer with the top-k selection fused in (index_select.cu).
-constexpr int kIselCap = 4096;         // candidates kept per query row
+constexpr int kIselSeg = 256;          // candidates kept per query row and filter warp
+constexpr int kIselCap = 16 * kIselSeg; // candidates kept per query row (16 filter warps)
 constexpr int kIselSampleStride = 16;  // the threshold sample holds every 16th entry tile
 struct IselArgs {
     const void *qI;        // FP8 codes [B, L, H_I, d_I]
@@ -89,6 +95,8 @@ void count_launches(int n);
 uint64_t launch_counter();
 
 void launch_status_reset(cudaStream_t st);
+void launch_probe_ffma(int blocks, int iters, float *out, cudaStream_t st);
+void launch_probe_read(const void *buf, int64_t bytes, int reps, int blocks, float *out, cudaStream_t st);
 void launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 void launch_rope_table(float *tab, int rope_len, int d_rope, float theta, cudaStream_t st);
 void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
@@ -104,6 +112,10 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st);
 // Mixed-precision entries (prefill) widened to BF16 rows [B, ncap, 128] in a.ws (csa_widen_bytes
 // bytes); returns the widened array.
 size_t csa_widen_bytes(const AttnArgs &a);
+// split-KV decode plan (items per sequence S, tiles per item T), partial-result bytes, combine
+void decode_split_plan(int B, int topk, int ncap, int dense, int *S, int *T);
+size_t decode_partial_bytes(int B, int S);
+void launch_decode_combine(const AttnArgs &a, cudaStream_t st);
 const void *launch_widen_mixed(const AttnArgs &a, cudaStream_t st);
 
 }  // namespace csa

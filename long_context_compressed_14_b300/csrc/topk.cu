@@ -326,9 +326,55 @@ __global__ void __launch_bounds__(tk::kThreads) topk_radix_kernel(TopkArgs a) {
     for (int i = written + threadIdx.x; i < k; i += kThreads) out[i] = -1;
 }
 
+// Decode: one query row per sequence, so one CTA of 1024 threads per row (the rows are few and
+// their latency is the step's): the exact full-row select (a histogram of the whole row, the
+// threshold bin's keys collected and selected exactly) and emission in index order.
+constexpr int kDecTopkThreads = 1024;
+
+__global__ void __launch_bounds__(kDecTopkThreads) decode_topk_kernel(TopkArgs a) {
+    using namespace tk;
+    extern __shared__ uint32_t dyn[];
+    uint32_t *hist = dyn;                                                   // [kBins]
+    uint32_t *cand_key = hist + kBins;                                      // [kCandCap]
+    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + kCandCap);  // [kCandCap]
+    uint32_t *bm_gt = reinterpret_cast<uint32_t *>(cand_idx + kCandCap);   // [nw], bm_eq [nw]
+    __shared__ int s_tmp[kDecTopkThreads / 32];
+    __shared__ int s_res[2];
+    __shared__ int s_ncand;
+    const int r = blockIdx.x;
+    const int64_t t = (int64_t)a.ctx[r] - 1;
+    int32_t *out = a.out + (int64_t)r * a.k;
+    const int k = a.k;
+    if (t < 0 || t >= a.L) {  // decode ctx_len outside [1, capacity]: reported by the attention
+        for (int i = threadIdx.x; i < k; i += kDecTopkThreads) out[i] = -1;
+        return;
+    }
+    const int n = visible_entries(t, a.m, a.ncap);
+    if (n <= k) {
+        for (int i = threadIdx.x; i < k; i += kDecTopkThreads) out[i] = i < n ? i : -1;
+        return;
+    }
+    const int nw = (n + 31) >> 5;
+    uint32_t *bm_eq = bm_gt + nw;
+    for (int i = threadIdx.x; i < 2 * nw; i += kDecTopkThreads) bm_gt[i] = 0;
+    __syncthreads();
+    const float *S = a.S + (int64_t)r * a.ldS;
+    const int need = select_full<kDecTopkThreads>(S, n, k, hist, cand_key, cand_idx, bm_gt, bm_eq, s_tmp, s_res,
+                                                  &s_ncand);
+    emit_selection<kDecTopkThreads>(bm_gt, bm_eq, nw, need, k, out, s_tmp);
+}
+
 void launch_topk(const TopkArgs &a, cudaStream_t st) {
     using namespace tk;
     if (a.nrows <= 0) return;
+    if (a.decode && a.ncap <= kMaxBitmapN) {
+        const int nw = (a.ncap + 31) / 32;
+        const size_t smem = sizeof(uint32_t) * ((size_t)kBins + 2 * kCandCap + 2 * (size_t)nw);
+        cudaFuncSetAttribute(decode_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        decode_topk_kernel<<<a.nrows, kDecTopkThreads, smem, st>>>(a);
+        count_launches(1);
+        return;
+    }
     if (a.ncap <= kMaxBitmapN) {
         const int nw = (a.ncap + 31) / 32;
         const size_t smem = sizeof(uint32_t) * ((size_t)kBins + 2 * kCandCap + 2 * (size_t)nw);

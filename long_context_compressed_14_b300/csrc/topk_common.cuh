@@ -1,8 +1,9 @@
 // topk_common.cuh -- block-wide pieces of the exact top-k selection shared by the top-k kernels
 // (topk.cu) and the fused indexer selection (index_select.cu): block scans, histogram threshold
 // search, the order-preserving key of a score, the exact full-row select and the emission of a
-// selection in ascending index order from bitmaps. Every routine assumes a CTA of tk::kThreads
-// threads.
+// selection in ascending index order from bitmaps. Every routine is block-wide over a CTA of NT
+// threads (a template argument, tk::kThreads = 256 unless stated; NT a multiple of 256 up to
+// 1024, so that a 2048-bin histogram splits evenly over the threads).
 #pragma once
 
 #include "common.cuh"
@@ -22,7 +23,9 @@ constexpr int kMaxBitmapN = 1 << 18;   // rows up to this many entries use the b
 // block-wide scans
 // ---------------------------------------------------------------------------------------
 
-// Exclusive prefix sum of v across the CTA in thread order; *total = sum. Uses s_tmp[kWarps].
+// Exclusive prefix sum of v across the CTA (NT threads) in thread order; *total = sum. Uses
+// s_tmp[NT / 32].
+template <int NT = tk::kThreads>
 __device__ __forceinline__ int block_excl_sum(int v, int *s_tmp, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
@@ -35,7 +38,7 @@ __device__ __forceinline__ int block_excl_sum(int v, int *s_tmp, int *total) {
     __syncthreads();
     int base = 0, tot = 0;
 #pragma unroll
-    for (int w = 0; w < tk::kWarps; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
         const int t = s_tmp[w];
         base += w < warp ? t : 0;
         tot += t;
@@ -45,7 +48,7 @@ __device__ __forceinline__ int block_excl_sum(int v, int *s_tmp, int *total) {
     return base + x - v;
 }
 
-// exclusive prefix sum of a 0/1 flag across the CTA (generic kernel)
+// exclusive prefix sum of a 0/1 flag across a CTA of tk::kThreads threads (generic kernel)
 __device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned bal = __ballot_sync(0xffffffffu, flag);
@@ -64,33 +67,34 @@ __device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int *tot
 }
 
 // Visits every score of the row once: fn(index, key). float4 loads (rows are 16-byte aligned).
-template <typename F>
+template <int NT = tk::kThreads, typename F>
 __device__ __forceinline__ void for_each_key(const float *S, int n, F &&fn) {
     const int n4 = n >> 2;
     const float4 *S4 = reinterpret_cast<const float4 *>(S);
-    for (int i4 = threadIdx.x; i4 < n4; i4 += tk::kThreads) {
+    for (int i4 = threadIdx.x; i4 < n4; i4 += NT) {
         const float4 v = __ldcg(S4 + i4);
         fn(4 * i4 + 0, score_key(v.x));
         fn(4 * i4 + 1, score_key(v.y));
         fn(4 * i4 + 2, score_key(v.z));
         fn(4 * i4 + 3, score_key(v.w));
     }
-    for (int i = 4 * n4 + threadIdx.x; i < n; i += tk::kThreads) fn(i, score_key(__ldcg(S + i)));
+    for (int i = 4 * n4 + threadIdx.x; i < n; i += NT) fn(i, score_key(__ldcg(S + i)));
 }
 
 // In a histogram of `nbins` bins (nbins / kThreads per thread), finds the bin b holding the
 // `want`-th largest element (1-based, counted from the top bin down): *bin = b and
 // *above = number of elements in bins above b. Block-wide; every thread gets the result.
+template <int NT = tk::kThreads>
 __device__ __forceinline__ void find_threshold_bin(const uint32_t *hist, int nbins, int want, int *s_tmp,
                                                    int *s_res, int *bin, int *above) {
-    const int per = nbins / tk::kThreads;  // 4 (2048 bins) or 1 (<= 512 bins, padded)
+    const int per = nbins / NT;  // 4 (2048 bins) or 1 (<= 512 bins, padded)
     // thread i owns bins [per*i, per*i + per); reverse order so that an exclusive prefix sum
     // in thread order counts the bins above
-    const int owner = tk::kThreads - 1 - threadIdx.x;
+    const int owner = NT - 1 - threadIdx.x;
     int mine = 0;
     for (int q = 0; q < per; ++q) mine += (int)hist[per * owner + q];
     int tot;
-    const int before = block_excl_sum(mine, s_tmp, &tot);  // elements in bins above my range
+    const int before = block_excl_sum<NT>(mine, s_tmp, &tot);  // elements in bins above my range
     if (before < want && before + mine >= want) {
         int run = before;
         for (int q = per - 1; q >= 0; --q) {
@@ -131,18 +135,20 @@ __device__ __forceinline__ float key_floor_value(uint32_t key) {
 // selected exactly (or, when that bin is too large for shared memory, by radix passes over the
 // row). On return bm_gt holds every key > K*, bm_eq every key == K*; the result is the number
 // of keys == K* to take (lowest indices first).
+template <int NT = tk::kThreads>
 __device__ inline int select_full(const float *S, int n, int k, uint32_t *hist, uint32_t *cand_key, int32_t *cand_idx,
                            uint32_t *bm_gt, uint32_t *bm_eq, int *s_tmp, int *s_res, int *s_ncand) {
     using namespace tk;
+    constexpr int kThreads = NT;
     for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
     if (threadIdx.x == 0) *s_ncand = 0;
     __syncthreads();
-    for_each_key(S, n, [&](int, uint32_t key) { atomicAdd(&hist[key >> kBinShift], 1u); });
+    for_each_key<NT>(S, n, [&](int, uint32_t key) { atomicAdd(&hist[key >> kBinShift], 1u); });
     __syncthreads();
     int bstar, above;
-    find_threshold_bin(hist, kBins, k, s_tmp, s_res, &bstar, &above);
+    find_threshold_bin<NT>(hist, kBins, k, s_tmp, s_res, &bstar, &above);
     int need = k - above;
-    for_each_key(S, n, [&](int i, uint32_t key) {
+    for_each_key<NT>(S, n, [&](int i, uint32_t key) {
         const int bin = (int)(key >> kBinShift);
         if (bin > bstar) {
             atomicOr(&bm_gt[i >> 5], 1u << (i & 31));
@@ -168,7 +174,7 @@ __device__ inline int select_full(const float *S, int n, int k, uint32_t *hist, 
             }
             __syncthreads();
             int b2, ab2;
-            find_threshold_bin(hist, kThreads, need, s_tmp, s_res, &b2, &ab2);  // bins >= 128 are empty
+            find_threshold_bin<NT>(hist, kThreads, need, s_tmp, s_res, &b2, &ab2);  // bins >= 128 are empty
             prefix |= (uint32_t)b2 << shift;
             mask |= 127u << shift;
             need -= ab2;
@@ -189,18 +195,18 @@ __device__ inline int select_full(const float *S, int n, int k, uint32_t *hist, 
             const uint32_t wmask = (1u << widths[round]) - 1u;
             for (int i = threadIdx.x; i < kThreads; i += kThreads) hist[i] = 0;
             __syncthreads();
-            for_each_key(S, n, [&](int, uint32_t key) {
+            for_each_key<NT>(S, n, [&](int, uint32_t key) {
                 if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & wmask], 1u);
             });
             __syncthreads();
             int b2, ab2;
-            find_threshold_bin(hist, kThreads, need, s_tmp, s_res, &b2, &ab2);
+            find_threshold_bin<NT>(hist, kThreads, need, s_tmp, s_res, &b2, &ab2);
             prefix |= (uint32_t)b2 << shift;
             mask |= wmask << shift;
             need -= ab2;
         }
         const uint32_t kstar = prefix;
-        for_each_key(S, n, [&](int i, uint32_t key) {
+        for_each_key<NT>(S, n, [&](int i, uint32_t key) {
             if ((key >> kBinShift) != (uint32_t)bstar) return;
             if (key > kstar) atomicOr(&bm_gt[i >> 5], 1u << (i & 31));
             else if (key == kstar) atomicOr(&bm_eq[i >> 5], 1u << (i & 31));
@@ -211,14 +217,16 @@ __device__ inline int select_full(const float *S, int n, int k, uint32_t *hist, 
 }
 
 // Emission in index order from the bitmaps: every gt bit and the first `need` eq bits.
+template <int NT = tk::kThreads>
 __device__ inline void emit_selection(uint32_t *bm_gt, uint32_t *bm_eq, int nw, int need, int k, int32_t *out, int *s_tmp) {
     using namespace tk;
+    constexpr int kThreads = NT;
     const int per = (nw + kThreads - 1) / kThreads;
     const int w0 = threadIdx.x * per, w1 = min(nw, w0 + per);
     int my_eq = 0;
     for (int w = w0; w < w1; ++w) my_eq += __popc(bm_eq[w]);
     int tot_eq;
-    int eq_before = block_excl_sum(my_eq, s_tmp, &tot_eq);
+    int eq_before = block_excl_sum<NT>(my_eq, s_tmp, &tot_eq);
     int my_sel = 0;
     for (int w = w0; w < w1; ++w) {
         uint32_t e = bm_eq[w];
@@ -235,7 +243,7 @@ __device__ inline void emit_selection(uint32_t *bm_gt, uint32_t *bm_eq, int nw, 
         my_sel += __popc(bm_gt[w] | kept);
     }
     int tot_sel;
-    int pos = block_excl_sum(my_sel, s_tmp, &tot_sel);
+    int pos = block_excl_sum<NT>(my_sel, s_tmp, &tot_sel);
     for (int w = w0; w < w1; ++w) {
         uint32_t sl = bm_gt[w] | bm_eq[w];
         while (sl) {

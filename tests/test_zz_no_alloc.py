@@ -16,9 +16,9 @@ import synth
 pytestmark = pytest.mark.gpu
 
 
-def _decode_setup(lib, B=4, L=8192, topk=256):
+def _decode_setup(lib, B=4, L=8192, topk=256, c_t="bf16"):
     from long_context_compressed_14_b300.pipeline import DecodeLayer
-    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=B, L=L, topk=topk)
+    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=B, L=L, topk=topk, c_t=c_t)
     inp = synth.decode_layer(wl, csa=True)
     inp["ctx"] = torch.tensor([L, 1, 77, L - 3191][:B], dtype=torch.int32)
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -28,11 +28,12 @@ def _decode_setup(lib, B=4, L=8192, topk=256):
     return wl, d, layer
 
 
-def test_static_scratch_decode_matches_workspace_decode(lib):
-    wl, d, layer = _decode_setup(lib)
+@pytest.mark.parametrize("c_t", ["bf16", "mixed"])
+def test_static_scratch_decode_matches_workspace_decode(lib, c_t):
+    wl, d, layer = _decode_setup(lib, c_t=c_t)
     p = layer.p
     assert lib.csa_workspace_bytes(p, lib.OP_CSA_DECODE) <= lib.STATIC_SCRATCH_BYTES
-    C = (d["C"], None, None)
+    C = layer.C if layer.C is not None else (d["C"], None, None)
     ref = torch.empty_like(layer.out)
     ref_idx = torch.empty_like(layer.topk)
     lib.csa_decode(p, d["q"], d["ctx"], C, layer.qI, layer.KI, d["w"], d["ring"], d["sink"], layer.rope, ref_idx, ref,
@@ -51,8 +52,11 @@ def test_static_scratch_decode_matches_workspace_decode(lib):
 
 
 def test_static_scratch_refuses_a_layer_larger_than_the_array(lib):
-    # 16 sequences x 131072 cached tokens at m = 4: 16 x 32768 float scores (2 MiB) fit; a
-    # 1M-token cache (16 x 262144 floats = 16 MiB) does not and is refused before any launch.
+    # 16 sequences x 131072 cached tokens at m = 4 fit (2 MiB of scores, 2.7 MB of split-KV
+    # partial results); a 1M-token cache (16 x 262144 float scores = 16 MiB) does not and is
+    # refused before any launch.
+    fits = lib.make_params(B=16, L=131072, H=64, m=4, topk=512)
+    assert lib.csa_workspace_bytes(fits, lib.OP_CSA_DECODE) <= lib.STATIC_SCRATCH_BYTES
     big = lib.make_params(B=16, L=1 << 20, H=64, m=4, topk=512)
     assert lib.csa_workspace_bytes(big, lib.OP_CSA_DECODE) > lib.STATIC_SCRATCH_BYTES
     with pytest.raises(lib.CsaError) as e:
