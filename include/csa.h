@@ -148,6 +148,30 @@ int kv_compress(const csa_params *p, const void *kv, const float *z, const float
                 const float *rope_tab, const csa_entries *C, const csa_index_rows *KI,
                 void *kv_rope, csa_stream_t stream);
 
+/* Incremental decode state ([P2] 訓練インフラの革新 §5: a heterogeneous inference cache -- a
+ * state cache of the recent raw tokens, where the incomplete block waits, and the compressed
+ * KV cache; 提案手法 §1: overlapping compression, sliding window, partial RoPE). Appends the
+ * new token of each sequence, at position u = ctx_len[b] - 1:
+ *  - ring[b][u mod n_win] = its raw row rotated by RoPE at u (the sliding-window keys that
+ *    csa_decode / hca_decode read);
+ *  - state_kv[b][u mod 2m] = its raw row, state_z[b][u mod 2m] = z, state_kI[b][u mod 2m] = its
+ *    raw indexer key (when kI_new is given): the last 2m raw tokens, the window of the next entry;
+ *  - when u completes block j = u / m (that is, (u + 1) % m == 0): entry j, computed from the
+ *    state as kv_compress computes it (softmax weights over rows [(j-1)m, (j+1)m) with z[.,0]
+ *    in block j and z[.,1] in block j-1, RoPE at (j+1)m - 1), is written to C per kv_t, and KI_j
+ *    (the same weights over the indexer keys) to KI per idx_t. Entries of incomplete blocks are
+ *    not written (no decode query sees them).
+ * A prefill of L0 tokens hands over to decode with: C and KI from kv_compress, ring slots filled
+ * from kv_rope (the last n_win rows), and the state from the last 2m raw rows of kv, z and kI.
+ *   kv_new [B, d] act_t (before RoPE); z_new [B, 2] float; kI_new [B, d_I] float or NULL;
+ *   ctx_len [B] int32 (device; counts the new token; 1 <= ctx_len <= L, the cache capacity);
+ *   ring [B, n_win, d] act_t; state_kv [B, 2m, d] act_t; state_z [B, 2m, 2] float;
+ *   state_kI [B, 2m, d_I] float (NULL when kI_new is NULL); C, KI: caches [B, ceil(L/m), ...].
+ * A position outside [0, L) is skipped and recorded as CSA_ERR_BOUNDS. */
+int kv_append(const csa_params *p, const void *kv_new, const float *z_new, const float *kI_new,
+              const int32_t *ctx_len, const float *rope_tab, void *ring, void *state_kv, float *state_z,
+              float *state_kI, const csa_entries *C, const csa_index_rows *KI, csa_stream_t stream);
+
 /* Lightning-indexer score and top-k selection for prefill rows ([P2] 提案手法 §1 CSA;
  * [P5] 一.1: each query attends only to its top-k compressed entries; [P4] 17:10).
  * s(t, j) = sum_h w[t,h] * ReLU(qI[t,h] . KI[j]) over the entries visible to t

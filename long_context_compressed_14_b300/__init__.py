@@ -72,6 +72,7 @@ def _load():
             "csa_rope_table": (I, [P, I, I, ctypes.c_float, P]),
             "csa_quant_fp8_rows": (I, [P, I64, I, P, P, P]),
             "kv_compress": (I, [PP, P, P, P, P, PE, PI, P, P]),
+            "kv_append": (I, [PP, P, P, P, P, P, P, P, P, P, PE, PI, P]),
             "csa_index_topk": (I, [PP, PI, PI, P, P, P, Z, P]),
             "csa_prefill": (I, [PP, P, P, PE, PI, PI, P, P, P, P, P, P, P, Z, P]),
             "hca_prefill": (I, [PP, P, P, PE, P, P, P, P, P, Z, P]),
@@ -175,6 +176,14 @@ def kv_compress(p: Params, kv, z, kI_raw, rope_tab, C, KI, kv_rope, stream=None)
     _ok(_load().kv_compress(ctypes.byref(p), _ptr(kv), _ptr(z), _ptr(kI_raw), _ptr(rope_tab),
                             _byref(_entries(C)), _byref(_rows(KI)), _ptr(kv_rope), _stream(stream)),
         "kv_compress")
+
+
+def kv_append(p: Params, kv_new, z_new, kI_new, ctx_len, rope_tab, ring, state_kv, state_z, state_kI, C, KI,
+              stream=None):
+    _ok(_load().kv_append(ctypes.byref(p), _ptr(kv_new), _ptr(z_new), _ptr(kI_new), _ptr(ctx_len), _ptr(rope_tab),
+                          _ptr(ring), _ptr(state_kv), _ptr(state_z), _ptr(state_kI), _byref(_entries(C)),
+                          _byref(_rows(KI)), _stream(stream)),
+        "kv_append")
 
 
 def csa_index_topk(p: Params, qI, KI, w, topk_out, ws, stream=None):

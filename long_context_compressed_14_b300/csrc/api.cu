@@ -110,7 +110,9 @@ size_t ws_bytes(const csa_params *p, int op) {
     case CSA_OP_CSA_DECODE:
         return (p->topk == 0 ? 0
                              : align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) +
-                                   align_up(sizeof(int32_t) * (size_t)p->B * p->topk)) +
+                                   align_up(sizeof(int32_t) * (size_t)p->B * p->topk) +
+                                   align_up(sizeof(uint32_t) * (size_t)p->B * 2048) +
+                                   align_up(decode_select_bytes(p->B, p->topk))) +
                decode_split_bytes(p, 0);
     case CSA_OP_HCA_DECODE:
         return decode_split_bytes(p, 1);
@@ -306,6 +308,29 @@ int kv_compress(const csa_params *p, const void *kv, const float *z, const float
     return launch_status();
 }
 
+int kv_append(const csa_params *p, const void *kv_new, const float *z_new, const float *kI_new,
+              const int32_t *ctx_len, const float *rope_tab, void *ring, void *state_kv, float *state_z,
+              float *state_kI, const csa_entries *C, const csa_index_rows *KI, csa_stream_t stream) {
+    int s = check(p, CSA_OP_HCA_DECODE);
+    if (s) return s;
+    if (!kv_new || !z_new || !ctx_len || !ring || !state_kv || !state_z || !entries_ok(p, C)) return CSA_ERR_INVALID;
+    if (!aligned16(kv_new) || !aligned16(ring) || !aligned16(state_kv)) return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    if (kI_new) {
+        if (!state_kI || p->d_I != kDI || !index_rows_ok(p, KI)) return CSA_ERR_INVALID;
+        if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3) return CSA_ERR_INVALID;
+    }
+    AppendArgs a{};
+    a.kv_new = kv_new; a.z_new = z_new; a.kI_new = kI_new; a.ctx = ctx_len; a.rope_tab = rope_tab;
+    a.ring = ring; a.state_kv = state_kv; a.state_z = state_z; a.state_kI = state_kI;
+    a.c_data = C->data; a.c_rope = reinterpret_cast<__nv_bfloat16 *>(C->rope); a.c_scale = C->scale;
+    a.ki_data = kI_new ? KI->data : nullptr; a.ki_scale = kI_new ? KI->scale : nullptr;
+    a.B = p->B; a.L = p->L; a.m = p->m; a.ncap = (int)ncap_of(p); a.n_win = p->n_win; a.d_rope = p->d_rope;
+    a.act_t = p->act_t; a.kv_t = p->kv_t; a.idx_t = p->idx_t;
+    launch_kv_append(a, cs(stream));
+    return launch_status();
+}
+
 int csa_index_topk(const csa_params *p, const csa_index_rows *qI, const csa_index_rows *KI,
                    const float *w, int32_t *topk_out, void *ws, size_t wsb, csa_stream_t stream) {
     int s = check(p, CSA_OP_INDEX_TOPK);
@@ -402,7 +427,13 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     const int ncap = (int)ncap_of(p);
     const size_t sbytes = p->topk > 0 ? align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) : 0;
     const size_t ibytes = p->topk > 0 ? align_up(sizeof(int32_t) * (size_t)p->B * p->topk) : 0;
-    void *part = need > 0 ? reinterpret_cast<char *>(ws) + sbytes + ibytes : nullptr;
+    const size_t hbytes = p->topk > 0 ? align_up(sizeof(uint32_t) * (size_t)p->B * 2048) : 0;
+    const size_t dbytes = p->topk > 0 ? align_up(decode_select_bytes(p->B, p->topk)) : 0;
+    char *wsc = reinterpret_cast<char *>(ws);
+    uint32_t *hist = p->topk > 0 ? reinterpret_cast<uint32_t *>(wsc + sbytes + ibytes) : nullptr;
+    // selection lists: the two counters per row right after the histogram (one memset clears both)
+    int *sel_cnt = p->topk > 0 ? reinterpret_cast<int *>(wsc + sbytes + ibytes + hbytes) : nullptr;
+    void *part = need > 0 ? wsc + sbytes + ibytes + hbytes + dbytes : nullptr;
     if (p->topk > 0) {
         float *S = reinterpret_cast<float *>(ws);
         idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
@@ -411,11 +442,31 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
         ia.w = w; ia.ctx = ctx_len; ia.S = S; ia.ldS = score_ld(p);
         ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap; ia.idx_t = p->idx_t;
         ia.decode = 1;
-        launch_indexer(ia, st);
-        TopkArgs ta{};
-        ta.S = S; ta.ldS = score_ld(p); ta.ctx = ctx_len; ta.out = idx;
-        ta.L = p->L; ta.m = p->m; ta.ncap = ncap; ta.k = p->topk; ta.nrows = p->B; ta.decode = 1;
-        launch_topk(ta, st);
+        // FP8 keys: the tensor-core scan, which also counts each row's keys for the top-k; the
+        // exact FP32 scan (and batches of fewer than 16 query rows) on CUDA cores
+        bool counted = false;
+        if (decode_index_tc_supported(ia)) {
+            if (cudaMemsetAsync(hist, 0, hbytes + 2 * sizeof(int) * (size_t)p->B, st) != cudaSuccess)
+                return CSA_ERR_CUDA;
+            counted = launch_decode_index_tc(ia, hist, st);
+            if (!counted) return CSA_ERR_UNSUPPORTED;
+        } else {
+            launch_indexer(ia, st);
+        }
+        if (counted) {
+            DecSelArgs da{};
+            da.S = S; da.ldS = score_ld(p); da.hist = hist; da.ctx = ctx_len; da.out = idx;
+            da.cnt = sel_cnt;
+            da.above = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(sel_cnt) + decode_select_above_off(p->B));
+            da.bin = reinterpret_cast<uint2 *>(reinterpret_cast<char *>(sel_cnt) + decode_select_bin_off(p->B, p->topk));
+            da.L = p->L; da.m = p->m; da.ncap = ncap; da.k = p->topk; da.B = p->B;
+            launch_decode_select(da, st);
+        } else {
+            TopkArgs ta{};
+            ta.S = S; ta.ldS = score_ld(p); ta.ctx = ctx_len; ta.out = idx;
+            ta.L = p->L; ta.m = p->m; ta.ncap = ncap; ta.k = p->topk; ta.nrows = p->B; ta.decode = 1;
+            launch_topk(ta, st);
+        }
     }
     AttnArgs a = attn_args(p, q, swa_ring, p->topk > 0 ? C : nullptr, idx, ctx_len, sink, rope_tab, out,
                            lse_out, 1, p->topk);

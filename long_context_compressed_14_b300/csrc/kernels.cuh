@@ -1,6 +1,7 @@
 // kernels.cuh -- launch interfaces between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -38,6 +39,7 @@ struct IndexArgs {
 
 struct TopkArgs {
     const float *S;
+    const uint32_t *hist;  // decode: [rows][2048] histogram of the rows' top 11 key bits, or NULL
     int64_t ldS;
     const int32_t *ctx;    // decode positions (ctx-1) or NULL for prefill
     int32_t *out;          // prefill: out + ((b*L)+t)*k; decode: out + b*k
@@ -90,6 +92,27 @@ int64_t isel_chunk_rows(int L, int ncap);
 bool isel_supported(const IselArgs &a);
 int launch_index_select(const IselArgs &a, cudaStream_t st);  // returns a csa_status
 
+// Incremental decode state (append.cu): one new token per sequence into the window ring, the
+// state cache of the last 2m raw tokens and, when it completes a block, the compressed caches.
+struct AppendArgs {
+    const void *kv_new;    // [B, d] act_t, before RoPE
+    const float *z_new;    // [B, 2]
+    const float *kI_new;   // [B, d_I] or NULL
+    const int32_t *ctx;    // [B]: tokens including the new one
+    const float *rope_tab;
+    void *ring;            // [B, n_win, d] act_t
+    void *state_kv;        // [B, 2m, d] act_t
+    float *state_z;        // [B, 2m, 2]
+    float *state_kI;       // [B, 2m, d_I]
+    void *c_data;
+    __nv_bfloat16 *c_rope;
+    float *c_scale;
+    void *ki_data;
+    float *ki_scale;
+    int B, L, m, ncap, n_win, d_rope, act_t, kv_t, idx_t;
+};
+void launch_kv_append(const AppendArgs &a, cudaStream_t st);
+
 // host-side count of kernel launches (every launch_* adds the kernels it launched)
 void count_launches(int n);
 uint64_t launch_counter();
@@ -104,6 +127,29 @@ void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, f
 void launch_kv_compress(const CompressArgs &a, cudaStream_t st);
 void launch_indexer(const IndexArgs &a, cudaStream_t st);
 void launch_topk(const TopkArgs &a, cudaStream_t st);
+// decode top-k from the scan's key histogram: a collect launch over slices of every row and a
+// finishing launch per row (topk.cu). cnt [B][2] must be zero before the launch.
+struct DecSelArgs {
+    const float *S;
+    int64_t ldS;
+    const uint32_t *hist;  // [B][2048]
+    const int32_t *ctx;
+    int32_t *out;          // [B][k]
+    int *cnt;              // [B][2]: keys above the threshold bin, keys in it
+    int32_t *above;        // [B][k]
+    uint2 *bin;            // [B][4096] (key, index)
+    int L, m, ncap, k, B;
+    int slices;            // collecting CTAs per row (set by the launcher)
+};
+size_t decode_select_bytes(int B, int k);
+size_t decode_select_above_off(int B);
+size_t decode_select_bin_off(int B, int k);
+void launch_decode_select(const DecSelArgs &a, cudaStream_t st);
+// decode indexer scan on the tensor cores (FP8, H_I in {4, 8, 16}, B * H_I >= 16): scores into
+// a.S and the per-row key histogram into hist [B][2048] (zeroed before the launch); false when
+// the layer is outside what it handles (launching nothing)
+bool decode_index_tc_supported(const IndexArgs &a);
+bool launch_decode_index_tc(const IndexArgs &a, uint32_t *hist, cudaStream_t st);
 void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
 // tensor-core kernels: return false (launching nothing) when the configuration is outside
 // what they handle

@@ -359,9 +359,186 @@ __global__ void __launch_bounds__(kDecTopkThreads) decode_topk_kernel(TopkArgs a
     for (int i = threadIdx.x; i < 2 * nw; i += kDecTopkThreads) bm_gt[i] = 0;
     __syncthreads();
     const float *S = a.S + (int64_t)r * a.ldS;
-    const int need = select_full<kDecTopkThreads>(S, n, k, hist, cand_key, cand_idx, bm_gt, bm_eq, s_tmp, s_res,
-                                                  &s_ncand);
+    int need;
+    if (a.hist) {  // the indexer scan already counted the row's keys
+        for (int i = threadIdx.x; i < kBins; i += kDecTopkThreads) hist[i] = __ldcg(a.hist + (int64_t)r * kBins + i);
+        __syncthreads();
+        need = select_from_hist<kDecTopkThreads>(S, n, k, hist, cand_key, cand_idx, bm_gt, bm_eq, s_tmp, s_res,
+                                                 &s_ncand);
+    } else {
+        need = select_full<kDecTopkThreads>(S, n, k, hist, cand_key, cand_idx, bm_gt, bm_eq, s_tmp, s_res, &s_ncand);
+    }
     emit_selection<kDecTopkThreads>(bm_gt, bm_eq, nw, need, k, out, s_tmp);
+}
+
+// Decode top-k over a known key histogram (the tensor-core indexer scan counts each row's keys)
+// in two launches, so that a row is not left to one SM:
+//  collect (a number of CTAs per row, each over at most kDecMaxSlice scores): the threshold bin b* of the row's k-th largest key from the
+//    histogram (the same in every CTA of the row); each CTA scans one slice of the row and
+//    appends the indices of keys above bin b* to the row's `above` list and the (key, index)
+//    pairs of keys in bin b* to the row's bin list (positions taken by warp-aggregated atomics;
+//    the order does not matter, the selection is emitted in index order);
+//  finish (one CTA per row): the exact k-th largest key among the bin's keys, then emission in
+//    index order from bitmaps. A bin that overflows its list takes the exact full-row path.
+constexpr int kDecBinCap = 4096;
+constexpr int kDecMaxSlice = 4096;  // scores per collecting CTA at most (kept in registers)
+constexpr int kDecFinishThreads = 512;
+
+__global__ void __launch_bounds__(tk::kThreads) decode_collect_kernel(DecSelArgs a) {
+    using namespace tk;
+    __shared__ uint32_t hist[kBins];
+    __shared__ int s_tmp[kWarps];
+    __shared__ int s_res[2];
+    const int r = blockIdx.x / a.slices, g = blockIdx.x % a.slices;
+    const int64_t t = (int64_t)a.ctx[r] - 1;
+    int32_t *out = a.out + (int64_t)r * a.k;
+    const int k = a.k;
+    if (t < 0 || t >= a.L) {  // reported by the attention kernel
+        if (g == 0)
+            for (int i = threadIdx.x; i < k; i += kThreads) out[i] = -1;
+        return;
+    }
+    const int n = visible_entries(t, a.m, a.ncap);
+    if (n <= k) {
+        if (g == 0)
+            for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
+        return;
+    }
+    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = __ldcg(a.hist + (int64_t)r * kBins + i);
+    __syncthreads();
+    int bstar, above;
+    find_threshold_bin(hist, kBins, k, s_tmp, s_res, &bstar, &above);
+    const int per = (n + a.slices - 1) / a.slices;
+    const int i0 = g * per, i1 = min(n, i0 + per);
+    const float *S = a.S + (int64_t)r * a.ldS;
+    // the slice's keys stay in registers: one pass counts (per thread, then a block scan, then
+    // one atomic per list per CTA), the second writes at the positions found
+    constexpr int kPer = (kDecMaxSlice + kThreads - 1) / kThreads;
+    uint32_t key[kPer];
+    int ngt = 0, neq = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = i0 + u * kThreads + (int)threadIdx.x;
+        key[u] = i < i1 ? key_of(__ldcg(S + i)) : 0u;
+        const int bin = i < i1 ? (int)(key[u] >> kBinShift) : -1;
+        ngt += bin > bstar;
+        neq += bin == bstar;
+    }
+    __shared__ int s_base[2];
+    int tot_gt, tot_eq;
+    int pg = block_excl_sum(ngt, s_tmp, &tot_gt);
+    int pe = block_excl_sum(neq, s_tmp, &tot_eq);
+    if (threadIdx.x == 0) {
+        s_base[0] = tot_gt ? atomicAdd(a.cnt + 2 * r, tot_gt) : 0;
+        s_base[1] = tot_eq ? atomicAdd(a.cnt + 2 * r + 1, tot_eq) : 0;
+    }
+    __syncthreads();
+    pg += s_base[0];
+    pe += s_base[1];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = i0 + u * kThreads + (int)threadIdx.x;
+        if (i >= i1) continue;
+        const int bin = (int)(key[u] >> kBinShift);
+        if (bin > bstar) {
+            if (pg < k) a.above[(int64_t)r * k + pg] = i;
+            ++pg;
+        } else if (bin == bstar) {
+            if (pe < kDecBinCap) a.bin[(int64_t)r * kDecBinCap + pe] = make_uint2(key[u], (uint32_t)i);
+            ++pe;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kDecFinishThreads) decode_finish_kernel(DecSelArgs a) {
+    using namespace tk;
+    constexpr int NT = kDecFinishThreads;
+    extern __shared__ uint32_t dyn[];
+    uint32_t *hist = dyn;                                                    // [kBins]
+    uint32_t *cand_key = hist + kBins;                                       // [kDecBinCap]
+    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + kDecBinCap);  // [kDecBinCap]
+    uint32_t *bm_gt = reinterpret_cast<uint32_t *>(cand_idx + kDecBinCap);   // [nw], bm_eq [nw]
+    __shared__ int s_tmp[NT / 32];
+    __shared__ int s_res[2];
+    __shared__ int s_ncand;
+    const int r = blockIdx.x;
+    const int64_t t = (int64_t)a.ctx[r] - 1;
+    if (t < 0 || t >= a.L) return;
+    const int n = visible_entries(t, a.m, a.ncap);
+    const int k = a.k;
+    if (n <= k) return;  // written by the collect step
+    int32_t *out = a.out + (int64_t)r * k;
+    const int nw = (n + 31) >> 5;
+    uint32_t *bm_eq = bm_gt + nw;
+    for (int i = threadIdx.x; i < 2 * nw; i += NT) bm_gt[i] = 0;
+    const int n_above = __ldcg(a.cnt + 2 * r), c = __ldcg(a.cnt + 2 * r + 1);
+    int need;
+    if (c > kDecBinCap || n_above >= k) {
+        // the threshold bin holds more keys than the list (heavy ties): exact full-row path
+        __syncthreads();
+        need = select_full<NT>(a.S + (int64_t)r * a.ldS, n, k, hist, cand_key, cand_idx, bm_gt, bm_eq, s_tmp, s_res,
+                               &s_ncand);
+    } else {
+        for (int i = threadIdx.x; i < c; i += NT) {
+            const uint2 v = __ldcg(a.bin + (int64_t)r * kDecBinCap + i);
+            cand_key[i] = v.x;
+            cand_idx[i] = (int32_t)v.y;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < n_above; i += NT) {
+            const int j = __ldcg(a.above + (int64_t)r * k + i);
+            atomicOr(&bm_gt[j >> 5], 1u << (j & 31));
+        }
+        // the bin's keys share their top 11 bits: radix rounds over the low 21 (7 bits each)
+        need = k - n_above;
+        uint32_t prefix = cand_key[0] & (~0u << kBinShift), mask = ~0u << kBinShift;
+        for (int round = 0; round < 3; ++round) {
+            const int shift = 14 - 7 * round;
+            for (int i = threadIdx.x; i < NT; i += NT) hist[i] = 0;
+            __syncthreads();
+            for (int i = threadIdx.x; i < c; i += NT) {
+                const uint32_t key = cand_key[i];
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 127u], 1u);
+            }
+            __syncthreads();
+            int b2, ab2;
+            find_threshold_bin<NT>(hist, NT, need, s_tmp, s_res, &b2, &ab2);  // bins >= 128 are empty
+            prefix |= (uint32_t)b2 << shift;
+            mask |= 127u << shift;
+            need -= ab2;
+        }
+        for (int i = threadIdx.x; i < c; i += NT) {
+            const uint32_t key = cand_key[i];
+            const int j = cand_idx[i];
+            if (key > prefix) atomicOr(&bm_gt[j >> 5], 1u << (j & 31));
+            else if (key == prefix) atomicOr(&bm_eq[j >> 5], 1u << (j & 31));
+        }
+        __syncthreads();
+    }
+    emit_selection<NT>(bm_gt, bm_eq, nw, need, k, out, s_tmp);
+}
+
+// Layout of the selection lists after the two counters per row: the `above` list at
+// decode_select_above_off, the bin list at decode_select_bin_off (both 256-byte aligned).
+size_t decode_select_above_off(int B) { return ((size_t)B * 2 * sizeof(int) + 255) / 256 * 256; }
+size_t decode_select_bin_off(int B, int k) {
+    return (decode_select_above_off(B) + (size_t)B * k * sizeof(int32_t) + 255) / 256 * 256;
+}
+size_t decode_select_bytes(int B, int k) {
+    return decode_select_bin_off(B, k) + (size_t)B * kDecBinCap * sizeof(uint2);
+}
+
+void launch_decode_select(const DecSelArgs &a, cudaStream_t st) {
+    using namespace tk;
+    DecSelArgs b = a;
+    b.slices = (int)((a.ncap + kDecMaxSlice - 1) / kDecMaxSlice);  // each slice fits the registers
+    if (b.slices < 16) b.slices = 16;
+    decode_collect_kernel<<<a.B * b.slices, kThreads, 0, st>>>(b);
+    const int nw = (a.ncap + 31) / 32;
+    const size_t smem = sizeof(uint32_t) * ((size_t)kBins + 2 * (size_t)kDecBinCap + 2 * (size_t)nw);
+    cudaFuncSetAttribute(decode_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    decode_finish_kernel<<<a.B, kDecFinishThreads, smem, st>>>(b);
+    count_launches(2);
 }
 
 void launch_topk(const TopkArgs &a, cudaStream_t st) {

@@ -135,16 +135,32 @@ __device__ __forceinline__ float key_floor_value(uint32_t key) {
 // selected exactly (or, when that bin is too large for shared memory, by radix passes over the
 // row). On return bm_gt holds every key > K*, bm_eq every key == K*; the result is the number
 // of keys == K* to take (lowest indices first).
+// The same when the histogram of the row's top 11 key bits is already known: hist (shared
+// memory, kBins counters) holds it on entry and is reused as scratch.
+template <int NT = tk::kThreads>
+__device__ inline int select_from_hist(const float *S, int n, int k, uint32_t *hist, uint32_t *cand_key,
+                                       int32_t *cand_idx, uint32_t *bm_gt, uint32_t *bm_eq, int *s_tmp, int *s_res,
+                                       int *s_ncand);
+
 template <int NT = tk::kThreads>
 __device__ inline int select_full(const float *S, int n, int k, uint32_t *hist, uint32_t *cand_key, int32_t *cand_idx,
                            uint32_t *bm_gt, uint32_t *bm_eq, int *s_tmp, int *s_res, int *s_ncand) {
     using namespace tk;
     constexpr int kThreads = NT;
     for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
-    if (threadIdx.x == 0) *s_ncand = 0;
     __syncthreads();
     for_each_key<NT>(S, n, [&](int, uint32_t key) { atomicAdd(&hist[key >> kBinShift], 1u); });
     __syncthreads();
+    return select_from_hist<NT>(S, n, k, hist, cand_key, cand_idx, bm_gt, bm_eq, s_tmp, s_res, s_ncand);
+}
+
+template <int NT>
+__device__ inline int select_from_hist(const float *S, int n, int k, uint32_t *hist, uint32_t *cand_key,
+                                       int32_t *cand_idx, uint32_t *bm_gt, uint32_t *bm_eq, int *s_tmp, int *s_res,
+                                       int *s_ncand) {
+    using namespace tk;
+    constexpr int kThreads = NT;
+    if (threadIdx.x == 0) *s_ncand = 0;
     int bstar, above;
     find_threshold_bin<NT>(hist, kBins, k, s_tmp, s_res, &bstar, &above);
     int need = k - above;

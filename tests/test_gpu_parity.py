@@ -513,6 +513,26 @@ def test_decode(lib, csa, c_t):
     _check_decode(wl, inp, layer, out, csa, range(4))
 
 
+def test_decode_heavy_ties(lib):
+    # sequences whose indexer weights are all zero score 0 on every entry: the whole row ties at
+    # the threshold and the lowest indices must win (the others by score)
+    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=65536, topk=512)
+    from long_context_compressed_14_b300.pipeline import DecodeLayer
+    inp = synth.decode_layer(wl, csa=True)
+    inp["ctx"] = torch.tensor([65536, 40000, 65536, 3000], dtype=torch.int32)
+    inp["w"][0] = 0.0
+    inp["w"][2] = 0.0
+    layer = DecodeLayer.create(wl, csa=True)
+    d = _dev(inp)
+    layer.load_caches(d)
+    out = layer.run(d)
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
+    got = layer.topk.cpu().numpy()
+    assert np.array_equal(got[0], np.arange(512)) and np.array_equal(got[2], np.arange(512))
+    _check_decode(wl, inp, layer, out, True, (1, 3))
+
+
 def test_device_status_clean(lib):
     torch.cuda.synchronize()
     assert lib.csa_device_status() == 0
