@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode record of the default line")
     ap.add_argument("--no-probes", action="store_true", help="skip the FP8 / FFMA / L2 peak probes")
+    ap.add_argument("--no-projections", action="store_true", help="skip the projections record of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle sample")
     return ap.parse_args()
 
@@ -431,6 +432,49 @@ def measure_decode(lib, args, pk, name="decode_b16_ctx131072"):
                          "bytes_per_step": byts, "peak_note": f"HBM copy ({pk['src']}); whole step, both layers"}}
 
 
+def measure_projections(lib, args, wl, pk):
+    """The projections on either side of the attention core for both layers of the layer-pair
+    workload (hidden 4096 -> q, kv, indexer inputs, compression logits; the grouped output
+    projection back to 4096), timed with CUDA events over a few steps on BF16 tensors resident
+    in HBM (larger than L2)."""
+    from long_context_compressed_14_b300.pipeline import Projections
+    rows = wl.B * wl.L
+    stream = torch.cuda.current_stream()
+    layers, flops = [], 0.0
+    for layer, csa in ((0, True), (1, False)):
+        P = synth.projection_inputs(wl, layer, csa=csa, rows=rows)
+        proj = Projections(wl, csa, P)
+        layers.append((proj, P["x"].cuda()))
+        n_in = wl.H * wl.d + wl.d + P["Widx"].shape[0]
+        flops += 2.0 * rows * wl.hidden * n_in
+        flops += 2.0 * rows * (wl.H * wl.d // wl.groups) * wl.d_g * wl.groups + 2.0 * rows * wl.groups * wl.d_g * wl.hidden
+        del P
+    o = torch.randn((rows, wl.H, wl.d), device="cuda").to(torch.bfloat16)
+
+    def step():
+        for proj, x in layers:
+            proj.inputs(x)
+            proj.output(o)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    ach = flops / (ms / 1e3) / 1e12
+    del layers, o
+    torch.cuda.empty_cache()
+    return {"what": "input projections (hidden 4096 -> q, kv, indexer inputs, logits) and the grouped output "
+                    "projection (8 groups x 512 -> 4096) of both layers, outside the attention step",
+            "ms_per_step": ms, "tflop_per_step": flops / 1e12, "TFLOP/s": ach, "peak": pk["bf16_sus"],
+            "frac": ach / pk["bf16_sus"], "peak_note": f"BF16 dense sustained ({pk['src']})"}
+
+
 def run_mine(args, rank, world, local_rank):
     import long_context_compressed_14_b300 as lib
     wl = synth.WORKLOADS[args.workload]
@@ -509,6 +553,8 @@ def run_mine(args, rank, world, local_rank):
         line["cuda_graph"] = True
     if wl.kind == "pair" and not args.no_decode:
         line["decode"] = measure_decode(lib, args, pk)
+    if wl.kind == "pair" and not args.no_projections:
+        line["projections"] = measure_projections(lib, args, wl, pk)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     return line

@@ -267,6 +267,27 @@ int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
                const void *swa_ring, const float *sink, const float *rope_tab, void *out,
                float *lse_out, void *ws, size_t ws_bytes, csa_stream_t stream);
 
+/* The projections on either side of the attention core ([P2] 概要: V4-Flash hidden size 4096;
+ * 提案手法 §1 CSA: shared-KV multi-query attention with a grouped output projection; [P5] 一.1
+ * 共享KV MQA与分组输出投影), as one BF16 GEMM on the tensor cores with FP32 accumulation:
+ *   C[M, N] = A[M, K] B[N, K]^T, A and B row-major BF16 with row strides lda, ldb (elements,
+ *   multiples of 8), K a multiple of 64.
+ *   groups > 1: the block-diagonal (grouped) product -- output columns [g N/groups, (g+1)
+ *   N/groups) read A's columns [g K, (g+1) K), so A has groups * K columns and B stacks the
+ *   groups' [N/groups, K] matrices; N/groups must be a multiple of 256.
+ * The output columns go to up to four segments: segment s receives columns [col0, col1) into a
+ * row-major tensor `ptr` (row stride ld elements, dtype CSA_BF16 or CSA_F32, column col0 at
+ * offset 0), so that one product can write several separate tensors (q, kv, the indexer
+ * inputs). Device pointers; asynchronous on stream. */
+typedef struct {
+    void *ptr;
+    int64_t ld;
+    int col0, col1;
+    int dtype;
+} csa_gemm_out;
+int csa_gemm_bf16(const void *A, int64_t lda, const void *B, int64_t ldb, int M, int N, int K, int groups,
+                  const csa_gemm_out *outs, int n_outs, csa_stream_t stream);
+
 /* Number of kernels this library has launched in the process so far (host counter). */
 uint64_t csa_launch_count(void);
 

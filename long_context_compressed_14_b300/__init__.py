@@ -46,6 +46,11 @@ class Entries(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("rope", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
 
+class GemmOut(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("ld", ctypes.c_int64), ("col0", ctypes.c_int), ("col1", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
 class IndexRows(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
@@ -81,6 +86,7 @@ def _load():
             "csa_sparse_attention": (I, [PP, P, P, PE, P, P, P, P, P, P, ctypes.c_size_t, P]),
             "csa_decode_static_scratch": (I, [PP, P, P, PE, PI, PI, P, P, P, P, P, P, P, P]),
             "csa_launch_count": (ctypes.c_uint64, []),
+            "csa_gemm_bf16": (I, [P, I64, P, I64, I, I, I, I, ctypes.POINTER(GemmOut), I, P]),
             "csa_device_status": (I, [ctypes.POINTER(ctypes.c_int), I, P]),
             "csa_selftest_wait_timeout": (I, [ctypes.c_uint64, P]),
             "csa_probe_ffma": (I, [I, I, P, P]),
@@ -205,6 +211,18 @@ def csa_sparse_attention(p: Params, q, kv_rope, C, topk_idx, sink, rope_tab, out
                                      _ptr(sink), _ptr(rope_tab), _ptr(out), _ptr(lse_out), _ptr(ws), _nbytes(ws),
                                      _stream(stream)),
         "csa_sparse_attention")
+
+
+def csa_gemm_bf16(A: torch.Tensor, B: torch.Tensor, outs, groups: int = 1, stream=None):
+    """C = A B^T on the tensor cores (BF16 in, FP32 accumulate). A [M, groups*K], B [N, K] BF16;
+    outs: list of (tensor, col0, col1): columns [col0, col1) of C into that row-major tensor
+    (BF16 or FP32, rows of col1 - col0 values)."""
+    M, N, K = A.shape[0], B.shape[0], B.shape[1]
+    arr = (GemmOut * len(outs))()
+    for i, (t, c0, c1) in enumerate(outs):
+        arr[i] = GemmOut(_ptr(t), t.shape[-1], c0, c1, _DT["f32" if t.dtype == torch.float32 else "bf16"])
+    _ok(_load().csa_gemm_bf16(_ptr(A), A.stride(0), _ptr(B), B.stride(0), M, N, K, groups, arr, len(outs),
+                              _stream(stream)), "csa_gemm_bf16")
 
 
 def csa_launch_count() -> int:

@@ -493,6 +493,21 @@ int hca_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     return run_decode_attention(a, ws, cs(stream));
 }
 
+int csa_gemm_bf16(const void *A, int64_t lda, const void *B, int64_t ldb, int M, int N, int K, int groups,
+                  const csa_gemm_out *outs, int n_outs, csa_stream_t stream) {
+    if (!A || !B || !outs || n_outs < 1 || n_outs > 4 || !aligned16(A) || !aligned16(B)) return CSA_ERR_INVALID;
+    GemmArgs g{};
+    g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.M = M; g.N = N; g.K = K; g.groups = groups; g.n_out = n_outs;
+    for (int i = 0; i < n_outs; ++i) {
+        const csa_gemm_out &o = outs[i];
+        if (!o.ptr || o.col0 < 0 || o.col1 <= o.col0 || o.col1 > N || o.ld < o.col1 - o.col0) return CSA_ERR_INVALID;
+        if (o.dtype != CSA_F32 && o.dtype != CSA_BF16) return CSA_ERR_INVALID;
+        g.out[i] = o;
+    }
+    const int s = launch_gemm_bf16(g, cs(stream));
+    return s ? s : launch_status();
+}
+
 uint64_t csa_launch_count(void) { return launch_counter(); }
 
 int csa_device_status(int *status, int reset, csa_stream_t stream) {

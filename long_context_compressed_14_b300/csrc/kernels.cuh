@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/csa.h"
+
 namespace csa {
 
 struct CompressArgs {
@@ -112,6 +114,20 @@ struct AppendArgs {
     int B, L, m, ncap, n_win, d_rope, act_t, kv_t, idx_t;
 };
 void launch_kv_append(const AppendArgs &a, cudaStream_t st);
+
+// BF16 GEMM for the projections around the core (gemm.cu): C = A B^T, output columns split into
+// up to four segments (csa_gemm_out), optionally block-diagonal over `groups`.
+using GemmOut = csa_gemm_out;
+struct GemmArgs {
+    const void *A;
+    int64_t lda;
+    const void *B;
+    int64_t ldb;
+    int M, N, K, groups;
+    GemmOut out[4];
+    int n_out;
+};
+int launch_gemm_bf16(const GemmArgs &a, cudaStream_t st);  // returns a csa_status
 
 // host-side count of kernel launches (every launch_* adds the kernels it launched)
 void count_launches(int n);

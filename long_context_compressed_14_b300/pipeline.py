@@ -148,3 +148,52 @@ class DecodeLayer:
 def to_device(inp: dict, device="cuda", non_blocking=False) -> dict:
     return {k: (v.to(device, non_blocking=non_blocking) if isinstance(v, torch.Tensor) else v)
             for k, v in inp.items()}
+
+
+class Projections:
+    """The projections on either side of one attention layer, as library GEMM calls (plumbing:
+    buffers and the call sequence). inputs(): hidden states -> q, kv (BF16) and, for CSA, the
+    indexer queries, indexer key, weights and compression logits (FP32; HCA: the logits only),
+    each its own contiguous tensor. output(): the attention output -> the grouped output
+    projection -> the hidden size."""
+
+    def __init__(self, wl, csa: bool, weights: dict, device="cuda"):
+        self.wl, self.csa = wl, csa
+        self.W = {k: v.to(device) for k, v in weights.items() if k.startswith("W")}
+        # one stacked weight per product: q | kv (BF16 outputs), the indexer inputs (FP32)
+        self.W_bf16 = torch.cat([self.W["Wq"], self.W["Wkv"]]).contiguous()
+        self.device = device
+
+    def inputs(self, x: torch.Tensor, stream=None) -> dict:
+        from . import csa_gemm_bf16
+        wl, rows = self.wl, x.shape[0]
+        dev = self.device
+        q = torch.empty((rows, wl.H, wl.d), dtype=torch.bfloat16, device=dev)
+        kv = torch.empty((rows, wl.d), dtype=torch.bfloat16, device=dev)
+        nq = wl.H * wl.d
+        csa_gemm_bf16(x, self.W_bf16, [(q.view(rows, nq), 0, nq), (kv, nq, nq + wl.d)], stream=stream)
+        out = {"q": q, "kv": kv}
+        z = torch.empty((rows, 2), dtype=torch.float32, device=dev)
+        if self.csa:
+            ni = wl.H_I * wl.d_I
+            qI = torch.empty((rows, wl.H_I, wl.d_I), dtype=torch.float32, device=dev)
+            kI = torch.empty((rows, wl.d_I), dtype=torch.float32, device=dev)
+            w = torch.empty((rows, wl.H_I), dtype=torch.float32, device=dev)
+            segs = [(qI.view(rows, ni), 0, ni), (kI, ni, ni + wl.d_I), (w, ni + wl.d_I, ni + wl.d_I + wl.H_I),
+                    (z, ni + wl.d_I + wl.H_I, ni + wl.d_I + wl.H_I + 2)]
+            csa_gemm_bf16(x, self.W["Widx"], segs, stream=stream)
+            out.update(qI=qI, kI_raw=kI, w=w)
+        else:
+            csa_gemm_bf16(x, self.W["Widx"], [(z, 0, 2)], stream=stream)
+        out["z"] = z
+        return out
+
+    def output(self, o: torch.Tensor, stream=None) -> torch.Tensor:
+        """o [rows, H, d] BF16 -> [rows, hidden] BF16 through the grouped projection."""
+        from . import csa_gemm_bf16
+        wl, rows = self.wl, o.shape[0]
+        y = torch.empty((rows, wl.groups * wl.d_g), dtype=torch.bfloat16, device=self.device)
+        csa_gemm_bf16(o.view(rows, wl.H * wl.d), self.W["Wg"], [(y, 0, y.shape[1])], groups=wl.groups, stream=stream)
+        h = torch.empty((rows, wl.hidden), dtype=torch.bfloat16, device=self.device)
+        csa_gemm_bf16(y, self.W["Wo"], [(h, 0, wl.hidden)], stream=stream)
+        return h

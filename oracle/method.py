@@ -21,7 +21,7 @@ from . import (attention_rows, compress, decode_one, dequant_fp8, entry_pos, ind
                index_scores_f64, num_entries, quant_rows_fp8, rope, round_bf16_fast, topk)
 
 __all__ = ["store_rows", "kv_compress", "indexer_topk", "csa_rows", "hca_rows", "csa_decode",
-           "hca_decode"]
+           "hca_decode", "project", "grouped_output_projection"]
 
 
 def store_rows(x: np.ndarray, store: str, d_rope: int = 0):
@@ -126,3 +126,26 @@ def csa_decode(q, ctx, C, qI, KI, w, ring, sink, *, m, k, d_rope, theta, n_win, 
 def hca_decode(q, ctx, C, ring, sink, *, m, d_rope, theta, n_win, scale):
     o, ps = decode_one(q, ctx, C, None, 0, m, ring, d_rope, theta, n_win, sink, scale)
     return dict(o=o, psum=ps)
+
+
+def project(x, W):
+    """A projection of rows: x [rows, K] times W [N, K] transposed -> [rows, N], in double
+    (the hidden-state projections to the layer's inputs; [P2] 概要: hidden size 4096)."""
+    return np.asarray(x, np.float64) @ np.asarray(W, np.float64).T
+
+
+def grouped_output_projection(o, Wg, Wo, groups):
+    """The grouped output projection ([P2] 提案手法 §1 CSA; [P5] 一.1 分组输出投影). o [rows, H, d]:
+    the heads are split into `groups` consecutive groups; group g's heads, concatenated
+    ([rows, H/groups * d]), are projected by its own matrix Wg[g] ([d_g, H/groups * d]); the
+    group outputs, concatenated in group order ([rows, groups * d_g]), are projected by Wo
+    ([hidden, groups * d_g]). Wg is given stacked: [groups * d_g, H/groups * d]."""
+    o = np.asarray(o, np.float64)
+    rows, H, d = o.shape
+    hg = H // groups
+    dg = Wg.shape[0] // groups
+    y = np.empty((rows, groups * dg), np.float64)
+    for g in range(groups):
+        og = o[:, g * hg:(g + 1) * hg, :].reshape(rows, hg * d)
+        y[:, g * dg:(g + 1) * dg] = project(og, Wg[g * dg:(g + 1) * dg])
+    return y, project(y, Wo)

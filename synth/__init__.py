@@ -42,6 +42,9 @@ class Workload:
     topk: int = 512
     n_win: int = 128
     theta: float = 1.0e4
+    hidden: int = 4096   # hidden size the layer's inputs are projected from (V4-Flash width)
+    groups: int = 8      # output-projection head groups
+    d_g: int = 512       # output-projection width per group
     q_t: str = "bf16"    # activations: q, raw kv, outputs
     c_t: str = "bf16"    # compressed entries: 'f32' | 'bf16' | 'mixed'
     idx_t: str = "fp8"   # indexer operands: 'f32' | 'fp8'
@@ -188,3 +191,31 @@ def sample_rows(L: int, n: int, seed: int, first: int = 256, last: int = 128) ->
     g = torch.Generator("cpu").manual_seed(seed * 31 + 17)
     mid = torch.randperm(max(0, mid_hi - mid_lo), generator=g)[:k] + mid_lo
     return torch.unique(torch.cat([head, tail, mid])).to(torch.int64)
+
+
+T_X, T_WQ, T_WKV, T_WIDX, T_WG, T_WO = 11, 12, 13, 14, 15, 16  # projections (per layer, + LAYER_STRIDE)
+
+
+def projection_inputs(wl: Workload, layer: int = 0, csa: bool = True, rows: Optional[int] = None) -> dict:
+    """Hidden states and projection weights of one layer, BF16 (CPU tensors): x [rows, hidden];
+    Wq [H*d, hidden]; Wkv [d, hidden]; Widx [n_idx, hidden] with n_idx = H_I*d_I + d_I + H_I + 2
+    (CSA: the indexer queries, indexer key, weights and compression logits) or 2 (HCA: the
+    compression logits); Wg [groups*d_g, (H/groups)*d] (the groups' output matrices, stacked);
+    Wo [hidden, groups*d_g]. Weights are N(0, 1) / sqrt(fan_in), so every projection has unit
+    scale like the layer inputs drawn directly."""
+    base = layer * LAYER_STRIDE
+    rows = wl.B * wl.L if rows is None else rows
+    hd = wl.hidden
+    n_idx = (wl.H_I * wl.d_I + wl.d_I + wl.H_I + 2) if csa else 2
+    hg = wl.H // wl.groups
+
+    def w(no, shape, fan_in):
+        return (randn_rows(wl.seed, base + no, shape, "f32") * fan_in ** -0.5).to(torch.bfloat16)
+    return {
+        "x": randn_rows(wl.seed, base + T_X, (rows, hd), "bf16"),
+        "Wq": w(T_WQ, (wl.H * wl.d, hd), hd),
+        "Wkv": w(T_WKV, (wl.d, hd), hd),
+        "Widx": w(T_WIDX, (n_idx, hd), hd),
+        "Wg": w(T_WG, (wl.groups * wl.d_g, hg * wl.d), hg * wl.d),
+        "Wo": w(T_WO, (hd, wl.groups * wl.d_g), wl.groups * wl.d_g),
+    }

@@ -455,3 +455,33 @@ def test_mixed_storage_rows():
     np.testing.assert_array_equal(vals[:, 64:], oracle.round_bf16_fast(x[:, 64:].astype(np.float32)))
     np.testing.assert_array_equal(vals[:, :64], oracle.dequant_fp8(codes, scales))
     assert codes.shape == (50, 64) and scales.shape == (50,)
+
+
+# ---------------------------------------------------------------------------------------
+# Projections around the core
+# ---------------------------------------------------------------------------------------
+
+def test_projection_identity_and_block_diagonal_grouping():
+    # identity weights give the rows back; the grouped output projection equals one dense
+    # projection with the groups' matrices on the block diagonal (a group-to-columns slip, e.g.
+    # group g reading the heads of another group, breaks it)
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((5, 16))
+    np.testing.assert_allclose(oracle.project(x, np.eye(16)), x, rtol=0, atol=0)
+    rows, H, d, groups, dg, hidden = 6, 8, 4, 4, 3, 5
+    o = rng.standard_normal((rows, H, d))
+    Wg = rng.standard_normal((groups * dg, (H // groups) * d))
+    Wo = rng.standard_normal((hidden, groups * dg))
+    y, h = oracle.grouped_output_projection(o, Wg, Wo, groups)
+    dense = np.zeros((groups * dg, H * d))
+    hw = (H // groups) * d
+    for g in range(groups):
+        dense[g * dg:(g + 1) * dg, g * hw:(g + 1) * hw] = Wg[g * dg:(g + 1) * dg]
+    np.testing.assert_allclose(y, o.reshape(rows, H * d) @ dense.T, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(h, y @ Wo.T, rtol=1e-13, atol=1e-13)
+    # one head group alone: the other groups' columns of y are untouched by it
+    o2 = o.copy()
+    o2[:, : H // groups] += 1.0
+    y2, _ = oracle.grouped_output_projection(o2, Wg, Wo, groups)
+    np.testing.assert_allclose(y2[:, dg:], y[:, dg:], rtol=0, atol=0)
+    assert np.abs(y2[:, :dg] - y[:, :dg]).max() > 1e-3
