@@ -44,7 +44,8 @@ typedef enum {
     CSA_F32 = 0,     /* float32 */
     CSA_BF16 = 1,    /* bfloat16 */
     CSA_FP8E4M3 = 2, /* FP8 E4M3 ("fn": no infinities, max 448), with a float scale per row */
-    CSA_MIXED = 3    /* compressed entry: dims [0, d-d_rope) FP8 E4M3 + row scale, RoPE dims BF16 */
+    CSA_MIXED = 3,   /* compressed entry: dims [0, d-d_rope) FP8 E4M3 + row scale, RoPE dims BF16 */
+    CSA_MXFP4 = 4    /* indexer operand rows in MXFP4: E2M1 elements, one E8M0 exponent per 32 */
 } csa_dtype;
 
 typedef enum {
@@ -73,7 +74,7 @@ typedef struct {
     float scale;    /* softmax scale of the logits (1/sqrt(d)) */
     int act_t;      /* csa_dtype of q, raw kv, kv_rope, the SWA ring and the output: F32 | BF16 */
     int kv_t;       /* csa_dtype of compressed entries: F32 | BF16 | MIXED */
-    int idx_t;      /* csa_dtype of the indexer operands: F32 | FP8E4M3 */
+    int idx_t;      /* csa_dtype of the indexer operands: F32 | FP8E4M3 | MXFP4 */
     int rope_len;   /* rows of the RoPE table (positions 0 .. rope_len-1) */
 } csa_params;
 
@@ -90,10 +91,16 @@ typedef struct {
 
 /* Rows of indexer operands (queries [.., H_I, d_I] or keys [.., d_I]).
  *  F32     : data = float rows, scale = NULL.
- *  FP8E4M3 : data = uint8 E4M3 codes, scale = one float per row of d_I values. */
+ *  FP8E4M3 : data = uint8 E4M3 codes, scale = one float per row of d_I values.
+ *  MXFP4   : data = uint8 [.., d_I / 2] E2M1 codes (element 2i in the low nibble of byte i),
+ *            mx_scale = uint8 [.., d_I / 32] E8M0 exponents (one per block of 32 elements:
+ *            value = E2M1 * 2^(e8 - 127)); scale = NULL. ([P2] 事後学習 §3: the indexer's QK
+ *            path in FP4 (MXFP4); FP4 -> FP8 dequantisation is lossless, so the library runs
+ *            the FP8 indexer on the exact FP8 form of these rows.) */
 typedef struct {
     void *data;
     float *scale;
+    uint8_t *mx_scale;
 } csa_index_rows;
 
 /* Operation selector for csa_workspace_bytes. */
@@ -131,6 +138,14 @@ int csa_rope_table(float *tab, int rope_len, int d_rope, float theta, csa_stream
  * scale 0 and zero codes. codes [rows, cols] uint8; scales [rows] float. */
 int csa_quant_fp8_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
                        csa_stream_t stream);
+
+/* Per-row MXFP4 quantisation of x [rows, 64] float (the indexer's FP4 operands, [P2] 事後学習
+ * §3): per block of 32 values, e = floor(log2(max |x|)) - 2 clamped to [-127, 127] (a block of
+ * zeros: e = -127), E8M0 byte e + 127, codes = E2M1(x / 2^e) rounded to nearest even and
+ * saturated at 6. codes [rows, 32] uint8 (two elements per byte, the even one in the low
+ * nibble); e8 [rows, 2] uint8. cols must be 64. */
+int csa_quant_mxfp4_rows(const float *x, int64_t rows, int cols, uint8_t *codes, uint8_t *e8,
+                         csa_stream_t stream);
 
 /* Overlapping compression, one layer ([P2] 提案手法 §1 CSA/HCA: one entry per m tokens by a
  * weighted average with overlap between adjacent blocks; [P5] 一.1: C^b overlaps C^a).

@@ -21,13 +21,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcsa.so")
 
 # csa_dtype
-F32, BF16, FP8E4M3, MIXED = 0, 1, 2, 3
+F32, BF16, FP8E4M3, MIXED, MXFP4 = 0, 1, 2, 3, 4
 # csa_op
 OP_INDEX_TOPK, OP_CSA_PREFILL, OP_HCA_PREFILL, OP_CSA_DECODE, OP_HCA_DECODE, OP_SPARSE_ATTENTION = range(6)
 # csa_status
 OK, ERR_INVALID, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_TIMEOUT, ERR_BOUNDS, ERR_CUDA = range(8)
 
-_DT = {"f32": F32, "bf16": BF16, "fp8": FP8E4M3, "mixed": MIXED}
+_DT = {"f32": F32, "bf16": BF16, "fp8": FP8E4M3, "mixed": MIXED, "mxfp4": MXFP4}
 
 
 class CsaError(RuntimeError):
@@ -52,7 +52,7 @@ class GemmOut(ctypes.Structure):
 
 
 class IndexRows(ctypes.Structure):
-    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("mx_scale", ctypes.c_void_p)]
 
 
 _lib = None
@@ -76,6 +76,7 @@ def _load():
             "csa_check_params": (I, [PP, I]),
             "csa_rope_table": (I, [P, I, I, ctypes.c_float, P]),
             "csa_quant_fp8_rows": (I, [P, I64, I, P, P, P]),
+            "csa_quant_mxfp4_rows": (I, [P, I64, I, P, P, P]),
             "kv_compress": (I, [PP, P, P, P, P, PE, PI, P, P]),
             "kv_append": (I, [PP, P, P, P, P, P, P, P, P, P, PE, PI, P]),
             "csa_index_topk": (I, [PP, PI, PI, P, P, P, Z, P]),
@@ -137,8 +138,8 @@ def _entries(C: Optional[Sequence]) -> Optional[Entries]:
 def _rows(R: Optional[Sequence]) -> Optional[IndexRows]:
     if R is None:
         return None
-    data, scale = (list(R) + [None, None])[:2]
-    return IndexRows(_ptr(data), _ptr(scale))
+    data, scale, mx = (list(R) + [None, None, None])[:3]
+    return IndexRows(_ptr(data), _ptr(scale), _ptr(mx))
 
 
 def _byref(x):
@@ -176,6 +177,12 @@ def csa_quant_fp8_rows(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tenso
     rows = x.numel() // x.shape[-1]
     _ok(_load().csa_quant_fp8_rows(_ptr(x), rows, x.shape[-1], _ptr(codes), _ptr(scales), _stream(stream)),
         "csa_quant_fp8_rows")
+
+
+def csa_quant_mxfp4_rows(x: torch.Tensor, codes: torch.Tensor, e8: torch.Tensor, stream=None):
+    rows = x.numel() // x.shape[-1]
+    _ok(_load().csa_quant_mxfp4_rows(_ptr(x), rows, x.shape[-1], _ptr(codes), _ptr(e8), _stream(stream)),
+        "csa_quant_mxfp4_rows")
 
 
 def kv_compress(p: Params, kv, z, kI_raw, rope_tab, C, KI, kv_rope, stream=None):
@@ -313,7 +320,11 @@ def alloc_entries(p: Params, device="cuda"):
 
 
 def alloc_index_rows(p: Params, rows_shape, device="cuda"):
-    """Indexer operand buffers (data, scale) of shape rows_shape + [d_I] per p.idx_t."""
+    """Indexer operand buffers of shape rows_shape + [d_I] per p.idx_t: (data, scale) for F32 /
+    FP8, (codes [.., d_I/2], None, E8M0 exponents [.., d_I/32]) for MXFP4."""
+    if p.idx_t == MXFP4:
+        return (torch.empty(tuple(rows_shape) + (p.d_I // 2,), dtype=torch.uint8, device=device), None,
+                torch.empty(tuple(rows_shape) + (p.d_I // 32,), dtype=torch.uint8, device=device))
     if p.idx_t == FP8E4M3:
         return (torch.empty(tuple(rows_shape) + (p.d_I,), dtype=torch.uint8, device=device),
                 torch.empty(tuple(rows_shape), dtype=torch.float32, device=device))

@@ -70,7 +70,7 @@ int check(const csa_params *p, int op) {
         if (p->topk > 0) {
             if (p->d_I != kDI) return CSA_ERR_UNSUPPORTED;
             if (p->H_I < 1 || p->H_I > 16) return CSA_ERR_UNSUPPORTED;
-            if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3) return CSA_ERR_INVALID;
+            if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3 && p->idx_t != CSA_MXFP4) return CSA_ERR_INVALID;
         }
     }
     return CSA_OK;
@@ -81,9 +81,17 @@ size_t widen_bytes(const csa_params *p) {
     return p->kv_t == CSA_MIXED ? align_up((size_t)p->B * (size_t)ncap_of(p) * kD * 2) : 0;
 }
 
+// Bytes of the exact FP8 form of `rows` MXFP4 indexer rows (codes + one float scale per row).
+size_t fp8_rows_bytes(int64_t rows) {
+    return align_up((size_t)rows * kDI) + align_up((size_t)rows * sizeof(float));
+}
+
 // Workspace of the prefill indexer + top-k: the FP8 path keeps per-row candidate lists (the
 // fused selection), the exact FP32 path a chunk of full score rows.
 size_t index_ws_bytes(const csa_params *p) {
+    if (p->idx_t == CSA_MXFP4)  // the FP8 form of the query and key rows, then the FP8 path's
+        return fp8_rows_bytes((int64_t)p->B * p->L * p->H_I) + fp8_rows_bytes((int64_t)p->B * ncap_of(p)) +
+               align_up(isel_workspace_bytes(p->L, (int)ncap_of(p)));
     if (p->idx_t == CSA_FP8E4M3) return align_up(isel_workspace_bytes(p->L, (int)ncap_of(p)));
     return align_up(sizeof(float) * (size_t)score_chunk_rows(p) * (size_t)score_ld(p));
 }
@@ -108,7 +116,10 @@ size_t ws_bytes(const csa_params *p, int op) {
     case CSA_OP_HCA_PREFILL:
         return widen_bytes(p);
     case CSA_OP_CSA_DECODE:
-        return (p->topk == 0 ? 0
+        return (p->topk > 0 && p->idx_t == CSA_MXFP4
+                    ? fp8_rows_bytes((int64_t)p->B * p->H_I) + fp8_rows_bytes((int64_t)p->B * ncap_of(p))
+                    : 0) +
+               (p->topk == 0 ? 0
                              : align_up(sizeof(float) * (size_t)p->B * (size_t)score_ld(p)) +
                                    align_up(sizeof(int32_t) * (size_t)p->B * p->topk) +
                                    align_up(sizeof(uint32_t) * (size_t)p->B * 2048) +
@@ -137,7 +148,19 @@ bool entries_ok(const csa_params *p, const csa_entries *C) {
 bool index_rows_ok(const csa_params *p, const csa_index_rows *r) {
     if (!r || !r->data || !aligned16(r->data)) return false;
     if (p->idx_t == CSA_FP8E4M3) return r->scale && aligned16(r->scale);
+    if (p->idx_t == CSA_MXFP4) return r->mx_scale != nullptr;
     return true;
+}
+
+// MXFP4 rows converted to their exact FP8 form in workspace at `ws`; the FP8 rows are returned
+// in `out` (data = codes, scale = row scales).
+void mxfp4_rows_to_fp8(const csa_index_rows *in, int64_t rows, void *ws, csa_index_rows *out, cudaStream_t st) {
+    uint8_t *codes = reinterpret_cast<uint8_t *>(ws);
+    float *scales = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + align_up((size_t)rows * kDI));
+    launch_mxfp4_to_fp8(reinterpret_cast<const uint8_t *>(in->data), in->mx_scale, rows, codes, scales, st);
+    out->data = codes;
+    out->scale = scales;
+    out->mx_scale = nullptr;
 }
 
 // indexer + top-k over all prefill rows: FP8 through the fused selection, FP32 (exact, the
@@ -145,6 +168,18 @@ bool index_rows_ok(const csa_params *p, const csa_index_rows *r) {
 int run_index_topk(const csa_params *p, const csa_index_rows *qI, const csa_index_rows *KI,
                    const float *w, int32_t *idx_out, float *S, cudaStream_t st) {
     const int ncap = (int)ncap_of(p);
+    if (p->idx_t == CSA_MXFP4) {
+        // the exact FP8 form of the FP4 rows, then the FP8 path
+        const int64_t qrows = (int64_t)p->B * p->L * p->H_I, krows = (int64_t)p->B * ncap;
+        char *w8 = reinterpret_cast<char *>(S);
+        csa_index_rows q8{}, k8{};
+        mxfp4_rows_to_fp8(qI, qrows, w8, &q8, st);
+        mxfp4_rows_to_fp8(KI, krows, w8 + fp8_rows_bytes(qrows), &k8, st);
+        csa_params p8 = *p;
+        p8.idx_t = CSA_FP8E4M3;
+        return run_index_topk(&p8, &q8, &k8, w, idx_out,
+                              reinterpret_cast<float *>(w8 + fp8_rows_bytes(qrows) + fp8_rows_bytes(krows)), st);
+    }
     if (p->idx_t == CSA_FP8E4M3) {
         IselArgs ia{};
         ia.qI = qI->data; ia.qI_scale = qI->scale; ia.KI = KI->data; ia.KI_scale = KI->scale; ia.w = w;
@@ -276,6 +311,13 @@ int csa_rope_table(float *tab, int rope_len, int d_rope, float theta, csa_stream
     return launch_status();
 }
 
+int csa_quant_mxfp4_rows(const float *x, int64_t rows, int cols, uint8_t *codes, uint8_t *e8,
+                         csa_stream_t stream) {
+    if (!x || !codes || !e8 || rows < 0 || cols != kDI) return CSA_ERR_INVALID;
+    launch_quant_mxfp4(x, rows, codes, e8, cs(stream));
+    return launch_status();
+}
+
 int csa_quant_fp8_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
                        csa_stream_t stream) {
     if (!x || !codes || !scales || rows < 0 || cols < 1) return CSA_ERR_INVALID;
@@ -292,7 +334,7 @@ int kv_compress(const csa_params *p, const void *kv, const float *z, const float
     if (!kv || !z || !aligned16(kv) || !entries_ok(p, C)) return CSA_ERR_INVALID;
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
     if (kI_raw) {
-        if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3) return CSA_ERR_INVALID;
+        if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3 && p->idx_t != CSA_MXFP4) return CSA_ERR_INVALID;
         if (!index_rows_ok(p, KI) || p->d_I != kDI) return CSA_ERR_INVALID;
     }
     if (kv_rope && !aligned16(kv_rope)) return CSA_ERR_INVALID;
@@ -301,6 +343,7 @@ int kv_compress(const csa_params *p, const void *kv, const float *z, const float
     a.c_data = C->data; a.c_rope = C->rope; a.c_scale = C->scale;
     a.ki_data = kI_raw ? KI->data : nullptr;
     a.ki_scale = kI_raw ? KI->scale : nullptr;
+    a.ki_e8 = kI_raw ? KI->mx_scale : nullptr;
     a.kv_rope = kv_rope;
     a.B = p->B; a.L = p->L; a.m = p->m; a.N = (int)ncap_of(p); a.d_rope = p->d_rope;
     a.act_t = p->act_t; a.kv_t = p->kv_t; a.idx_t = p->idx_t;
@@ -318,13 +361,14 @@ int kv_append(const csa_params *p, const void *kv_new, const float *z_new, const
     if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
     if (kI_new) {
         if (!state_kI || p->d_I != kDI || !index_rows_ok(p, KI)) return CSA_ERR_INVALID;
-        if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3) return CSA_ERR_INVALID;
+        if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3 && p->idx_t != CSA_MXFP4) return CSA_ERR_INVALID;
     }
     AppendArgs a{};
     a.kv_new = kv_new; a.z_new = z_new; a.kI_new = kI_new; a.ctx = ctx_len; a.rope_tab = rope_tab;
     a.ring = ring; a.state_kv = state_kv; a.state_z = state_z; a.state_kI = state_kI;
     a.c_data = C->data; a.c_rope = reinterpret_cast<__nv_bfloat16 *>(C->rope); a.c_scale = C->scale;
     a.ki_data = kI_new ? KI->data : nullptr; a.ki_scale = kI_new ? KI->scale : nullptr;
+    a.ki_e8 = kI_new ? KI->mx_scale : nullptr;
     a.B = p->B; a.L = p->L; a.m = p->m; a.ncap = (int)ncap_of(p); a.n_win = p->n_win; a.d_rope = p->d_rope;
     a.act_t = p->act_t; a.kv_t = p->kv_t; a.idx_t = p->idx_t;
     launch_kv_append(a, cs(stream));
@@ -434,13 +478,23 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     // selection lists: the two counters per row right after the histogram (one memset clears both)
     int *sel_cnt = p->topk > 0 ? reinterpret_cast<int *>(wsc + sbytes + ibytes + hbytes) : nullptr;
     void *part = need > 0 ? wsc + sbytes + ibytes + hbytes + dbytes : nullptr;
+    // MXFP4 indexer operands: their exact FP8 form after the split-KV partials
+    csa_index_rows q8{}, k8{};
+    if (p->topk > 0 && p->idx_t == CSA_MXFP4) {
+        char *w8 = wsc + sbytes + ibytes + hbytes + dbytes + decode_split_bytes(p, 0);
+        mxfp4_rows_to_fp8(qI, (int64_t)p->B * p->H_I, w8, &q8, st);
+        mxfp4_rows_to_fp8(KI, (int64_t)p->B * ncap, w8 + fp8_rows_bytes((int64_t)p->B * p->H_I), &k8, st);
+        qI = &q8;
+        KI = &k8;
+    }
+    const int idx_t_eff = p->idx_t == CSA_MXFP4 ? (int)CSA_FP8E4M3 : p->idx_t;
     if (p->topk > 0) {
         float *S = reinterpret_cast<float *>(ws);
         idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
         IndexArgs ia{};
         ia.qI = qI->data; ia.qI_scale = qI->scale; ia.KI = KI->data; ia.KI_scale = KI->scale;
         ia.w = w; ia.ctx = ctx_len; ia.S = S; ia.ldS = score_ld(p);
-        ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap; ia.idx_t = p->idx_t;
+        ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap; ia.idx_t = idx_t_eff;
         ia.decode = 1;
         // FP8 keys: the tensor-core scan, which also counts each row's keys for the top-k; the
         // exact FP32 scan (and batches of fewer than 16 query rows) on CUDA cores

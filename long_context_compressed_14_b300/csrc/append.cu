@@ -20,6 +20,7 @@
 //                       with scale = amax / 448).
 // Entries of incomplete blocks are not written: no decode query can see them.
 #include "common.cuh"
+#include "fp4.cuh"
 #include "kernels.cuh"
 
 namespace csa {
@@ -125,6 +126,14 @@ __global__ void __launch_bounds__(128) kv_append_kernel(AppendArgs a) {
     if (a.kI_new) {
         if (IDX_T == CSA_F32) {
             if (d < kDI) reinterpret_cast<float *>(a.ki_data)[row * kDI + d] = ck;
+        } else if (IDX_T == CSA_MXFP4) {
+            // warp 0 holds dims 0..31, warp 1 dims 32..63: gather the row into warp 0
+            __syncthreads();
+            s_x[d] = ck;
+            __syncthreads();
+            if (warp == 0)
+                mxfp4_row_store(s_x[lane], s_x[32 + lane], reinterpret_cast<uint8_t *>(a.ki_data) + row * (kDI / 2),
+                                a.ki_e8 + row * 2);
         } else {
             const float am = warp_max(d < kDI ? fabsf(ck) : 0.0f);
             if (lane == 0) s_red[warp] = am;
@@ -139,14 +148,18 @@ __global__ void __launch_bounds__(128) kv_append_kernel(AppendArgs a) {
     }
 }
 
+template <typename ActT, int KV_T>
+static void launch_append_k(const AppendArgs &a, cudaStream_t st) {
+    if (a.idx_t == CSA_FP8E4M3) kv_append_kernel<ActT, KV_T, CSA_FP8E4M3><<<a.B, 128, 0, st>>>(a);
+    else if (a.idx_t == CSA_MXFP4) kv_append_kernel<ActT, KV_T, CSA_MXFP4><<<a.B, 128, 0, st>>>(a);
+    else kv_append_kernel<ActT, KV_T, CSA_F32><<<a.B, 128, 0, st>>>(a);
+}
+
 template <typename ActT>
 static void launch_append_a(const AppendArgs &a, cudaStream_t st) {
-    const bool fp8 = a.idx_t == CSA_FP8E4M3;
-#define CSA_APPEND(KV, IX) kv_append_kernel<ActT, KV, IX><<<a.B, 128, 0, st>>>(a)
-    if (a.kv_t == CSA_F32) { if (fp8) CSA_APPEND(CSA_F32, CSA_FP8E4M3); else CSA_APPEND(CSA_F32, CSA_F32); }
-    else if (a.kv_t == CSA_BF16) { if (fp8) CSA_APPEND(CSA_BF16, CSA_FP8E4M3); else CSA_APPEND(CSA_BF16, CSA_F32); }
-    else { if (fp8) CSA_APPEND(CSA_MIXED, CSA_FP8E4M3); else CSA_APPEND(CSA_MIXED, CSA_F32); }
-#undef CSA_APPEND
+    if (a.kv_t == CSA_F32) launch_append_k<ActT, CSA_F32>(a, st);
+    else if (a.kv_t == CSA_BF16) launch_append_k<ActT, CSA_BF16>(a, st);
+    else launch_append_k<ActT, CSA_MIXED>(a, st);
 }
 
 void launch_kv_append(const AppendArgs &a, cudaStream_t st) {

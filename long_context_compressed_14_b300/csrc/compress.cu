@@ -6,6 +6,7 @@
 // 訓練インフラの革新 §5 (KV entries: RoPE dims BF16, other dims FP8); [P5] "deepseek V4
 // 技术论文" 一.1 (C^b overlaps C^a).
 #include "common.cuh"
+#include "fp4.cuh"
 #include "kernels.cuh"
 
 namespace csa {
@@ -81,8 +82,8 @@ kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
                    const float *__restrict__ kI_raw, const float2 *__restrict__ rope,
                    void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
                    float *__restrict__ c_scale, void *__restrict__ ki_data,
-                   float *__restrict__ ki_scale, ActT *__restrict__ kv_rope, int L, int m, int N,
-                   int d_rope) {
+                   float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope, int L,
+                   int m, int N, int d_rope) {
     __shared__ float s_w[kMaxWindow];
     __shared__ float s_red[4][kD + kDI];
     __shared__ float s_scalar[8];
@@ -200,6 +201,8 @@ kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
             float *dst = reinterpret_cast<float *>(ki_data) + row * kDI;
             dst[lane] = k0;
             dst[lane + 32] = k1;
+        } else if (IDX_T == CSA_MXFP4) {
+            mxfp4_row_store(k0, k1, reinterpret_cast<uint8_t *>(ki_data) + row * (kDI / 2), ki_e8 + row * 2);
         } else {
             const float amax = warp_max(fmaxf(fabsf(k0), fabsf(k1)));
             const float scale = __fdiv_rn(amax, 448.0f);
@@ -220,7 +223,7 @@ static void launch_compress_t(const CompressArgs &a, cudaStream_t st) {
     auto *cr = reinterpret_cast<__nv_bfloat16 *>(a.c_rope);
 #define CSA_LAUNCH(KI, KVR)                                                                          \
     kv_compress_kernel<ActT, KV_T, IDX_T, KI, KVR><<<grid, 128, 0, st>>>(                            \
-        kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, kvr, a.L, a.m, a.N, \
+        kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, \
         a.d_rope)
     if (a.kI_raw && a.kv_rope) CSA_LAUNCH(true, true);
     else if (a.kI_raw) CSA_LAUNCH(true, false);
@@ -229,12 +232,18 @@ static void launch_compress_t(const CompressArgs &a, cudaStream_t st) {
 #undef CSA_LAUNCH
 }
 
+template <typename ActT, int KV_T>
+static void launch_compress_k(const CompressArgs &a, cudaStream_t st) {
+    if (a.idx_t == CSA_FP8E4M3) launch_compress_t<ActT, KV_T, CSA_FP8E4M3>(a, st);
+    else if (a.idx_t == CSA_MXFP4) launch_compress_t<ActT, KV_T, CSA_MXFP4>(a, st);
+    else launch_compress_t<ActT, KV_T, CSA_F32>(a, st);
+}
+
 template <typename ActT>
 static void launch_compress_a(const CompressArgs &a, cudaStream_t st) {
-    const bool fp8 = a.idx_t == CSA_FP8E4M3;
-    if (a.kv_t == CSA_F32) fp8 ? launch_compress_t<ActT, CSA_F32, CSA_FP8E4M3>(a, st) : launch_compress_t<ActT, CSA_F32, CSA_F32>(a, st);
-    else if (a.kv_t == CSA_BF16) fp8 ? launch_compress_t<ActT, CSA_BF16, CSA_FP8E4M3>(a, st) : launch_compress_t<ActT, CSA_BF16, CSA_F32>(a, st);
-    else fp8 ? launch_compress_t<ActT, CSA_MIXED, CSA_FP8E4M3>(a, st) : launch_compress_t<ActT, CSA_MIXED, CSA_F32>(a, st);
+    if (a.kv_t == CSA_F32) launch_compress_k<ActT, CSA_F32>(a, st);
+    else if (a.kv_t == CSA_BF16) launch_compress_k<ActT, CSA_BF16>(a, st);
+    else launch_compress_k<ActT, CSA_MIXED>(a, st);
 }
 
 void launch_kv_compress(const CompressArgs &a, cudaStream_t st) {

@@ -19,6 +19,7 @@ struct CompressArgs {
     float *c_scale;
     void *ki_data;
     float *ki_scale;
+    uint8_t *ki_e8;        // MXFP4 keys: E8M0 exponents [B, N, 2]
     void *kv_rope;
     int B, L, m, N, d_rope, act_t, kv_t, idx_t;
 };
@@ -111,6 +112,7 @@ struct AppendArgs {
     float *c_scale;
     void *ki_data;
     float *ki_scale;
+    uint8_t *ki_e8;
     int B, L, m, ncap, n_win, d_rope, act_t, kv_t, idx_t;
 };
 void launch_kv_append(const AppendArgs &a, cudaStream_t st);
@@ -140,6 +142,10 @@ void launch_wait_selftest(uint64_t limit_ns, cudaStream_t st);
 void launch_rope_table(float *tab, int rope_len, int d_rope, float theta, cudaStream_t st);
 void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
                        cudaStream_t st);
+// MXFP4 rows of 64 values (fp4.cu): quantisation, and the exact FP8 form (codes + row scale)
+void launch_quant_mxfp4(const float *x, int64_t rows, uint8_t *codes, uint8_t *e8, cudaStream_t st);
+void launch_mxfp4_to_fp8(const uint8_t *codes, const uint8_t *e8, int64_t rows, uint8_t *out, float *out_scale,
+                         cudaStream_t st);
 void launch_kv_compress(const CompressArgs &a, cudaStream_t st);
 void launch_indexer(const IndexArgs &a, cudaStream_t st);
 void launch_topk(const TopkArgs &a, cudaStream_t st);

@@ -14,10 +14,23 @@ from typing import Optional
 
 import torch
 
-from . import (FP8E4M3, MIXED, OP_CSA_DECODE, OP_CSA_PREFILL, OP_HCA_DECODE, OP_HCA_PREFILL, Params,
+from . import (FP8E4M3, MIXED, MXFP4, OP_CSA_DECODE, OP_CSA_PREFILL, OP_HCA_DECODE, OP_HCA_PREFILL, Params,
                alloc_entries, alloc_index_rows, alloc_workspace, csa_decode, csa_prefill,
-               csa_quant_fp8_rows, hca_decode, hca_prefill, kv_compress, make_params, rope_table,
+               csa_quant_fp8_rows, csa_quant_mxfp4_rows, hca_decode, hca_prefill, kv_compress, make_params,
+               rope_table,
                torch_dtype)
+
+
+def quantise_index_rows(p: Params, x: torch.Tensor, buf, stream=None):
+    """Indexer operand rows in the layer's format: FP8 or MXFP4 codes written into buf by the
+    library's quantisers, float rows as they are."""
+    if p.idx_t == FP8E4M3:
+        csa_quant_fp8_rows(x, buf[0], buf[1], stream)
+        return buf
+    if p.idx_t == MXFP4:
+        csa_quant_mxfp4_rows(x, buf[0], buf[2], stream)
+        return buf
+    return (x, None)
 
 
 def layer_params(wl, csa: bool) -> Params:
@@ -61,11 +74,7 @@ class PrefillLayer:
         p = self.p
         lse = self.lse if want_lse else None
         if self.csa and p.topk > 0:
-            if p.idx_t == FP8E4M3:
-                csa_quant_fp8_rows(inp["qI"], self.qI[0], self.qI[1], stream)
-                qI = self.qI
-            else:
-                qI = (inp["qI"], None)
+            qI = quantise_index_rows(p, inp["qI"], self.qI, stream)
             kv_compress(p, inp["kv"], inp["z"], inp["kI_raw"], self.rope, self.C, self.KI, self.kv_rope, stream)
             csa_prefill(p, inp["q"], self.kv_rope, self.C, qI, self.KI, inp["w"], inp.get("sink"), self.rope,
                         self.topk if want_topk else None, self.out, lse, self.ws, stream)
@@ -119,10 +128,7 @@ class DecodeLayer:
             csa_quant_fp8_rows(C[..., :nope].float().contiguous(), codes, scales, stream)
             self.C = (codes, C[..., nope:].to(torch.bfloat16).contiguous(), scales)
         if self.csa:
-            if self.p.idx_t == FP8E4M3:
-                csa_quant_fp8_rows(inp["KI"], self.KI[0], self.KI[1], stream)
-            else:
-                self.KI = (inp["KI"], None)
+            self.KI = quantise_index_rows(self.p, inp["KI"], self.KI, stream)
 
     def run(self, inp: dict, stream=None, want_lse: bool = False, want_topk: bool = True) -> torch.Tensor:
         p = self.p
@@ -132,11 +138,7 @@ class DecodeLayer:
         else:
             C = inp["C"] if isinstance(inp["C"], (tuple, list)) else (inp["C"], None, None)
         if self.csa:
-            if p.idx_t == FP8E4M3:
-                csa_quant_fp8_rows(inp["qI"], self.qI[0], self.qI[1], stream)
-                qI = self.qI
-            else:
-                qI = (inp["qI"], None)
+            qI = quantise_index_rows(p, inp["qI"], self.qI, stream)
             csa_decode(p, inp["q"], inp["ctx"], C, qI, self.KI, inp["w"], inp["ring"], inp.get("sink"), self.rope,
                        self.topk if want_topk else None, self.out, lse, self.ws, stream)
         else:

@@ -60,6 +60,9 @@ def _load():
             "orc_fp8_decode": (ctypes.c_float, [ctypes.c_uint8]),
             "orc_fp8_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "orc_quant_rows_fp8": (None, [_P, _I64, _INT, _P, _P]),
+            "orc_e2m1_decode": (_DBL, [ctypes.c_uint8]),
+            "orc_e2m1_encode": (ctypes.c_uint8, [_DBL]),
+            "orc_quant_rows_mxfp4": (None, [_P, _I64, _INT, _P, _P]),
             "orc_index_scores_f32": (None, [_P, _P, _P, _I64, _INT, _INT, _INT, _P, _I64, _P]),
             "orc_index_scores_f64": (None, [_P, _P, _P, _I64, _INT, _INT, _INT, _P, _I64, _P]),
             "orc_topk": (None, [_P, _I64, _INT, _P, _I64, _INT, _P]),
@@ -172,6 +175,40 @@ def quant_rows_fp8(x: np.ndarray):
     scales = np.zeros(x2.shape[0], dtype=np.float32)
     _load().orc_quant_rows_fp8(_ptr(x2), x2.shape[0], x2.shape[1], _ptr(codes), _ptr(scales))
     return codes.reshape(shp), scales.reshape(shp[:-1])
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    lib = _load()
+    table = np.array([lib.orc_e2m1_decode(c) for c in range(16)], dtype=np.float64)
+    return table[_c(codes, np.uint8) & 15]
+
+
+def e2m1_encode(x: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = _c(x, np.float64).reshape(-1)
+    return np.array([lib.orc_e2m1_encode(float(v)) for v in flat], dtype=np.uint8).reshape(np.shape(x))
+
+
+def quant_rows_mxfp4(x: np.ndarray):
+    """Per-row MXFP4 quantisation -> (codes uint8 [rows, cols/2] (element 2i in the low nibble),
+    block exponents uint8 [rows, cols/32] (E8M0))."""
+    x = _c(x, np.float32)
+    shp = x.shape
+    x2 = x.reshape(-1, shp[-1])
+    codes = np.zeros((x2.shape[0], shp[-1] // 2), dtype=np.uint8)
+    e8 = np.zeros((x2.shape[0], shp[-1] // 32), dtype=np.uint8)
+    _load().orc_quant_rows_mxfp4(_ptr(x2), x2.shape[0], x2.shape[1], _ptr(codes), _ptr(e8))
+    return codes.reshape(shp[:-1] + (shp[-1] // 2,)), e8.reshape(shp[:-1] + (shp[-1] // 32,))
+
+
+def dequant_mxfp4(codes: np.ndarray, e8: np.ndarray) -> np.ndarray:
+    """Values of MXFP4 rows: E2M1 element times 2^(e8 - 127) of its 32-element block."""
+    codes = np.asarray(codes, np.uint8)
+    elems = np.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), dtype=np.uint8)
+    elems[..., 0::2] = codes & 15
+    elems[..., 1::2] = codes >> 4
+    scale = np.exp2(np.asarray(e8, np.float64) - 127.0)
+    return e2m1_decode(elems) * np.repeat(scale, 32, axis=-1)
 
 
 def dequant_fp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:

@@ -20,6 +20,7 @@
  *   - orc_index_scores_f32: the FP32 lightning-indexer score in a fixed single-precision
  *     fma order, so a top-k decision can be compared bit for bit with the GPU;
  *   - the FP8 E4M3 codec and the per-row scale, which are defined on float values;
+ *   - the FP4 (E2M1 / MXFP4) codec, whose encoder takes its input in double;
  *   - orc_round_bf16, the storage rounding of a float to bfloat16.
  * Build with -ffp-contract=off so that the compiler adds no fused operations of its own.
  */
@@ -175,6 +176,72 @@ void orc_quant_rows_fp8(const float *x, int64_t rows, int cols, uint8_t *codes, 
         scales[r] = scale;
         for (int c = 0; c < cols; ++c) {
             codes[r * cols + c] = (scale > 0.0f) ? orc_fp8_encode(row[c] / scale) : 0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* FP4: E2M1 elements and the MXFP4 block format.                                        */
+/* [P2] 事後学習 §3: the CSA indexer's QK path is quantised to FP4 (MXFP4); dequantising  */
+/* FP4 to FP8 is lossless, so the FP8 stack is reused. [P3] (V4.1): the KV cache is       */
+/* stored in NVFP4, quantised after RoPE.                                                 */
+/* E2M1 (OCP microscaling formats): 1 sign bit, 2 exponent bits with bias 1, 1 mantissa  */
+/* bit, no infinities or NaN. Codes 0..7 are the magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6;  */
+/* bit 3 is the sign. Encoding rounds to nearest, ties to the even code, and saturates   */
+/* at 6. MXFP4: blocks of 32 elements share a power-of-two scale X = 2^e stored as an    */
+/* E8M0 byte (e + 127); e = floor(log2(max |v|)) - 2 (2 = the exponent of E2M1's largest */
+/* value), elements = E2M1(v / X). Reading: a block of zeros gets the byte 0 (X = 2^-127) */
+/* and zero codes.                                                                        */
+/* ------------------------------------------------------------------------------------ */
+
+double orc_e2m1_decode(uint8_t code)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    const double v = mag[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+uint8_t orc_e2m1_encode(double x)
+{
+    const uint8_t sgn = signbit(x) ? 8 : 0;
+    const double a = fabs(x);
+    if (a >= 6.0) return sgn | 7;
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c < 8; ++c) {
+        const double err = fabs(orc_e2m1_decode((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sgn | (uint8_t)best;
+}
+
+/* Per-row MXFP4 quantisation of x [rows, cols] (cols a multiple of 32): codes [rows,     */
+/* cols/2] with element 2i in the low nibble of byte i and element 2i+1 in the high one, */
+/* and one E8M0 byte per block [rows, cols/32]. Dequantised value = E2M1 * 2^(byte-127). */
+void orc_quant_rows_mxfp4(const float *x, int64_t rows, int cols, uint8_t *codes, uint8_t *e8)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int blk = 0; blk < cols / 32; ++blk) {
+            const float *v = x + r * cols + blk * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs((double)v[i]));
+            int e = -127;
+            if (amax > 0.0) {
+                int ex;
+                frexp(amax, &ex);  /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+                e = ex - 1 - 2;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            e8[r * (cols / 32) + blk] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i) {
+                const uint8_t q = amax > 0.0 ? orc_e2m1_encode(ldexp((double)v[i], -e)) : 0;
+                uint8_t *byte = codes + r * (cols / 2) + blk * 16 + i / 2;
+                if (i % 2 == 0) *byte = q; else *byte |= (uint8_t)(q << 4);
+            }
         }
     }
 }

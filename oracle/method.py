@@ -8,8 +8,9 @@ stored, because they are approximations the result depends on:
   * compressed entries ("c_store"): 'f32', 'bf16', or 'mixed' -- [P2] 訓練インフラの革新 §5:
     a KV entry keeps its RoPE dimensions in BF16 and its other dimensions in FP8 (reading:
     E4M3 with one float scale per entry row, amax/448);
-  * indexer operands ("idx_store"): 'f32' or 'fp8' (E4M3, one scale per row of d_I values;
-    the pages run the indexer in FP4 -- the configurations ask for FP32 and FP8);
+  * indexer operands ("idx_store"): 'f32', 'fp8' (E4M3, one scale per row of d_I values) or
+    'mxfp4' (E2M1 elements, one power-of-two scale per 32 -- the pages' own indexer precision,
+    [P2] 事後学習 §3; the configurations ask for FP32 and FP8);
   * raw rows after RoPE ("q_store"): 'f32' or 'bf16', the activation dtype.
 Everything else is double precision.
 """
@@ -17,8 +18,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (attention_rows, compress, decode_one, dequant_fp8, entry_pos, index_scores_f32,
-               index_scores_f64, num_entries, quant_rows_fp8, rope, round_bf16_fast, topk)
+from . import (attention_rows, compress, decode_one, dequant_fp8, dequant_mxfp4, entry_pos, index_scores_f32,
+               index_scores_f64, num_entries, quant_rows_fp8, quant_rows_mxfp4, rope, round_bf16_fast, topk)
 
 __all__ = ["store_rows", "kv_compress", "indexer_topk", "csa_rows", "hca_rows", "csa_decode",
            "hca_decode", "project", "grouped_output_projection"]
@@ -39,6 +40,9 @@ def store_rows(x: np.ndarray, store: str, d_rope: int = 0):
     if store == "fp8":
         codes, scales = quant_rows_fp8(x.astype(np.float32))
         return dequant_fp8(codes, scales), (codes, scales)
+    if store == "mxfp4":
+        codes, e8 = quant_rows_mxfp4(x.astype(np.float32))
+        return dequant_mxfp4(codes, e8), (codes, e8)
     if store == "mixed":
         d = x.shape[-1]
         nope = x[..., : d - d_rope]
@@ -85,10 +89,10 @@ def indexer_topk(qI_rows, KI, w_rows, m, k, pos, idx_store):
     if idx_store == "f32":
         s = index_scores_f32(np.asarray(qI_rows, np.float32), np.asarray(KI, np.float32),
                              np.asarray(w_rows, np.float32), m, pos)
-    elif idx_store in ("fp8", "f64"):
+    elif idx_store in ("fp8", "mxfp4", "f64"):
         q = np.asarray(qI_rows, np.float64)
-        if idx_store == "fp8":
-            q, _ = store_rows(q, "fp8")
+        if idx_store != "f64":
+            q, _ = store_rows(q, idx_store)
         s = index_scores_f64(q, np.asarray(KI, np.float64), np.asarray(w_rows, np.float64), m, pos)
     else:
         raise ValueError(idx_store)

@@ -474,8 +474,8 @@ def _oracle_decode(wl, inp, b, csa, gpu_idx=None):
     ctx = int(inp["ctx"][b])
     C, _ = oracle.store_rows(np64(inp["C"][b]), wl.c_t if wl.c_t == "mixed" else "f64", wl.d_rope)
     if csa:
-        kc, ks = oracle.quant_rows_fp8(np32(inp["KI"][b]))
-        res = oracle.csa_decode(np64(inp["q"][b]), ctx, C, np32(inp["qI"][b]), oracle.dequant_fp8(kc, ks),
+        KI, _ = oracle.store_rows(np32(inp["KI"][b]), wl.idx_t)
+        res = oracle.csa_decode(np64(inp["q"][b]), ctx, C, np32(inp["qI"][b]), KI,
                                 np32(inp["w"][b]), np64(inp["ring"][b]), np64(inp["sink"]), m=m, k=wl.topk,
                                 idx_store=wl.idx_t, **kw)
         if gpu_idx is not None:
@@ -498,9 +498,11 @@ def _check_decode(wl, inp, layer, out, csa, seqs):
 
 
 @pytest.mark.parametrize("csa", [True, False])
-@pytest.mark.parametrize("c_t", ["bf16", "mixed"])
-def test_decode(lib, csa, c_t):
-    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=8192, topk=256, c_t=c_t)
+@pytest.mark.parametrize("c_t,idx_t", [("bf16", "fp8"), ("mixed", "fp8"), ("bf16", "mxfp4")])
+def test_decode(lib, csa, c_t, idx_t):
+    if idx_t == "mxfp4" and not csa:
+        pytest.skip("the HCA layer has no indexer")
+    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=8192, topk=256, c_t=c_t, idx_t=idx_t)
     from long_context_compressed_14_b300.pipeline import DecodeLayer
     inp = synth.decode_layer(wl, csa=csa)
     inp["ctx"] = torch.tensor([8192, 1, 77, 5001], dtype=torch.int32)

@@ -485,3 +485,65 @@ def test_projection_identity_and_block_diagonal_grouping():
     y2, _ = oracle.grouped_output_projection(o2, Wg, Wo, groups)
     np.testing.assert_allclose(y2[:, dg:], y[:, dg:], rtol=0, atol=0)
     assert np.abs(y2[:, :dg] - y[:, :dg]).max() > 1e-3
+
+
+# ---------------------------------------------------------------------------------------
+# FP4 (E2M1, MXFP4) codec
+# ---------------------------------------------------------------------------------------
+
+def test_e2m1_values_and_round_trip():
+    vals = oracle.e2m1_decode(np.arange(16))
+    np.testing.assert_array_equal(vals[:8], [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    np.testing.assert_array_equal(vals[8:], -vals[:8])
+    assert np.all(oracle.e2m1_encode(vals[1:8]) == np.arange(1, 8))
+    assert np.all(oracle.e2m1_encode(vals[9:]) == np.arange(9, 16))
+
+
+def test_e2m1_rounding_fixture():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "e2m1_rounding.txt")) if l.strip() and not l.startswith("#")]
+    x = np.array([float(r[0]) for r in rows])
+    want = np.array([float(r[1]) for r in rows])
+    np.testing.assert_array_equal(oracle.e2m1_decode(oracle.e2m1_encode(x)), want)
+
+
+def test_mxfp4_block_exponent_rule_and_error_bound():
+    # the block exponent is floor(log2(block max)) - 2, so the block max lands in [4, 8) and a
+    # max of 6 * 2^e is exact; a zero block gets exponent byte 0 and zero codes
+    x = np.zeros((3, 64), np.float32)
+    x[0, 0], x[0, 32:35] = 12.0, [1.0, 2.0, 3.0]
+    x[1, 5] = 6.0
+    codes, e8 = oracle.quant_rows_mxfp4(x)
+    np.testing.assert_array_equal(e8, [[128, 126], [127, 0], [0, 0]])
+    deq = oracle.dequant_mxfp4(codes, e8)
+    np.testing.assert_array_equal(deq[0, [0, 32, 33, 34]], [12.0, 1.0, 2.0, 3.0])
+    assert deq[1, 5] == 6.0 and np.all(deq[2] == 0.0)
+    # random rows: below 6 * 2^e an element errs by at most half a gap (at most 1 * 2^e,
+    # between 4 and 6); above it -- the block max lies in [4, 8) * 2^e -- it saturates at 6 * 2^e,
+    # an error below 2 * 2^e; the block max is never exceeded
+    rng = np.random.default_rng(3)
+    r = (rng.standard_normal((200, 64)) * np.exp(rng.standard_normal((200, 1)) * 4)).astype(np.float32)
+    c, e = oracle.quant_rows_mxfp4(r)
+    d = oracle.dequant_mxfp4(c, e)
+    scale = np.repeat(np.exp2(e.astype(np.float64) - 127), 32, axis=1)
+    inside = np.abs(r) <= 6 * scale
+    assert np.all(np.abs(d - r)[inside] <= 1.0 * scale[inside])
+    assert np.all(np.abs(d - r)[~inside] < 2.0 * scale[~inside])
+    assert np.all(np.abs(d[~inside]) == 6 * scale[~inside])
+    blkmax = np.repeat(np.abs(r.reshape(200, 2, 32)).max(axis=2), 32, axis=1)
+    assert np.all(np.abs(d) <= np.maximum(blkmax, 6 * scale) + 1e-300)
+
+
+def test_mxfp4_to_fp8_is_exact():
+    # [P2] 事後学習 §3: FP4 -> FP8 dequantisation is lossless. With E the row's larger block
+    # exponent, every element times 2^(e_blk - E + 6) is an E4M3 value (checked with the
+    # oracle's E4M3 codec, pinned against torch), so codes * 2^(E - 6) reproduce the row exactly
+    rng = np.random.default_rng(4)
+    r = (rng.standard_normal((300, 64)) * np.exp(rng.standard_normal((300, 1)) * 3)).astype(np.float32)
+    r[:, 32:] *= np.exp2(rng.integers(-10, 10, (300, 1))).astype(np.float32)
+    c, e = oracle.quant_rows_mxfp4(r)
+    v = oracle.dequant_mxfp4(c, e)
+    E = e.astype(np.int64).max(axis=1, keepdims=True) - 127
+    scaled = v * np.exp2(6.0 - E)
+    codes8 = oracle.fp8_encode(scaled.astype(np.float32))
+    back = oracle.fp8_decode(codes8).astype(np.float64) * np.exp2(E - 6.0)
+    np.testing.assert_array_equal(back, v)
