@@ -63,6 +63,7 @@ def _load():
             "orc_e2m1_decode": (_DBL, [ctypes.c_uint8]),
             "orc_e2m1_encode": (ctypes.c_uint8, [_DBL]),
             "orc_quant_rows_mxfp4": (None, [_P, _I64, _INT, _P, _P]),
+            "orc_quant_rows_nvfp4": (None, [_P, _I64, _INT, _P, _P, _P]),
             "orc_index_scores_f32": (None, [_P, _P, _P, _I64, _INT, _INT, _INT, _P, _I64, _P]),
             "orc_index_scores_f64": (None, [_P, _P, _P, _I64, _INT, _INT, _INT, _P, _I64, _P]),
             "orc_topk": (None, [_P, _I64, _INT, _P, _I64, _INT, _P]),
@@ -209,6 +210,31 @@ def dequant_mxfp4(codes: np.ndarray, e8: np.ndarray) -> np.ndarray:
     elems[..., 1::2] = codes >> 4
     scale = np.exp2(np.asarray(e8, np.float64) - 127.0)
     return e2m1_decode(elems) * np.repeat(scale, 32, axis=-1)
+
+
+def quant_rows_nvfp4(x: np.ndarray):
+    """Per-row NVFP4 quantisation -> (codes uint8 [rows, cols/2] (element 2i in the low nibble),
+    block-scale codes uint8 [rows, cols/16] (E4M3), row scales float32 [rows])."""
+    x = _c(x, np.float32)
+    shp = x.shape
+    x2 = x.reshape(-1, shp[-1])
+    codes = np.zeros((x2.shape[0], shp[-1] // 2), dtype=np.uint8)
+    bcode = np.zeros((x2.shape[0], shp[-1] // 16), dtype=np.uint8)
+    rs = np.zeros(x2.shape[0], dtype=np.float32)
+    _load().orc_quant_rows_nvfp4(_ptr(x2), x2.shape[0], x2.shape[1], _ptr(codes), _ptr(bcode), _ptr(rs))
+    return (codes.reshape(shp[:-1] + (shp[-1] // 2,)), bcode.reshape(shp[:-1] + (shp[-1] // 16,)),
+            rs.reshape(shp[:-1]))
+
+
+def dequant_nvfp4(codes: np.ndarray, bcode: np.ndarray, rs: np.ndarray) -> np.ndarray:
+    """Values of NVFP4 rows: E2M1 element times its block's scale, the float product
+    E4M3(block code) * row scale."""
+    codes = np.asarray(codes, np.uint8)
+    elems = np.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), dtype=np.uint8)
+    elems[..., 0::2] = codes & 15
+    elems[..., 1::2] = codes >> 4
+    scale = (fp8_decode(bcode).astype(np.float32) * np.asarray(rs, np.float32)[..., None]).astype(np.float64)
+    return e2m1_decode(elems) * np.repeat(scale, 16, axis=-1)
 
 
 def dequant_fp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:

@@ -246,6 +246,41 @@ void orc_quant_rows_mxfp4(const float *x, int64_t rows, int cols, uint8_t *codes
     }
 }
 
+/* NVFP4 rows (reading of [P3] "Технический отчёт DeepSeek-V4.1-Flash — часть 2/2": the   */
+/* V4.1 KV cache is stored in NVFP4, quantised after RoPE). NVFP4: blocks of 16 E2M1      */
+/* elements, each with an E4M3 scale. Reading of its second-level scale: one float per    */
+/* row, s = amax / (6 * 448) in float, so that every block scale fits E4M3 (6 = E2M1's    */
+/* largest value, 448 = E4M3's). Block b with max |x| = bmax: code_b = E4M3(bmax / (6 s)) */
+/* (the product 6 s and the division in float); scale_b = decode(code_b) * s in float;    */
+/* element = E2M1(x / scale_b), the division in float, 0 when scale_b is 0 (also when the */
+/* block scale underflows E4M3). Dequantised value = E2M1 * scale_b.                     */
+/* x [rows, cols] (cols a multiple of 16) -> codes [rows, cols/2] (element 2i in the low   */
+/* nibble of byte i), block codes [rows, cols/16], row scales [rows].                     */
+void orc_quant_rows_nvfp4(const float *x, int64_t rows, int cols, uint8_t *codes, uint8_t *bcode, float *rs)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *row = x + r * cols;
+        float amax = 0.0f;
+        for (int c = 0; c < cols; ++c) amax = fmaxf(amax, fabsf(row[c]));
+        const float s = amax / 2688.0f;
+        rs[r] = s;
+        for (int blk = 0; blk < cols / 16; ++blk) {
+            const float *v = row + blk * 16;
+            float bmax = 0.0f;
+            for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+            const float six_s = 6.0f * s;
+            const uint8_t bc = s > 0.0f ? orc_fp8_encode(bmax / six_s) : 0;
+            bcode[r * (cols / 16) + blk] = bc;
+            const float scale = orc_fp8_decode(bc) * s;
+            for (int i = 0; i < 16; ++i) {
+                const uint8_t q = scale > 0.0f ? orc_e2m1_encode((double)(v[i] / scale)) : 0;
+                uint8_t *byte = codes + r * (cols / 2) + blk * 8 + i / 2;
+                if (i % 2 == 0) *byte = q; else *byte |= (uint8_t)(q << 4);
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Lightning indexer score.                                                              */
 /* [P2] 提案手法 §1 CSA: a lightning indexer scores the compressed entries so that top-k */

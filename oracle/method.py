@@ -5,9 +5,13 @@ Sources: [P2] "DeepSeek-V4: Towards Highly Efficient Million-Token Context Intel
 
 Storage formats that the configurations fix are applied exactly where the data would be
 stored, because they are approximations the result depends on:
-  * compressed entries ("c_store"): 'f32', 'bf16', or 'mixed' -- [P2] 訓練インフラの革新 §5:
+  * compressed entries ("c_store"): 'f32', 'bf16', 'mixed' -- [P2] 訓練インフラの革新 §5:
     a KV entry keeps its RoPE dimensions in BF16 and its other dimensions in FP8 (reading:
-    E4M3 with one float scale per entry row, amax/448);
+    E4M3 with one float scale per entry row, amax/448) -- or 'nvfp4' -- [P3] "Технический
+    отчёт DeepSeek-V4.1-Flash — часть 2/2": the V4.1 KV cache in NVFP4, quantised after RoPE
+    (blocks of 16 E2M1 values with an E4M3 scale; reading: one float scale per entry row);
+  * window rows: as the activations ('f32', 'bf16') or, for the V4.1 decode ring ([P3]: the
+    SWA cache in FP8), 'fp8' rows with one scale each;
   * indexer operands ("idx_store"): 'f32', 'fp8' (E4M3, one scale per row of d_I values) or
     'mxfp4' (E2M1 elements, one power-of-two scale per 32 -- the pages' own indexer precision,
     [P2] 事後学習 §3; the configurations ask for FP32 and FP8);
@@ -18,8 +22,9 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (attention_rows, compress, decode_one, dequant_fp8, dequant_mxfp4, entry_pos, index_scores_f32,
-               index_scores_f64, num_entries, quant_rows_fp8, quant_rows_mxfp4, rope, round_bf16_fast, topk)
+from . import (attention_rows, compress, decode_one, dequant_fp8, dequant_mxfp4, dequant_nvfp4, entry_pos,
+               index_scores_f32, index_scores_f64, num_entries, quant_rows_fp8, quant_rows_mxfp4, quant_rows_nvfp4,
+               rope, round_bf16_fast, topk)
 
 __all__ = ["store_rows", "kv_compress", "indexer_topk", "csa_rows", "hca_rows", "csa_decode",
            "hca_decode", "project", "grouped_output_projection"]
@@ -43,6 +48,9 @@ def store_rows(x: np.ndarray, store: str, d_rope: int = 0):
     if store == "mxfp4":
         codes, e8 = quant_rows_mxfp4(x.astype(np.float32))
         return dequant_mxfp4(codes, e8), (codes, e8)
+    if store == "nvfp4":
+        codes, bcode, rs = quant_rows_nvfp4(x.astype(np.float32))
+        return dequant_nvfp4(codes, bcode, rs), (codes, bcode, rs)
     if store == "mixed":
         d = x.shape[-1]
         nope = x[..., : d - d_rope]
@@ -61,10 +69,12 @@ def kv_compress(kv, z, kI_raw, m, d_rope, theta, c_store="f64", idx_store="f64",
     kI_raw [L, dI] raw indexer-key rows or None.
     Returns dict with
       C      [N, d]  entries after RoPE at (j+1)m-1, in c_store (as doubles),
-      C_raw  stored representation (codes, scales) for 'mixed', else None,
+      C_raw  stored representation for 'mixed' (codes, scales) and 'nvfp4' (codes, block
+             codes, row scales), else None,
       KI     [N, dI] compressed indexer keys in idx_store (as doubles) or None,
       KI_raw stored representation for 'fp8', else None,
-      kv_rope [L, d] raw rows after RoPE at their own positions, in q_store.
+      kv_rope [L, d] raw rows after RoPE at their own positions, in q_store (the window
+             keys; q_store 'fp8' gives the rows of an FP8 decode ring).
     """
     kv = np.asarray(kv, np.float64)
     L, d = kv.shape

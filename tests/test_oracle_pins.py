@@ -419,7 +419,7 @@ def test_attention_is_invariant_to_a_common_position_shift():
                            oracle.rope(outs[1], np.array([1039]), 64, theta), atol=1e-3)
 
 
-@pytest.mark.parametrize("idx_store,c_store", [("f32", "f32"), ("fp8", "mixed")])
+@pytest.mark.parametrize("idx_store,c_store", [("f32", "f32"), ("fp8", "mixed"), ("mxfp4", "nvfp4")])
 def test_decode_equals_last_prefill_row(idx_store, c_store):
     # Decode at ctx = L against caches built from the same raw rows equals row L-1 of a
     # prefill of length L (CSA and HCA).
@@ -547,3 +547,90 @@ def test_mxfp4_to_fp8_is_exact():
     codes8 = oracle.fp8_encode(scaled.astype(np.float32))
     back = oracle.fp8_decode(codes8).astype(np.float64) * np.exp2(E - 6.0)
     np.testing.assert_array_equal(back, v)
+
+
+# ---------------------------------------------------------------------------------------
+# NVFP4 entries and FP8 window rows (the V4.1 cache variant)
+# ---------------------------------------------------------------------------------------
+
+def _nvfp4_fixture():
+    x = np.zeros(128, np.float32)
+    want = np.zeros(128)
+    scale, blocks = None, None
+    for line in open(os.path.join(GOLDEN, "nvfp4_row_hand.txt")):
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "scale":
+            scale = float(f[1])
+        elif f[0] == "blocks":
+            blocks = [int(v, 16) for v in f[1:]]
+        else:
+            x[int(f[0])], want[int(f[0])] = float(f[1]), float(f[2])
+    return x, want, scale, blocks
+
+
+def test_nvfp4_hand_worked_row():
+    x, want, scale, blocks = _nvfp4_fixture()
+    codes, bcode, rs = oracle.quant_rows_nvfp4(x[None])
+    assert rs[0] == scale
+    np.testing.assert_array_equal(bcode[0], blocks)
+    np.testing.assert_array_equal(oracle.dequant_nvfp4(codes, bcode, rs)[0], want)
+
+
+def test_nvfp4_exact_on_representable_rows():
+    # rows built from the format itself -- s a power of two, block scale c_b an E4M3 value, the
+    # block's elements E2M1 values (one of them +-6) times c_b s, one block with c_b = 448 -- come
+    # back exactly, with block codes E4M3(c_b) and row scale s (a wrong 6 or 448, a block of
+    # 32 instead of 16, or a misplaced scale breaks it)
+    rng = np.random.default_rng(11)
+    grid = oracle.e2m1_decode(np.arange(16))
+    e4m3 = oracle.fp8_decode(np.arange(0x08, 0x7F)).astype(np.float64)  # normal E4M3 values
+    rows = np.zeros((64, 128))
+    cb = np.zeros((64, 8))
+    s = np.exp2(rng.integers(-20, 10, 64)).astype(np.float64)
+    for r in range(64):
+        cb[r] = rng.choice(e4m3, 8)
+        cb[r, rng.integers(0, 8)] = 448.0
+        for b in range(8):
+            el = rng.choice(grid, 16)
+            el[rng.integers(0, 16)] = rng.choice([-6.0, 6.0])
+            rows[r, 16 * b:16 * b + 16] = el * cb[r, b] * s[r]
+    x = rows.astype(np.float32)
+    assert np.array_equal(x.astype(np.float64), rows)
+    codes, bcode, rs = oracle.quant_rows_nvfp4(x)
+    np.testing.assert_array_equal(rs, s.astype(np.float32))
+    np.testing.assert_array_equal(oracle.fp8_decode(bcode), cb)
+    np.testing.assert_array_equal(oracle.dequant_nvfp4(codes, bcode, rs), rows)
+
+
+def test_nvfp4_error_bound_on_random_rows():
+    # each element errs by at most half a gap of the E2M1 grid (at most 1 x the block scale,
+    # between 4 and 6) when inside 6 x scale, and saturates to +-6 x scale outside it, which the
+    # block-scale rounding (relative 2^-4 for a normal E4M3 code) keeps below 6.4 x scale
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((300, 128)) * np.exp(rng.standard_normal((300, 1)) * 3)).astype(np.float32)
+    codes, bcode, rs = oracle.quant_rows_nvfp4(x)
+    d = oracle.dequant_nvfp4(codes, bcode, rs)
+    scale = np.repeat((oracle.fp8_decode(bcode).astype(np.float32) * rs[:, None]).astype(np.float64), 16, axis=1)
+    normal = np.repeat(bcode >= 0x08, 16, axis=1)
+    xs = x.astype(np.float64)
+    inside = normal & (np.abs(xs) <= 6 * scale)
+    assert np.all(np.abs(d - xs)[inside] <= 1.0 * scale[inside])
+    out = normal & ~inside
+    assert np.all(np.abs(d[out]) == 6 * scale[out]) and np.all(np.abs(xs[out]) <= 6.4 * scale[out])
+    # the whole row: relative L2 error of a 4-bit format, well below 0.2
+    rel = np.linalg.norm(d - xs, axis=1) / np.linalg.norm(xs, axis=1)
+    assert rel.max() < 0.2
+
+
+def test_nvfp4_and_fp8_window_storage_rows():
+    # store_rows applies the formats: 'nvfp4' is the quantiser's dequantised row, 'fp8' the
+    # per-row FP8 of the window ring
+    x = RNG.standard_normal((20, 128)) * 3
+    vals, (codes, bcode, rs) = oracle.store_rows(x, "nvfp4")
+    np.testing.assert_array_equal(vals, oracle.dequant_nvfp4(codes, bcode, rs))
+    assert codes.shape == (20, 64) and bcode.shape == (20, 8) and rs.shape == (20,)
+    v8, (c8, s8) = oracle.store_rows(x, "fp8")
+    np.testing.assert_array_equal(s8, (np.abs(x.astype(np.float32)).max(axis=1) / np.float32(448)).astype(np.float32))
+    np.testing.assert_array_equal(v8, oracle.dequant_fp8(c8, s8))
