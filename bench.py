@@ -424,7 +424,8 @@ def measure_decode(lib, args, pk, name="decode_b16_ctx131072"):
     byts = decode_bytes(wl, True) + decode_bytes(wl, False)
     ms = rec["ms_step_graph"]
     ach = byts / (ms / 1e3) / 1e9
-    return {"workload": wl.name, "B": wl.B, "ctx": wl.L, "ms_per_step": ms, "tokens_per_s": wl.B / (ms / 1e3),
+    return {"workload": wl.name, "B": wl.B, "ctx": wl.L, "entries": wl.c_t, "window_ring": wl.w_t or wl.q_t,
+            "ms_per_step": ms, "tokens_per_s": wl.B / (ms / 1e3),
             "ms_per_step_eager": rec["ms_step"], "stages_eager_ms": rec["stage_ms"], "cuda_graph": True,
             "l2": "L2 flushed between steps (2x126 MiB write)" if rec["flush"] else "inputs larger than L2",
             "gpu_launches_per_step": rec["launches"] / args.steps, "clocks": rec["clocks"],
@@ -553,6 +554,7 @@ def run_mine(args, rank, world, local_rank):
         line["cuda_graph"] = True
     if wl.kind == "pair" and not args.no_decode:
         line["decode"] = measure_decode(lib, args, pk)
+        line["decode_v41_cache"] = measure_decode(lib, args, pk, "decode_v41_b16_ctx131072")
     if wl.kind == "pair" and not args.no_projections:
         line["projections"] = measure_projections(lib, args, wl, pk)
     if world == 1 and not args.no_cpu_baseline:
@@ -561,15 +563,20 @@ def run_mine(args, rank, world, local_rank):
 
 
 def decode_bytes(wl, csa):
-    """HBM bytes one decode step of one layer must move (all sequences)."""
+    """HBM bytes one decode step of one layer must move (all sequences): q and the output, the
+    window rows and the entries read in their stored form, and for CSA the indexer-key cache
+    and the indexer query rows."""
     B, d, H = wl.B, wl.d, wl.H
     n_c = wl.L // wl.m
     act = 2 if wl.q_t == "bf16" else 4
-    by = B * (H * d * act * 2 + wl.n_win * d * act)          # q, out, window rows
+    entry = {"f32": 4 * d, "bf16": 2 * d, "mixed": (d - wl.d_rope) + 2 * wl.d_rope + 4, "nvfp4": 80}[wl.c_t]
+    win = 144 if wl.w_t == "fp8" else d * act
+    key = {"f32": 4 * wl.d_I, "fp8": wl.d_I + 4, "mxfp4": wl.d_I // 2 + wl.d_I // 32}[wl.idx_t]
+    by = B * (H * d * act * 2 + wl.n_win * win)              # q, out, window rows
     if csa:
-        by += B * (n_c * (wl.d_I + 4) + wl.topk * d * act + wl.H_I * (wl.d_I * 4 + 4))
+        by += B * (n_c * key + wl.topk * entry + wl.H_I * (wl.d_I * 4 + 4))
     else:
-        by += B * (wl.L // wl.m_hca) * d * act
+        by += B * (wl.L // wl.m_hca) * entry
     return by
 
 
@@ -623,6 +630,8 @@ def workload_config(wl, big_inputs):
         cfg.update({"m": wl.m, "topk": wl.topk, "H_I": wl.H_I, "d_I": wl.d_I, "indexer": wl.idx_t})
     if wl.kind in ("hca", "pair", "decode"):
         cfg["m_hca"] = wl.m_hca
+    if wl.kind == "decode":
+        cfg["window_ring"] = wl.w_t or wl.q_t
     cfg["l2"] = "inputs larger than L2 (no flush)" if big_inputs else "L2 flushed between steps (2x126 MiB write)"
     return cfg
 
@@ -680,17 +689,22 @@ def _oracle_decode_sample(wl, layer, csa, n_seq):
     sub = wl.replace(B=n_seq)
     inp = synth.decode_layer(sub, layer, csa=csa)
     kw = dict(d_rope=wl.d_rope, theta=wl.theta, n_win=wl.n_win, scale=wl.scale)
+    # the caches in their stored formats (state written before the step, not timed)
+    caches = []
+    for b in range(n_seq):
+        C, _ = oracle.store_rows(_np64(inp["C"][b]), wl.c_t if wl.c_t in ("mixed", "nvfp4") else "f64", wl.d_rope)
+        ring, _ = oracle.store_rows(_np64(inp["ring"][b]), "fp8" if wl.w_t == "fp8" else "f64")
+        KI = oracle.store_rows(inp["KI"][b].numpy(), wl.idx_t)[0] if csa else None
+        caches.append((C, ring, KI))
     t0 = time.perf_counter()
     for b in range(n_seq):
         ctx = int(inp["ctx"][b])
+        C, ring, KI = caches[b]
         if csa:
-            kc, ks = oracle.quant_rows_fp8(inp["KI"][b].numpy())
-            oracle.csa_decode(_np64(inp["q"][b]), ctx, _np64(inp["C"][b]), inp["qI"][b].numpy(),
-                              oracle.dequant_fp8(kc, ks), inp["w"][b].numpy(), _np64(inp["ring"][b]),
+            oracle.csa_decode(_np64(inp["q"][b]), ctx, C, inp["qI"][b].numpy(), KI, inp["w"][b].numpy(), ring,
                               _np64(inp["sink"]), m=wl.m, k=wl.topk, idx_store=wl.idx_t, **kw)
         else:
-            oracle.hca_decode(_np64(inp["q"][b]), ctx, _np64(inp["C"][b]), _np64(inp["ring"][b]), _np64(inp["sink"]),
-                              m=wl.m_hca, **kw)
+            oracle.hca_decode(_np64(inp["q"][b]), ctx, C, ring, _np64(inp["sink"]), m=wl.m_hca, **kw)
     dt = time.perf_counter() - t0
     return dt / n_seq, n_seq, dt
 

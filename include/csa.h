@@ -45,7 +45,9 @@ typedef enum {
     CSA_BF16 = 1,    /* bfloat16 */
     CSA_FP8E4M3 = 2, /* FP8 E4M3 ("fn": no infinities, max 448), with a float scale per row */
     CSA_MIXED = 3,   /* compressed entry: dims [0, d-d_rope) FP8 E4M3 + row scale, RoPE dims BF16 */
-    CSA_MXFP4 = 4    /* indexer operand rows in MXFP4: E2M1 elements, one E8M0 exponent per 32 */
+    CSA_MXFP4 = 4,   /* indexer operand rows in MXFP4: E2M1 elements, one E8M0 exponent per 32 */
+    CSA_NVFP4 = 5    /* compressed entry in NVFP4: E2M1 elements, one E4M3 scale per 16, a float
+                        scale per entry (an 80-byte row, layout at csa_entries) */
 } csa_dtype;
 
 typedef enum {
@@ -72,16 +74,26 @@ typedef struct {
     int H_I;        /* CSA indexer heads */
     int d_I;        /* CSA indexer dim; must be 64 */
     float scale;    /* softmax scale of the logits (1/sqrt(d)) */
-    int act_t;      /* csa_dtype of q, raw kv, kv_rope, the SWA ring and the output: F32 | BF16 */
-    int kv_t;       /* csa_dtype of compressed entries: F32 | BF16 | MIXED */
+    int act_t;      /* csa_dtype of q, raw kv, kv_rope and the output: F32 | BF16 */
+    int kv_t;       /* csa_dtype of compressed entries: F32 | BF16 | MIXED | NVFP4 (BF16 act_t) */
     int idx_t;      /* csa_dtype of the indexer operands: F32 | FP8E4M3 | MXFP4 */
     int rope_len;   /* rows of the RoPE table (positions 0 .. rope_len-1) */
+    int win_t;      /* csa_dtype of the decode SWA ring: act_t, or FP8E4M3 with BF16 act_t (the
+                       ring's rows then are 144-byte FP8 rows, layout at csa_decode) */
 } csa_params;
 
 /* Compressed entries of B sequences, N_cap = ceil(L / m) rows per sequence.
  *  F32 / BF16: data = [B, N_cap, d];  rope = scale = NULL.
  *  MIXED     : data = [B, N_cap, d - d_rope] FP8 E4M3 codes, rope = [B, N_cap, d_rope] BF16,
  *              scale = [B, N_cap] float; value = decode(code) * scale on the first dims.
+ *  NVFP4     : data = [B, N_cap, 80] bytes, one row per entry; rope = scale = NULL. Row: bytes
+ *              [0, 64) E2M1 codes (dim 2i in the low nibble of byte i), [64, 72) one E4M3 scale
+ *              code per block of 16 dims, [72, 76) the float entry scale s = max|c| / (6 * 448),
+ *              [76, 80) zero. Block b: scale_b = E4M3(code_b) * s (float product); dim value =
+ *              E2M1 * scale_b. Quantised after RoPE. ([P3] "Технический отчёт DeepSeek-V4.1-Flash
+ *              — часть 2/2": the V4.1 KV cache in NVFP4, quantised after RoPE; the block of 16
+ *              with an E4M3 scale is the NVFP4 format, the float scale per entry is this
+ *              library's reading of its second-level scale.)
  * Entries hold RoPE already applied at the entry position (j+1)m - 1. */
 typedef struct {
     void *data;
@@ -139,6 +151,21 @@ int csa_rope_table(float *tab, int rope_len, int d_rope, float theta, csa_stream
 int csa_quant_fp8_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
                        csa_stream_t stream);
 
+/* NVFP4 entry rows (layout at csa_entries) of x [rows, 128] float: s = max|x[r,:]| / (6 * 448)
+ * (float division), block code_b = E4M3(max_b / (6 s)) (E4M3 rounded to nearest even,
+ * saturated), scale_b = E4M3(code_b) * s, element = E2M1(x / scale_b) rounded to nearest even
+ * and saturated at 6 (0 when scale_b is 0). out [rows, 80] bytes, 16-byte aligned. Used to
+ * build an entry cache from rows that already hold RoPE (the library's own compression writes
+ * NVFP4 entries itself). */
+int csa_quant_nvfp4_entries(const float *x, int64_t rows, uint8_t *out, csa_stream_t stream);
+
+/* FP8 SWA-ring rows of x [rows, 128] float (RoPE already applied): bytes [0, 128) E4M3 codes
+ * E4M3(x / s) with s = max|x[r,:]| / 448, bytes [128, 132) the float s, [132, 144) zero; a zero
+ * row gets s = 0 and zero codes. out [rows, 144] bytes, 16-byte aligned. ([P3]: the V4.1
+ * sliding-window KV cache in FP8.) Used for the prefill -> decode hand-over of the ring;
+ * kv_append writes ring rows in this form itself when win_t = FP8E4M3. */
+int csa_quant_fp8_window_rows(const float *x, int64_t rows, uint8_t *out, csa_stream_t stream);
+
 /* Per-row MXFP4 quantisation of x [rows, 64] float (the indexer's FP4 operands, [P2] 事後学習
  * §3): per block of 32 values, e = floor(log2(max |x|)) - 2 clamped to [-127, 127] (a block of
  * zeros: e = -127), E8M0 byte e + 127, codes = E2M1(x / 2^e) rounded to nearest even and
@@ -177,10 +204,12 @@ int kv_compress(const csa_params *p, const void *kv, const float *z, const float
  *    (the same weights over the indexer keys) to KI per idx_t. Entries of incomplete blocks are
  *    not written (no decode query sees them).
  * A prefill of L0 tokens hands over to decode with: C and KI from kv_compress, ring slots filled
- * from kv_rope (the last n_win rows), and the state from the last 2m raw rows of kv, z and kI.
+ * from kv_rope (the last n_win rows; through csa_quant_fp8_window_rows for an FP8 ring), and the
+ * state from the last 2m raw rows of kv, z and kI.
  *   kv_new [B, d] act_t (before RoPE); z_new [B, 2] float; kI_new [B, d_I] float or NULL;
  *   ctx_len [B] int32 (device; counts the new token; 1 <= ctx_len <= L, the cache capacity);
- *   ring [B, n_win, d] act_t; state_kv [B, 2m, d] act_t; state_z [B, 2m, 2] float;
+ *   ring [B, n_win, d] act_t, or FP8 rows [B, n_win, 144] bytes when win_t = FP8E4M3 (the row
+ *   quantised as csa_quant_fp8_window_rows does); state_kv [B, 2m, d] act_t; state_z [B, 2m, 2] float;
  *   state_kI [B, 2m, d_I] float (NULL when kI_new is NULL); C, KI: caches [B, ceil(L/m), ...].
  * A position outside [0, L) is skipped and recorded as CSA_ERR_BOUNDS. */
 int kv_append(const csa_params *p, const void *kv_new, const float *z_new, const float *kI_new,
@@ -239,8 +268,9 @@ int hca_prefill(const csa_params *p, const void *q, const void *kv_rope, const c
  *   q [B, H, d] act_t (before RoPE); ctx_len [B] int32 (device), 1 <= ctx_len[b] <= L;
  *   C: entry cache [B, ceil(L/m), ...] (entries j < ctx_len/m are read);
  *   qI rows [B, H_I, d_I] (+scale [B, H_I]); KI cache rows [B, ceil(L/m), d_I] (+scale);
- *   w [B, H_I]; swa_ring [B, n_win, d] act_t: the raw row of position u, after RoPE at u,
- *   at slot u mod n_win, for u in [max(0, p - n_win + 1), p];
+ *   w [B, H_I]; swa_ring [B, n_win, d] act_t (win_t = act_t) or [B, n_win, 144] bytes of FP8
+ *   rows (win_t = FP8E4M3; row layout at csa_quant_fp8_window_rows): the raw row of position
+ *   u, after RoPE at u, at slot u mod n_win, for u in [max(0, p - n_win + 1), p];
  *   topk_out [B, topk] or NULL; out [B, H, d]; lse_out [B, H] or NULL. */
 int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const csa_entries *C,
                const csa_index_rows *qI, const csa_index_rows *KI, const float *w,

@@ -21,13 +21,15 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcsa.so")
 
 # csa_dtype
-F32, BF16, FP8E4M3, MIXED, MXFP4 = 0, 1, 2, 3, 4
+F32, BF16, FP8E4M3, MIXED, MXFP4, NVFP4 = 0, 1, 2, 3, 4, 5
+NVFP4_ROW_BYTES = 80      # an NVFP4 entry row (layout in include/csa.h, csa_entries)
+FP8_WIN_ROW_BYTES = 144   # an FP8 window-ring row (layout in include/csa.h)
 # csa_op
 OP_INDEX_TOPK, OP_CSA_PREFILL, OP_HCA_PREFILL, OP_CSA_DECODE, OP_HCA_DECODE, OP_SPARSE_ATTENTION = range(6)
 # csa_status
 OK, ERR_INVALID, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_TIMEOUT, ERR_BOUNDS, ERR_CUDA = range(8)
 
-_DT = {"f32": F32, "bf16": BF16, "fp8": FP8E4M3, "mixed": MIXED, "mxfp4": MXFP4}
+_DT = {"f32": F32, "bf16": BF16, "fp8": FP8E4M3, "mixed": MIXED, "mxfp4": MXFP4, "nvfp4": NVFP4}
 
 
 class CsaError(RuntimeError):
@@ -39,7 +41,7 @@ class CsaError(RuntimeError):
 class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("B", "L", "H", "d", "d_rope", "m", "topk", "n_win", "H_I", "d_I")] + \
                [("scale", ctypes.c_float)] + \
-               [(n, ctypes.c_int) for n in ("act_t", "kv_t", "idx_t", "rope_len")]
+               [(n, ctypes.c_int) for n in ("act_t", "kv_t", "idx_t", "rope_len", "win_t")]
 
 
 class Entries(ctypes.Structure):
@@ -77,6 +79,8 @@ def _load():
             "csa_rope_table": (I, [P, I, I, ctypes.c_float, P]),
             "csa_quant_fp8_rows": (I, [P, I64, I, P, P, P]),
             "csa_quant_mxfp4_rows": (I, [P, I64, I, P, P, P]),
+            "csa_quant_nvfp4_entries": (I, [P, I64, P, P]),
+            "csa_quant_fp8_window_rows": (I, [P, I64, P, P]),
             "kv_compress": (I, [PP, P, P, P, P, PE, PI, P, P]),
             "kv_append": (I, [PP, P, P, P, P, P, P, P, P, P, PE, PI, P]),
             "csa_index_topk": (I, [PP, PI, PI, P, P, P, Z, P]),
@@ -183,6 +187,22 @@ def csa_quant_mxfp4_rows(x: torch.Tensor, codes: torch.Tensor, e8: torch.Tensor,
     rows = x.numel() // x.shape[-1]
     _ok(_load().csa_quant_mxfp4_rows(_ptr(x), rows, x.shape[-1], _ptr(codes), _ptr(e8), _stream(stream)),
         "csa_quant_mxfp4_rows")
+
+
+def csa_quant_nvfp4_entries(x: torch.Tensor, out: torch.Tensor, stream=None):
+    """x [.., 128] float -> NVFP4 entry rows out [.., 80] uint8."""
+    rows = x.numel() // x.shape[-1]
+    if x.shape[-1] != 128 or out.numel() != rows * NVFP4_ROW_BYTES:
+        raise ValueError("csa_quant_nvfp4_entries: x [.., 128] float, out [.., 80] uint8")
+    _ok(_load().csa_quant_nvfp4_entries(_ptr(x), rows, _ptr(out), _stream(stream)), "csa_quant_nvfp4_entries")
+
+
+def csa_quant_fp8_window_rows(x: torch.Tensor, out: torch.Tensor, stream=None):
+    """x [.., 128] float -> FP8 window rows out [.., 144] uint8."""
+    rows = x.numel() // x.shape[-1]
+    if x.shape[-1] != 128 or out.numel() != rows * FP8_WIN_ROW_BYTES:
+        raise ValueError("csa_quant_fp8_window_rows: x [.., 128] float, out [.., 144] uint8")
+    _ok(_load().csa_quant_fp8_window_rows(_ptr(x), rows, _ptr(out), _stream(stream)), "csa_quant_fp8_window_rows")
 
 
 def kv_compress(p: Params, kv, z, kI_raw, rope_tab, C, KI, kv_rope, stream=None):
@@ -296,12 +316,13 @@ def csa_selftest_wait_timeout(limit_ns: int, stream=None):
 # ---------------------------------------------------------------------------------------
 
 def make_params(*, B, L, H, m, topk=0, n_win=128, H_I=8, d_I=64, d=128, d_rope=64, scale=None,
-                act="bf16", kv="bf16", idx="fp8", rope_len=None) -> Params:
+                act="bf16", kv="bf16", idx="fp8", rope_len=None, win=None) -> Params:
+    """win: the decode ring's dtype, the activation dtype (default) or "fp8"."""
     ncap = -(-L // m)
     if rope_len is None:
         rope_len = max(L, ncap * m)
     return Params(B, L, H, d, d_rope, m, topk, n_win, H_I, d_I, float(d ** -0.5 if scale is None else scale),
-                  _DT[act], _DT[kv], _DT[idx], rope_len)
+                  _DT[act], _DT[kv], _DT[idx], rope_len, _DT[act if win is None else win])
 
 
 def torch_dtype(name: str):
@@ -315,8 +336,19 @@ def alloc_entries(p: Params, device="cuda"):
         return (torch.empty((p.B, ncap, p.d - p.d_rope), dtype=torch.uint8, device=device),
                 torch.empty((p.B, ncap, p.d_rope), dtype=torch.bfloat16, device=device),
                 torch.empty((p.B, ncap), dtype=torch.float32, device=device))
+    if p.kv_t == NVFP4:
+        return (torch.empty((p.B, ncap, NVFP4_ROW_BYTES), dtype=torch.uint8, device=device), None, None)
     dt = torch.float32 if p.kv_t == F32 else torch.bfloat16
     return (torch.empty((p.B, ncap, p.d), dtype=dt, device=device), None, None)
+
+
+def alloc_ring(p: Params, device="cuda") -> torch.Tensor:
+    """The decode SWA ring per p.win_t: [B, n_win, d] in the activation dtype, or FP8 rows
+    [B, n_win, 144] uint8."""
+    if p.win_t == FP8E4M3:
+        return torch.zeros((p.B, p.n_win, FP8_WIN_ROW_BYTES), dtype=torch.uint8, device=device)
+    dt = torch.float32 if p.act_t == F32 else torch.bfloat16
+    return torch.zeros((p.B, p.n_win, p.d), dtype=dt, device=device)
 
 
 def alloc_index_rows(p: Params, rows_shape, device="cuda"):

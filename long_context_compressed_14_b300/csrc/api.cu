@@ -56,8 +56,12 @@ int check(const csa_params *p, int op) {
     if (p->H > 64) return CSA_ERR_UNSUPPORTED;
     if (p->m > 1024) return CSA_ERR_UNSUPPORTED;
     if (p->act_t != CSA_F32 && p->act_t != CSA_BF16) return CSA_ERR_INVALID;
-    if (p->kv_t != CSA_F32 && p->kv_t != CSA_BF16 && p->kv_t != CSA_MIXED) return CSA_ERR_INVALID;
+    if (p->kv_t != CSA_F32 && p->kv_t != CSA_BF16 && p->kv_t != CSA_MIXED && p->kv_t != CSA_NVFP4)
+        return CSA_ERR_INVALID;
     if (p->kv_t == CSA_MIXED && p->d_rope != 64) return CSA_ERR_INVALID;
+    if (p->win_t != p->act_t && p->win_t != CSA_FP8E4M3) return CSA_ERR_INVALID;
+    // the NVFP4 entries and the FP8 ring are read by the tensor-core (BF16) kernels only
+    if ((p->kv_t == CSA_NVFP4 || p->win_t == CSA_FP8E4M3) && p->act_t != CSA_BF16) return CSA_ERR_UNSUPPORTED;
     if ((int64_t)p->B * p->L > ((int64_t)1 << 40)) return CSA_ERR_UNSUPPORTED;
     if (p->d_rope > 0) {
         // positions used: raw rows < L, entries at (j+1)m-1 < ceil(L/m)*m
@@ -76,9 +80,9 @@ int check(const csa_params *p, int op) {
     return CSA_OK;
 }
 
-// Bytes of the entries widened to BF16 (prefill with mixed-precision entries).
+// Bytes of the entries widened to BF16 (prefill with MIXED or NVFP4 entries).
 size_t widen_bytes(const csa_params *p) {
-    return p->kv_t == CSA_MIXED ? align_up((size_t)p->B * (size_t)ncap_of(p) * kD * 2) : 0;
+    return (p->kv_t == CSA_MIXED || p->kv_t == CSA_NVFP4) ? align_up((size_t)p->B * (size_t)ncap_of(p) * kD * 2) : 0;
 }
 
 // Bytes of the exact FP8 form of `rows` MXFP4 indexer rows (codes + one float scale per row).
@@ -235,7 +239,7 @@ AttnArgs attn_args(const csa_params *p, const void *q, const void *kvr, const cs
     a.lse = lse;
     a.B = p->B; a.L = p->L; a.H = p->H; a.m = p->m; a.topk = topk; a.n_win = p->n_win;
     a.d_rope = p->d_rope; a.ncap = (int)ncap_of(p); a.scale = p->scale;
-    a.decode = decode; a.act_t = p->act_t; a.kv_t = p->kv_t;
+    a.decode = decode; a.act_t = p->act_t; a.kv_t = p->kv_t; a.win_t = p->win_t;
     return a;
 }
 
@@ -294,7 +298,7 @@ const char *csa_strerror(int s) {
     }
 }
 
-int csa_version(void) { return 100; }
+int csa_version(void) { return 110; }
 
 int csa_check_params(const csa_params *p, int op) { return check(p, op); }
 
@@ -315,6 +319,18 @@ int csa_quant_mxfp4_rows(const float *x, int64_t rows, int cols, uint8_t *codes,
                          csa_stream_t stream) {
     if (!x || !codes || !e8 || rows < 0 || cols != kDI) return CSA_ERR_INVALID;
     launch_quant_mxfp4(x, rows, codes, e8, cs(stream));
+    return launch_status();
+}
+
+int csa_quant_nvfp4_entries(const float *x, int64_t rows, uint8_t *out, csa_stream_t stream) {
+    if (!x || !out || rows < 0 || !aligned16(out)) return CSA_ERR_INVALID;
+    launch_quant_nvfp4_entries(x, rows, out, cs(stream));
+    return launch_status();
+}
+
+int csa_quant_fp8_window_rows(const float *x, int64_t rows, uint8_t *out, csa_stream_t stream) {
+    if (!x || !out || rows < 0 || !aligned16(out)) return CSA_ERR_INVALID;
+    launch_quant_fp8_window(x, rows, out, cs(stream));
     return launch_status();
 }
 
@@ -370,7 +386,7 @@ int kv_append(const csa_params *p, const void *kv_new, const float *z_new, const
     a.ki_data = kI_new ? KI->data : nullptr; a.ki_scale = kI_new ? KI->scale : nullptr;
     a.ki_e8 = kI_new ? KI->mx_scale : nullptr;
     a.B = p->B; a.L = p->L; a.m = p->m; a.ncap = (int)ncap_of(p); a.n_win = p->n_win; a.d_rope = p->d_rope;
-    a.act_t = p->act_t; a.kv_t = p->kv_t; a.idx_t = p->idx_t;
+    a.act_t = p->act_t; a.kv_t = p->kv_t; a.idx_t = p->idx_t; a.win_t = p->win_t;
     launch_kv_append(a, cs(stream));
     return launch_status();
 }

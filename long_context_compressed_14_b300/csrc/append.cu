@@ -7,10 +7,11 @@
 // the recent raw tokens, whose incomplete block waits there, and the compressed KV cache) and
 // 提案手法 §1 (overlapping compression: entry j averages the raw rows of blocks j-1 and j with
 // softmax weights; sliding window of the last n_win raw tokens; partial RoPE); [P5] "deepseek V4
-// 技术论文" 一.1 (C^b overlaps C^a).
+// 技术论文" 一.1 (C^b overlaps C^a); [P3] "Технический отчёт DeepSeek-V4.1-Flash — часть 2/2"
+// (the V4.1 variant: entries in NVFP4 quantised after RoPE, the window cache in FP8).
 //
 // One CTA of 128 threads per sequence, thread = head dimension. For the new token at position u:
-//   ring[u mod n_win]   = its raw row rotated at u (the window keys);
+//   ring[u mod n_win]   = its raw row rotated at u (the window keys), in act_t or as an FP8 row;
 //   state[u mod 2m]     = its raw row, its compression logits z and its raw indexer key (the last
 //                         2m tokens: exactly the window rows [u - 2m + 1, u] an entry needs);
 //   if u = (j+1)m - 1   entry j = sum_t alpha_t kv[t] over t in [(j-1)m, (j+1)m) ∩ [0, u], alpha =
@@ -28,6 +29,7 @@ namespace csa {
 template <typename ActT, int KV_T, int IDX_T>
 __global__ void __launch_bounds__(128) kv_append_kernel(AppendArgs a) {
     __shared__ float s_x[kD];       // the new raw row / the entry before storage
+    __shared__ float s_y[kD];       // a rotated row gathered for a warp's row quantiser
     __shared__ float s_w[2 * 1024]; // window weights
     __shared__ float s_red[8];
     const int b = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
@@ -55,7 +57,17 @@ __global__ void __launch_bounds__(128) kv_append_kernel(AppendArgs a) {
         const float x0 = s_x[64 + i], x1 = s_x[96 + i];
         y = d < 96 ? x0 * cs.x - x1 * cs.y : x0 * cs.y + x1 * cs.x;
     }
-    reinterpret_cast<ActT *>(a.ring)[((int64_t)b * a.n_win + u % a.n_win) * kD + d] = from_f<ActT>(y);
+    const int64_t slot = (int64_t)b * a.n_win + u % a.n_win;
+    if (a.win_t == CSA_FP8E4M3) {  // an FP8 ring row (fp4.cuh): warp 0 quantises the whole row
+        s_y[d] = y;
+        __syncthreads();
+        if (warp == 0) {
+            const float r[4] = {s_y[lane], s_y[32 + lane], s_y[64 + lane], s_y[96 + lane]};
+            fp8win_row_store(r, reinterpret_cast<uint8_t *>(a.ring) + slot * kFp8WinRowBytes);
+        }
+    } else {
+        reinterpret_cast<ActT *>(a.ring)[slot * kD + d] = from_f<ActT>(y);
+    }
     if ((u + 1) % m != 0) return;  // the token does not complete a block
 
     // 2. the token completes block j: entry j from the window rows held in the state cache
@@ -110,6 +122,13 @@ __global__ void __launch_bounds__(128) kv_append_kernel(AppendArgs a) {
         reinterpret_cast<float *>(a.c_data)[row * kD + d] = c;
     } else if (KV_T == CSA_BF16) {
         reinterpret_cast<__nv_bfloat16 *>(a.c_data)[row * kD + d] = __float2bfloat16_rn(c);
+    } else if (KV_T == CSA_NVFP4) {  // the rotated entry in NVFP4 (fp4.cuh), stored by warp 0
+        s_y[d] = c;
+        __syncthreads();
+        if (warp == 0) {
+            const float r[4] = {s_y[lane], s_y[32 + lane], s_y[64 + lane], s_y[96 + lane]};
+            nvfp4_row_store(r, reinterpret_cast<uint8_t *>(a.c_data) + row * kNvfp4RowBytes);
+        }
     } else {  // MIXED: dims 0..63 FP8 with one scale, dims 64..127 BF16
         const float am = warp_max(d < 64 ? fabsf(c) : 0.0f);
         if (lane == 0) s_red[warp] = am;
@@ -159,6 +178,7 @@ template <typename ActT>
 static void launch_append_a(const AppendArgs &a, cudaStream_t st) {
     if (a.kv_t == CSA_F32) launch_append_k<ActT, CSA_F32>(a, st);
     else if (a.kv_t == CSA_BF16) launch_append_k<ActT, CSA_BF16>(a, st);
+    else if (a.kv_t == CSA_NVFP4) launch_append_k<ActT, CSA_NVFP4>(a, st);
     else launch_append_k<ActT, CSA_MIXED>(a, st);
 }
 

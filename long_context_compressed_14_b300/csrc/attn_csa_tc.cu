@@ -4,7 +4,8 @@
 // (wiki notes), 提案手法 §1 (CSA: each query attends to its top-k compressed entries;
 // shared-KV multi-query attention; sliding-window branch n_win = 128; attention sink;
 // partial RoPE + inverse RoPE on the core output) and 訓練インフラの革新 §5 (mixed-precision
-// entries); [P5] "deepseek V4 技术论文" 一.1 (an entry is both key and value).
+// entries); [P5] "deepseek V4 技术论文" 一.1 (an entry is both key and value); [P3] "Технический
+// отчёт DeepSeek-V4.1-Flash — часть 2/2" (the V4.1 variant: NVFP4 entries, an FP8 window cache).
 //
 // Every token has its own key list: its top-k entries (ascending, gathered by index) followed
 // by the 128 raw rows of its window. All 64 heads of a token share that list, so the kernel
@@ -27,17 +28,20 @@
 //   warps 0-7   softmax and epilogue (two warpgroups; TMEM lanes 0-127 each);
 //   warp 8      MMA issue (one thread);
 //   warps 9-11  producers: query rows by TMA + RoPE, top-k row by bulk copy, key tiles gathered
-//               with cp.async (decode with mixed entries: the FP8 half widened to BF16 by the
-//               threads), the window tile by TMA (prefill) or gathered from the ring (decode).
+//               with cp.async, the window tile by TMA (prefill) or gathered from the ring
+//               (decode). Decode tiles stored in a low-precision form (MIXED or NVFP4 entries,
+//               an FP8 ring) are widened to BF16 by the producer threads: each thread loads a
+//               group of its chunks, then converts and stores them.
 // Pipelines: key tiles in a 3-buffer ring, S^T and O^T double-buffered in TMEM (O^T by token),
 // P^T double-buffered in shared memory, query rows double-buffered; every wait is bounded.
 // Epilogue: O^T is normalised per head, the RoPE half is rotated back (the two dims of a pair
 // live in different warps and meet in shared memory), staged as BF16 [head][dim] and written
 // with one 16 KB bulk copy per token.
 //
-// Prefill with mixed-precision entries first widens every entry to BF16 once (code * row
-// scale, rounded to nearest even) into caller workspace; the gather then reads BF16 rows.
+// Prefill with MIXED or NVFP4 entries first widens every entry to BF16 once (the dequantised
+// value rounded to nearest even) into caller workspace; the gather then reads BF16 rows.
 #include "common.cuh"
+#include "fp4.cuh"
 #include "kernels.cuh"
 #include "tma_host.cuh"
 #include "umma.cuh"
@@ -54,6 +58,7 @@ constexpr int kThreads = kProd0 + kProducers; // 384
 constexpr int kH = 64;                        // heads (N of both MMAs)
 constexpr int kTile = 128;                    // keys per tile
 constexpr int kGatherPer = 22;                // 16-byte chunks of a key tile per producer thread
+constexpr int kConvBatch = 8;                 // converted chunks whose loads are in flight together
 // Shared memory (1024-aligned), for NB key-tile buffers:
 //   Q       2 buffers x 16 KB (two 64-dim halves of 8 KB)
 //   keys    NB x 32 KB (two 64-dim halves of 16 KB)
@@ -80,14 +85,16 @@ struct CsaTcParams {
     const void *c_data;
     const __nv_bfloat16 *c_rope;
     const float *c_scale;
-    const __nv_bfloat16 *win;   // decode: ring [B][n_win][128]
+    const void *win;            // decode: ring [B][n_win][128] BF16, or [B][n_win] FP8 rows (win8)
     const int32_t *idx;         // [rows][topk]
     const int32_t *ctx;         // decode: [B]
     const float *sink;
     const float2 *rope;
     __nv_bfloat16 *out;
     float *lse;
-    int B, L, ncap, topk, n_win, d_rope, mixed, decode, rows;
+    int B, L, ncap, topk, n_win, d_rope, decode, rows;
+    int ent;        // entry storage read by the gather: 0 BF16, 1 MIXED, 2 NVFP4 (decode only)
+    int win8;       // decode: the ring holds FP8 rows
     int dense, m;   // dense: keys are entries 0 .. visible(t) - 1 in order (no top-k row)
     float scale_log2;
     // split-KV decode: work item r = (sequence r / S, split r % S) takes the key tiles
@@ -111,9 +118,52 @@ struct TokenMeta {
     int pos_ok;  // 0: a decode position outside the cache (nothing is stored)
 };
 
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
+__device__ __forceinline__ uint32_t pack2(float a, float b) { return bf16x2_bits(a, b); }
+
+// One 16-byte chunk (8 dims) of a key row as loaded from a low-precision store, widened to BF16
+// when it is written to the key tile.
+enum : int { kChZero = 0, kChBf16 = 1, kChFp8 = 2, kChFp4 = 3 };
+struct RawChunk {
+    uint4 v;   // BF16: the chunk; FP8: codes in v.x, v.y; FP4: codes in v.x, block-scale code in v.y
+    float s;   // row scale (FP8, FP4)
+    int kind;
+};
+
+__device__ __forceinline__ uint4 widen_chunk(const RawChunk &r) {
+    if (r.kind == kChBf16) return r.v;
+    if (r.kind == kChFp8) return fp8x8_to_bf16(r.v.x, r.v.y, r.s);
+    if (r.kind == kChFp4) return fp4x8_to_bf16(r.v.x, r.v.y, r.s);
+    return make_uint4(0, 0, 0, 0);
+}
+
+// chunk ch of entry row er: MIXED (ent 1) or NVFP4 (ent 2)
+__device__ __forceinline__ void load_entry_chunk(const CsaTcParams &P, int64_t er, int ch, RawChunk &r) {
+    if (P.ent == 2) {
+        const uint8_t *row = reinterpret_cast<const uint8_t *>(P.c_data) + er * kNvfp4RowBytes;
+        r.v.x = __ldg(reinterpret_cast<const uint32_t *>(row) + ch);
+        r.v.y = __ldg(row + 64 + (ch >> 1));
+        r.s = __ldg(reinterpret_cast<const float *>(row + 72));
+        r.kind = kChFp4;
+    } else if (ch >= 8) {
+        r.v = __ldg(reinterpret_cast<const uint4 *>(P.c_rope + er * 64 + (ch - 8) * 8));
+        r.kind = kChBf16;
+    } else {
+        const uint2 c = __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const uint8_t *>(P.c_data) + er * 64) + ch);
+        r.v.x = c.x;
+        r.v.y = c.y;
+        r.s = __ldg(P.c_scale + er);
+        r.kind = kChFp8;
+    }
+}
+
+// chunk ch of FP8 ring row `slot` (of all sequences' rows)
+__device__ __forceinline__ void load_win8_chunk(const CsaTcParams &P, int64_t slot, int ch, RawChunk &r) {
+    const uint8_t *row = reinterpret_cast<const uint8_t *>(P.win) + slot * kFp8WinRowBytes;
+    const uint2 c = __ldg(reinterpret_cast<const uint2 *>(row) + ch);
+    r.v.x = c.x;
+    r.v.y = c.y;
+    r.s = __ldg(reinterpret_cast<const float *>(row + 128));
+    r.kind = kChFp8;
 }
 
 // bulk copy shared -> global (both 16-byte aligned, size a multiple of 16), bulk-group tracked
@@ -344,7 +394,7 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 uint8_t *kbuf = sm + kKOff + kb * 32768;
                 const uint32_t kbuf_s = s_base + kKOff + kb * 32768;
                 const uint32_t kf = smem_u32(&b_kfull[kb]);
-                if (c < mt.n_ct && !P.mixed) {
+                if (c < mt.n_ct && P.ent == 0) {
                     // gathered BF16 rows; an invalid slot reads nothing and is zero-filled (its
                     // weight is masked to 0 by the softmax). 96 threads: thread = chunk ch of keys
                     // i0 + 6q; all indices are read first so that the copies issue back to back.
@@ -374,43 +424,41 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         }
                     }
                     cp_async_mbar_arrive(kf);
-                } else if (c < mt.n_ct) {
-                    // decode with mixed entries: the FP8 half is widened by the threads
-                    for (int u = ptid; u < kTile * 16; u += kProducers) {
-                        const int i = u >> 4, ch = u & 15;
-                        const int pos = c * kTile + i;
-                        const uint32_t off = (ch >> 3) * 16384 + sw128_off(i, ch & 7);
-                        int j = pos < mt.n_sel ? (P.dense ? pos : sidx[pos]) : -1;
-                        if (j >= P.ncap) {
-                            set_status(CSA_ERR_BOUNDS);
-                            j = -1;
-                        }
-                        if (j < 0) {
-                            *reinterpret_cast<uint4 *>(kbuf + off) = make_uint4(0, 0, 0, 0);
-                            continue;
-                        }
-                        const int64_t er = (int64_t)mt.b * P.ncap + j;
-                        if (ch >= 8) {
-                            cp_async16(kbuf_s + off, P.c_rope + er * 64 + (ch - 8) * 8);
-                        } else {
-                            const uint2 codes = *reinterpret_cast<const uint2 *>(
-                                reinterpret_cast<const uint8_t *>(P.c_data) + er * 64 + ch * 8);
-                            const float sc = P.c_scale[er];
-                            const uint32_t cw[2] = {codes.x, codes.y};
-                            uint32_t pk[4];
+                } else if (c < mt.n_ct || P.win8) {
+                    // decode tiles in a low-precision store (MIXED / NVFP4 entries, an FP8 ring):
+                    // widened by the threads; chunk u = ptid + 96 q (the BF16 gather's mapping),
+                    // the loads of kConvBatch chunks issued before any is converted
+                    const bool ents = c < mt.n_ct;
+                    bool bad = false;
+                    for (int q0 = 0; q0 < kGatherPer; q0 += kConvBatch) {
+                        RawChunk r[kConvBatch];
 #pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2)
+                        for (int q = 0; q < kConvBatch; ++q) {
+                            const int u = ptid + kProducers * (q0 + q);
+                            r[q].kind = kChZero;
+                            if (q0 + q >= kGatherPer || u >= kTile * 16) continue;
+                            const int i = u >> 4, ch = u & 15;
+                            if (ents) {
+                                const int pos = c * kTile + i;
+                                const int j = pos < mt.n_sel ? (P.dense ? pos : sidx[pos]) : -1;
+                                bad |= j >= P.ncap;
+                                if (j >= 0 && j < P.ncap) load_entry_chunk(P, (int64_t)mt.b * P.ncap + j, ch, r[q]);
+                            } else {
+                                const int uu = mt.t - kTile + 1 + i;  // position of window row i
+                                if (!(uu < 0 || uu <= mt.t - mt.n_win_t))
+                                    load_win8_chunk(P, (int64_t)mt.b * P.n_win + uu % P.n_win, ch, r[q]);
+                            }
+                        }
 #pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const uint16_t two = (uint16_t)(cw[h2] >> (16 * e));
-                                    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-                                    const float2 f = __half22float2(__half2(hr));
-                                    pk[2 * h2 + e] = pack2(f.x * sc, f.y * sc);
-                                }
-                            *reinterpret_cast<uint4 *>(kbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        for (int q = 0; q < kConvBatch; ++q) {
+                            const int u = ptid + kProducers * (q0 + q);
+                            if (q0 + q >= kGatherPer || u >= kTile * 16) continue;
+                            const int i = u >> 4, ch = u & 15;
+                            *reinterpret_cast<uint4 *>(kbuf + (ch >> 3) * 16384 + sw128_off(i, ch & 7)) =
+                                widen_chunk(r[q]);
                         }
                     }
-                    cp_async_wait_all();
+                    if (bad) set_status(CSA_ERR_BOUNDS);
                     fence_async_smem();
                     mbar_arrive(kf);
                 } else if (!P.decode) {
@@ -429,7 +477,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                         const bool have = !(uu < 0 || uu <= mt.t - mt.n_win_t);
                         const int64_t slot = have ? (uu % P.n_win) : 0;
                         cp_async16_zfill(kbuf_s + (ch >> 3) * 16384 + sw128_off(i, ch & 7),
-                                         P.win + ((int64_t)mt.b * P.n_win + slot) * 128 + ch * 8, have ? 16u : 0u);
+                                         reinterpret_cast<const __nv_bfloat16 *>(P.win) +
+                                             ((int64_t)mt.b * P.n_win + slot) * 128 + ch * 8,
+                                         have ? 16u : 0u);
                     }
                     cp_async_mbar_arrive(kf);
                 }
@@ -739,57 +789,52 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Mixed-precision entries widened to BF16 rows: dims [0, 64) = code * row scale (rounded to
-// nearest even), dims [64, 128) copied. Thread = one 16-byte output chunk.
-__global__ void widen_mixed_kernel(const uint8_t *__restrict__ codes, const __nv_bfloat16 *__restrict__ rope,
-                                   const float *__restrict__ scale, int64_t rows, __nv_bfloat16 *__restrict__ out) {
+// MIXED or NVFP4 entries widened to BF16 rows (the dequantised value rounded to nearest even):
+// MIXED dims [0, 64) = code * row scale, dims [64, 128) copied; NVFP4 every dim = E2M1 * block
+// scale. Thread = one 16-byte output chunk.
+__global__ void widen_entries_kernel(const uint8_t *__restrict__ codes, const __nv_bfloat16 *__restrict__ rope,
+                                     const float *__restrict__ scale, int64_t rows, int nvfp4,
+                                     __nv_bfloat16 *__restrict__ out) {
     const int64_t n = rows * 16;
     for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < n; u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = u >> 4;
         const int ch = (int)(u & 15);
         uint4 v;
-        if (ch >= 8) {
+        if (nvfp4) {
+            const uint8_t *row = codes + r * kNvfp4RowBytes;
+            v = fp4x8_to_bf16(reinterpret_cast<const uint32_t *>(row)[ch], row[64 + (ch >> 1)],
+                              *reinterpret_cast<const float *>(row + 72));
+        } else if (ch >= 8) {
             v = *reinterpret_cast<const uint4 *>(rope + r * 64 + (ch - 8) * 8);
         } else {
             const uint2 cw = *reinterpret_cast<const uint2 *>(codes + r * 64 + ch * 8);
-            const float sc = scale[r];
-            const uint32_t w2[2] = {cw.x, cw.y};
-            uint32_t pk[4];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint16_t two = (uint16_t)(w2[h2] >> (16 * e));
-                    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-                    const float2 f = __half22float2(__half2(hr));
-                    pk[2 * h2 + e] = pack2(f.x * sc, f.y * sc);
-                }
-            v = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            v = fp8x8_to_bf16(cw.x, cw.y, scale[r]);
         }
         *reinterpret_cast<uint4 *>(out + r * 128 + ch * 8) = v;
     }
 }
 
 size_t csa_widen_bytes(const AttnArgs &a) {
-    return (a.kv_t == CSA_MIXED && !a.decode) ? (size_t)a.B * (size_t)a.ncap * 128 * 2 : 0;
+    return ((a.kv_t == CSA_MIXED || a.kv_t == CSA_NVFP4) && !a.decode) ? (size_t)a.B * (size_t)a.ncap * 128 * 2 : 0;
 }
 
-const void *launch_widen_mixed(const AttnArgs &a, cudaStream_t st) {
+const void *launch_widen_entries(const AttnArgs &a, cudaStream_t st) {
     const int64_t erows = (int64_t)a.B * a.ncap;
     __nv_bfloat16 *wide = reinterpret_cast<__nv_bfloat16 *>(a.ws);
     int blocks = (int)ceil_div64(erows * 16, 256);
     if (blocks > 148 * 8) blocks = 148 * 8;
     if (blocks < 1) blocks = 1;
-    widen_mixed_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint8_t *>(a.c_data),
-                                              reinterpret_cast<const __nv_bfloat16 *>(a.c_rope), a.c_scale, erows,
-                                              wide);
+    widen_entries_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint8_t *>(a.c_data),
+                                                reinterpret_cast<const __nv_bfloat16 *>(a.c_rope), a.c_scale, erows,
+                                                a.kv_t == CSA_NVFP4 ? 1 : 0, wide);
     count_launches(1);
     return wide;
 }
 
 bool csa_tc_supported(const AttnArgs &a) {
     if (a.act_t != CSA_BF16) return false;
-    if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED) return false;
+    if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED && a.kv_t != CSA_NVFP4) return false;
+    if (a.decode && a.win_t != CSA_BF16 && a.win_t != CSA_FP8E4M3) return false;
     if (a.H != csa_tc::kH || a.n_win != 128) return false;
     if (!a.dense && (a.topk < 4 || a.topk > kMaxTopk || a.topk % 4 != 0)) return false;
     if (a.dense && !a.decode && a.ncap != 0) return false;  // prefill: dense only as window-only (no entries)
@@ -817,15 +862,16 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     P.c_data = a.c_data;
     P.c_rope = reinterpret_cast<const __nv_bfloat16 *>(a.c_rope);
     P.c_scale = a.c_scale;
-    P.mixed = a.kv_t == CSA_MIXED;
-    if (P.mixed && !a.decode && a.ncap > 0) {
-        // widen every entry once; the attention then gathers BF16 rows
-        P.c_data = launch_widen_mixed(a, st);
+    P.ent = a.kv_t == CSA_MIXED ? 1 : (a.kv_t == CSA_NVFP4 ? 2 : 0);
+    if (P.ent != 0 && !a.decode) {
+        // prefill: widen every entry once; the attention then gathers BF16 rows
+        if (a.ncap > 0) P.c_data = launch_widen_entries(a, st);
         P.c_rope = nullptr;
         P.c_scale = nullptr;
-        P.mixed = 0;
+        P.ent = 0;
     }
-    P.win = a.decode ? reinterpret_cast<const __nv_bfloat16 *>(a.kv_rope) : nullptr;
+    P.win = a.decode ? a.kv_rope : nullptr;
+    P.win8 = a.decode && a.win_t == CSA_FP8E4M3 ? 1 : 0;
     P.idx = a.idx;
     P.ctx = a.ctx;
     P.sink = a.sink;

@@ -4,7 +4,8 @@
 // (wiki notes), 提案手法 §1 (HCA: m' = 128 compression, no sparse selection, dense attention
 // over the compressed entries; shared-KV MQA; sliding-window branch n_win = 128; attention
 // sink; partial RoPE with inverse RoPE on the output) and 訓練インフラの革新 §5 (mixed-precision
-// entries); [P5] "deepseek V4 技术论文" 一.1 (an entry is both key and value).
+// entries); [P5] "deepseek V4 技术论文" 一.1 (an entry is both key and value); [P3] "Технический
+// отчёт DeepSeek-V4.1-Flash — часть 2/2" (NVFP4 entries).
 //
 // Every query head shares the one KV head, so a work item stacks T = 128 / H consecutive tokens
 // x H heads into M = 128 query rows (row r = token t0 + r / H, head r % H) and walks one key
@@ -26,7 +27,7 @@
 // tile's P V while the softmax works on this one; a slot is rewritten by S(n + 2) only after
 // P V(n) has read it, which the in-order tensor pipe guarantees (P V(n) is issued first). Key
 // tiles flow through four buffers; query rows are double-buffered and fetched one item ahead.
-// Mixed-precision entries are widened to BF16 once per call (caller workspace) before this
+// MIXED and NVFP4 entries are widened to BF16 once per call (caller workspace) before this
 // kernel runs. Every wait is bounded, and every TMEM access and every wait whose result guards
 // one sits in a warp-uniform branch (tcgen05.ld / st are .sync.aligned).
 #include "common.cuh"
@@ -504,11 +505,11 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Host: returns false when the configuration is outside what this kernel handles (the caller
-// then uses the CUDA-core kernel).
+// Host: returns false when the configuration is outside what this kernel handles (the call is
+// then refused as unsupported).
 bool hca_tc_supported(const AttnArgs &a) {
     if (a.decode || a.act_t != CSA_BF16) return false;
-    if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED) return false;
+    if (a.kv_t != CSA_BF16 && a.kv_t != CSA_MIXED && a.kv_t != CSA_NVFP4) return false;
     if (a.H != 16 && a.H != 32 && a.H != 64 && a.H != 128) return false;
     if (a.n_win != 128) return false;
     if (128 / a.H + a.n_win - 1 > hca_tc::kMaxKeys) return false;
@@ -524,8 +525,8 @@ bool launch_hca_tc(const AttnArgs &a, cudaStream_t st) {
     HcaTcParams P;
     memset(&P, 0, sizeof(P));
     const uint64_t L = a.L, H = a.H, B = a.B, ncap = a.ncap;
-    const void *entries = a.c_data;
-    if (a.kv_t == CSA_MIXED) entries = launch_widen_mixed(a, st);
+    const bool widen = a.kv_t == CSA_MIXED || a.kv_t == CSA_NVFP4;  // entries widened to BF16 into a.ws
+    const void *entries = widen ? a.ws : a.c_data;
     bool ok = make_map_3d(&P.mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, 128, L * H, B, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map_3d(&P.mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, entries, 128, ncap, B, 64, 128,
@@ -533,6 +534,7 @@ bool launch_hca_tc(const AttnArgs &a, cudaStream_t st) {
     ok = ok && make_map_3d(&P.mkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kv_rope, 128, L, B, 64, kMaxKeys,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return false;
+    if (widen && a.ncap > 0) launch_widen_entries(a, st);
     P.sink = a.sink;
     P.rope = reinterpret_cast<const float2 *>(a.rope_tab);
     P.out = reinterpret_cast<__nv_bfloat16 *>(a.out);

@@ -4,7 +4,8 @@
 // (wiki notes), 提案手法 §1 (CSA: weighted-average compression of every m = 4 tokens with
 // overlap between adjacent blocks; HCA: m' = 128; partial RoPE on the last 64 dims) and
 // 訓練インフラの革新 §5 (KV entries: RoPE dims BF16, other dims FP8); [P5] "deepseek V4
-// 技术论文" 一.1 (C^b overlaps C^a).
+// 技术论文" 一.1 (C^b overlaps C^a); [P3] "Технический отчёт DeepSeek-V4.1-Flash — часть 2/2"
+// (the V4.1 variant: entries in NVFP4, quantised after RoPE).
 #include "common.cuh"
 #include "fp4.cuh"
 #include "kernels.cuh"
@@ -182,6 +183,8 @@ kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
         __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(c_data) + row * kD;
 #pragma unroll
         for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(c[e]);
+    } else if (KV_T == CSA_NVFP4) {  // the whole rotated entry in NVFP4 (fp4.cuh)
+        nvfp4_row_store(c, reinterpret_cast<uint8_t *>(c_data) + row * kNvfp4RowBytes);
     } else {  // MIXED: dims 0..63 FP8 + row scale, dims 64..127 BF16
         float amax = warp_max(fmaxf(fabsf(c[0]), fabsf(c[1])));
         const float scale = __fdiv_rn(amax, 448.0f);
@@ -243,6 +246,7 @@ template <typename ActT>
 static void launch_compress_a(const CompressArgs &a, cudaStream_t st) {
     if (a.kv_t == CSA_F32) launch_compress_k<ActT, CSA_F32>(a, st);
     else if (a.kv_t == CSA_BF16) launch_compress_k<ActT, CSA_BF16>(a, st);
+    else if (a.kv_t == CSA_NVFP4) launch_compress_k<ActT, CSA_NVFP4>(a, st);
     else launch_compress_k<ActT, CSA_MIXED>(a, st);
 }
 

@@ -1,5 +1,7 @@
 // fp4.cu -- FP4 (E2M1) rows for the lightning indexer: MXFP4 quantisation and the lossless
-// dequantisation to FP8 E4M3 rows that lets the FP8 tensor-core indexer consume them.
+// dequantisation to FP8 E4M3 rows that lets the FP8 tensor-core indexer consume them; and the
+// quantisers of the low-precision caches: NVFP4 entry rows and FP8 window rows (formats in
+// fp4.cuh).
 //
 // Sources: [P2] "DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence"
 // (wiki notes), 事後学習 §3 (the CSA indexer's QK path is quantised to FP4 (MXFP4); the FP4 to
@@ -49,6 +51,25 @@ __global__ void mxfp4_to_fp8_kernel(const uint8_t *__restrict__ codes, const uin
     }
 }
 
+// NVFP4 entry rows and FP8 window rows of 128-dim float rows: one warp per row (fp4.cuh)
+__global__ void quant_nvfp4_kernel(const float *__restrict__ x, int64_t rows, uint8_t *__restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const float c[4] = {x[r * kD + lane], x[r * kD + 32 + lane], x[r * kD + 64 + lane], x[r * kD + 96 + lane]};
+        nvfp4_row_store(c, out + r * kNvfp4RowBytes);
+    }
+}
+
+__global__ void quant_fp8win_kernel(const float *__restrict__ x, int64_t rows, uint8_t *__restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const float c[4] = {x[r * kD + lane], x[r * kD + 32 + lane], x[r * kD + 64 + lane], x[r * kD + 96 + lane]};
+        fp8win_row_store(c, out + r * kFp8WinRowBytes);
+    }
+}
+
 static int blocks_for(int64_t rows) {
     int64_t b = (rows + 7) / 8;
     if (b > 148 * 32) b = 148 * 32;
@@ -65,6 +86,18 @@ void launch_mxfp4_to_fp8(const uint8_t *codes, const uint8_t *e8, int64_t rows, 
                          cudaStream_t st) {
     if (rows <= 0) return;
     mxfp4_to_fp8_kernel<<<blocks_for(rows), 256, 0, st>>>(codes, e8, rows, out, out_scale);
+    count_launches(1);
+}
+
+void launch_quant_nvfp4_entries(const float *x, int64_t rows, uint8_t *out, cudaStream_t st) {
+    if (rows <= 0) return;
+    quant_nvfp4_kernel<<<blocks_for(rows), 256, 0, st>>>(x, rows, out);
+    count_launches(1);
+}
+
+void launch_quant_fp8_window(const float *x, int64_t rows, uint8_t *out, cudaStream_t st) {
+    if (rows <= 0) return;
+    quant_fp8win_kernel<<<blocks_for(rows), 256, 0, st>>>(x, rows, out);
     count_launches(1);
 }
 

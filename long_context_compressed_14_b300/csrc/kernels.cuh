@@ -63,11 +63,12 @@ struct AttnArgs {
     const float *rope_tab; // [rope_len, half, 2]
     void *out;
     float *lse;
-    void *ws;              // prefill with mixed entries: room for the entries widened to BF16
+    void *ws;              // prefill with MIXED / NVFP4 entries: room for the entries widened to BF16
     size_t ws_bytes;
     int B, L, H, m, topk, n_win, d_rope, ncap;
     float scale;
     int decode, act_t, kv_t;
+    int win_t;             // decode ring: act_t rows, or FP8 rows of 144 bytes (CSA_FP8E4M3)
     int dense;             // 1: the key list is every visible entry in order (HCA decode), no idx
     // split-KV decode (0 = off): S work items per sequence, T key tiles per item; partial results
     // in part_o [B*S, H, 128] float and part_ml [B*S, H] (max, sum), merged by the combine step
@@ -103,7 +104,7 @@ struct AppendArgs {
     const float *kI_new;   // [B, d_I] or NULL
     const int32_t *ctx;    // [B]: tokens including the new one
     const float *rope_tab;
-    void *ring;            // [B, n_win, d] act_t
+    void *ring;            // [B, n_win, d] act_t, or [B, n_win, 144] bytes of FP8 rows (win_t)
     void *state_kv;        // [B, 2m, d] act_t
     float *state_z;        // [B, 2m, 2]
     float *state_kI;       // [B, 2m, d_I]
@@ -113,7 +114,7 @@ struct AppendArgs {
     void *ki_data;
     float *ki_scale;
     uint8_t *ki_e8;
-    int B, L, m, ncap, n_win, d_rope, act_t, kv_t, idx_t;
+    int B, L, m, ncap, n_win, d_rope, act_t, kv_t, idx_t, win_t;
 };
 void launch_kv_append(const AppendArgs &a, cudaStream_t st);
 
@@ -146,6 +147,9 @@ void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, f
 void launch_quant_mxfp4(const float *x, int64_t rows, uint8_t *codes, uint8_t *e8, cudaStream_t st);
 void launch_mxfp4_to_fp8(const uint8_t *codes, const uint8_t *e8, int64_t rows, uint8_t *out, float *out_scale,
                          cudaStream_t st);
+// NVFP4 entry rows (80 bytes) and FP8 window rows (144 bytes) of 128-dim float rows (fp4.cu)
+void launch_quant_nvfp4_entries(const float *x, int64_t rows, uint8_t *out, cudaStream_t st);
+void launch_quant_fp8_window(const float *x, int64_t rows, uint8_t *out, cudaStream_t st);
 void launch_kv_compress(const CompressArgs &a, cudaStream_t st);
 void launch_indexer(const IndexArgs &a, cudaStream_t st);
 void launch_topk(const TopkArgs &a, cudaStream_t st);
@@ -177,13 +181,13 @@ void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
 // what they handle
 bool launch_hca_tc(const AttnArgs &a, cudaStream_t st);
 bool launch_csa_tc(const AttnArgs &a, cudaStream_t st);
-// Mixed-precision entries (prefill) widened to BF16 rows [B, ncap, 128] in a.ws (csa_widen_bytes
+// MIXED or NVFP4 entries (prefill) widened to BF16 rows [B, ncap, 128] in a.ws (csa_widen_bytes
 // bytes); returns the widened array.
 size_t csa_widen_bytes(const AttnArgs &a);
 // split-KV decode plan (items per sequence S, tiles per item T), partial-result bytes, combine
 void decode_split_plan(int B, int topk, int ncap, int dense, int *S, int *T);
 size_t decode_partial_bytes(int B, int S);
 void launch_decode_combine(const AttnArgs &a, cudaStream_t st);
-const void *launch_widen_mixed(const AttnArgs &a, cudaStream_t st);
+const void *launch_widen_entries(const AttnArgs &a, cudaStream_t st);
 
 }  // namespace csa

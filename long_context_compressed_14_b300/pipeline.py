@@ -14,11 +14,10 @@ from typing import Optional
 
 import torch
 
-from . import (FP8E4M3, MIXED, MXFP4, OP_CSA_DECODE, OP_CSA_PREFILL, OP_HCA_DECODE, OP_HCA_PREFILL, Params,
-               alloc_entries, alloc_index_rows, alloc_workspace, csa_decode, csa_prefill,
-               csa_quant_fp8_rows, csa_quant_mxfp4_rows, hca_decode, hca_prefill, kv_compress, make_params,
-               rope_table,
-               torch_dtype)
+from . import (FP8E4M3, MIXED, MXFP4, NVFP4, OP_CSA_DECODE, OP_CSA_PREFILL, OP_HCA_DECODE, OP_HCA_PREFILL, Params,
+               alloc_entries, alloc_index_rows, alloc_ring, alloc_workspace, csa_decode, csa_prefill,
+               csa_quant_fp8_rows, csa_quant_fp8_window_rows, csa_quant_mxfp4_rows, csa_quant_nvfp4_entries,
+               hca_decode, hca_prefill, kv_compress, make_params, rope_table, torch_dtype)
 
 
 def quantise_index_rows(p: Params, x: torch.Tensor, buf, stream=None):
@@ -38,7 +37,7 @@ def layer_params(wl, csa: bool) -> Params:
     m = wl.m if csa else wl.m_hca
     return make_params(B=wl.B, L=wl.L, H=wl.H, m=m, topk=wl.topk if csa else 0, n_win=wl.n_win,
                        H_I=wl.H_I, d_I=wl.d_I, d=wl.d, d_rope=wl.d_rope, act=wl.q_t, kv=wl.c_t,
-                       idx=wl.idx_t if csa else "f32")
+                       idx=wl.idx_t if csa else "f32", win=getattr(wl, "w_t", "") or None)
 
 
 @dataclass
@@ -117,9 +116,19 @@ class DecodeLayer:
     def load_caches(self, inp: dict, stream=None):
         """Cache set-up (not part of a decode step): the FP8 indexer-key cache is quantised
         from the float keys; a mixed-precision entry cache is stored from the given rows (the
-        first d - d_rope dims as FP8 codes with one scale per entry, the RoPE dims as they are);
-        other entry caches and the ring are used as given."""
+        first d - d_rope dims as FP8 codes with one scale per entry, the RoPE dims as they are),
+        an NVFP4 entry cache and an FP8 ring by the library's quantisers; other entry caches and
+        the ring are used as given."""
         self.C = None
+        self.ring = None
+        if self.p.win_t == FP8E4M3:
+            self.ring = alloc_ring(self.p, inp["ring"].device)
+            csa_quant_fp8_window_rows(inp["ring"].float().contiguous(), self.ring, stream)
+        if self.p.kv_t == NVFP4:
+            C = inp["C"]
+            codes = torch.empty(C.shape[:-1] + (80,), dtype=torch.uint8, device=C.device)
+            csa_quant_nvfp4_entries(C.float().contiguous(), codes, stream)
+            self.C = (codes, None, None)
         if self.p.kv_t == MIXED:
             C = inp["C"]
             nope = self.p.d - self.p.d_rope
@@ -137,12 +146,13 @@ class DecodeLayer:
             C = self.C
         else:
             C = inp["C"] if isinstance(inp["C"], (tuple, list)) else (inp["C"], None, None)
+        ring = self.ring if getattr(self, "ring", None) is not None else inp["ring"]
         if self.csa:
             qI = quantise_index_rows(p, inp["qI"], self.qI, stream)
-            csa_decode(p, inp["q"], inp["ctx"], C, qI, self.KI, inp["w"], inp["ring"], inp.get("sink"), self.rope,
+            csa_decode(p, inp["q"], inp["ctx"], C, qI, self.KI, inp["w"], ring, inp.get("sink"), self.rope,
                        self.topk if want_topk else None, self.out, lse, self.ws, stream)
         else:
-            hca_decode(p, inp["q"], inp["ctx"], C, inp["ring"], inp.get("sink"), self.rope, self.out, lse, self.ws,
+            hca_decode(p, inp["q"], inp["ctx"], C, ring, inp.get("sink"), self.rope, self.out, lse, self.ws,
                        stream)
         return self.out
 

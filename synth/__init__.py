@@ -46,8 +46,9 @@ class Workload:
     groups: int = 8      # output-projection head groups
     d_g: int = 512       # output-projection width per group
     q_t: str = "bf16"    # activations: q, raw kv, outputs
-    c_t: str = "bf16"    # compressed entries: 'f32' | 'bf16' | 'mixed'
-    idx_t: str = "fp8"   # indexer operands: 'f32' | 'fp8'
+    c_t: str = "bf16"    # compressed entries: 'f32' | 'bf16' | 'mixed' | 'nvfp4'
+    idx_t: str = "fp8"   # indexer operands: 'f32' | 'fp8' | 'mxfp4'
+    w_t: str = ""        # decode window ring: '' (as the activations) | 'fp8'
 
     @property
     def scale(self) -> float:
@@ -68,6 +69,9 @@ WORKLOADS = {
     "csa_bf16_4x32768": Workload("csa_bf16_4x32768", "csa", B=4, L=32768, H=64, seed=2),
     # CSA + HCA decode, 16 sequences with 131072 cached tokens each.
     "decode_b16_ctx131072": Workload("decode_b16_ctx131072", "decode", B=16, L=131072, H=64, seed=3),
+    # The same decode step on the V4.1 cache: NVFP4 entries, an FP8 window ring.
+    "decode_v41_b16_ctx131072": Workload("decode_v41_b16_ctx131072", "decode", B=16, L=131072, H=64, seed=3,
+                                         c_t="nvfp4", w_t="fp8"),
     # Interleaved CSA + HCA layer pair, L = 262144, mixed-precision KV entries, top-1024.
     "pair_mixed_L262144": Workload("pair_mixed_L262144", "pair", B=1, L=262144, H=64, seed=4,
                                    topk=1024, c_t="mixed"),

@@ -22,13 +22,15 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
 
-def oracle_prefill(wl, inp: dict, b: int, rows, csa: bool, q_rows=None):
-    """Oracle result of one prefill layer for rows of sequence b (CPU torch inputs)."""
+def oracle_prefill(wl, inp: dict, b: int, rows, csa: bool, q_rows=None, w_store=None):
+    """Oracle result of one prefill layer for rows of sequence b (CPU torch inputs). w_store:
+    the storage of the window rows (default: the activation dtype; 'fp8' for rows read from an
+    FP8 decode ring)."""
     m = wl.m if csa else wl.m_hca
     rows = np.asarray(rows, np.int64)
     comp = oracle.kv_compress(np64(inp["kv"][b]), np64(inp["z"][b]),
                               np64(inp["kI_raw"][b]) if csa and wl.topk > 0 else None, m, wl.d_rope, wl.theta,
-                              c_store=wl.c_t, idx_store=wl.idx_t if csa else "f64", q_store=wl.q_t)
+                              c_store=wl.c_t, idx_store=wl.idx_t if csa else "f64", q_store=w_store or wl.q_t)
     qr = np64(inp["q"][b][rows]) if q_rows is None else q_rows
     kw = dict(d_rope=wl.d_rope, theta=wl.theta, n_win=wl.n_win, scale=wl.scale)
     sink = np64(inp["sink"]) if inp.get("sink") is not None else None
@@ -99,3 +101,16 @@ def check_csa_rows(wl, inp, b, rows, gpu_out_rows, gpu_idx_rows, res, tol=2e-2):
     assert e1 <= tol, ("attention on the GPU selection", e1)
     assert e2 <= tol, ("end to end", e2)
     return e1, e2
+
+
+def unpack_nvfp4(rows: torch.Tensor):
+    """NVFP4 entry rows [.., 80] uint8 (layout in include/csa.h) -> (codes [.., 64], block codes
+    [.., 8], row scales [..] float32, pad bytes [.., 4])."""
+    r = rows.cpu().numpy()
+    return r[..., :64], r[..., 64:72], np.ascontiguousarray(r[..., 72:76]).view(np.float32)[..., 0], r[..., 76:80]
+
+
+def unpack_fp8_window(rows: torch.Tensor):
+    """FP8 window rows [.., 144] uint8 -> (codes [.., 128], scales [..] float32, pad [.., 12])."""
+    r = rows.cpu().numpy()
+    return r[..., :128], np.ascontiguousarray(r[..., 128:132]).view(np.float32)[..., 0], r[..., 132:144]

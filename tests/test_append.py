@@ -11,22 +11,24 @@ import torch
 
 import oracle
 import synth
-from _helpers import attention_on_gpu_selection, check_topk_by_score, np64, oracle_prefill, rel_l2
+from _helpers import attention_on_gpu_selection, check_topk_by_score, np64, oracle_prefill, rel_l2, unpack_nvfp4
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("csa,c_t,L0,L1", [
-    (True, "bf16", 301, 363),    # CSA m = 4: a block completes every 4 appends
-    (True, "mixed", 255, 300),
-    (False, "bf16", 200, 400),   # HCA m' = 128: blocks complete at 255 and 383
+@pytest.mark.parametrize("csa,c_t,w_t,L0,L1", [
+    (True, "bf16", "", 301, 363),    # CSA m = 4: a block completes every 4 appends
+    (True, "mixed", "", 255, 300),
+    (False, "bf16", "", 200, 400),   # HCA m' = 128: blocks complete at 255 and 383
+    (True, "nvfp4", "fp8", 301, 350),  # the V4.1 cache: NVFP4 entries, FP8 window ring
+    (False, "nvfp4", "fp8", 200, 300),
 ])
-def test_prefill_then_append_decode_continuity(lib, csa, c_t, L0, L1):
+def test_prefill_then_append_decode_continuity(lib, csa, c_t, w_t, L0, L1):
     from long_context_compressed_14_b300.pipeline import layer_params
     if csa:
-        wl = synth.WORKLOADS["csa_bf16_4x32768"].replace(B=1, L=L1, topk=64, c_t=c_t)
+        wl = synth.WORKLOADS["csa_bf16_4x32768"].replace(B=1, L=L1, topk=64, c_t=c_t, w_t=w_t)
     else:
-        wl = synth.WORKLOADS["hca_bf16_L16384"].replace(B=1, L=L1, H=64, c_t=c_t)
+        wl = synth.WORKLOADS["hca_bf16_L16384"].replace(B=1, L=L1, H=64, c_t=c_t, w_t=w_t)
     m = wl.m if csa else wl.m_hca
     inp = synth.prefill_layer(wl, csa=csa)
     d = {k: v.cuda() for k, v in inp.items()}
@@ -40,10 +42,15 @@ def test_prefill_then_append_decode_continuity(lib, csa, c_t, L0, L1):
     # prefill: entries of the first L0 tokens (B = 1, so they are a prefix of the capacity cache)
     lib.kv_compress(p0, d["kv"][:, :L0].contiguous(), d["z"][:, :L0].contiguous(),
                     d["kI_raw"][:, :L0].contiguous() if csa else None, rope, C, KI, kv_rope)
-    # hand-over: the window ring from kv_rope, the state cache from the last 2m raw tokens
+    # hand-over: the window ring from kv_rope (an FP8 ring through the library's quantiser), the
+    # state cache from the last 2m raw tokens
     ring = torch.zeros((1, wl.n_win, 128), dtype=torch.bfloat16, device="cuda")
     for u in range(max(0, L0 - wl.n_win), L0):
         ring[0, u % wl.n_win] = kv_rope[0, u]
+    if w_t == "fp8":
+        ring8 = lib.alloc_ring(p)
+        lib.csa_quant_fp8_window_rows(ring.float().contiguous(), ring8)
+        ring = ring8
     st_kv = torch.zeros((1, 2 * m, 128), dtype=torch.bfloat16, device="cuda")
     st_z = torch.zeros((1, 2 * m, 2), dtype=torch.float32, device="cuda")
     st_kI = torch.zeros((1, 2 * m, 64), dtype=torch.float32, device="cuda") if csa else None
@@ -72,7 +79,8 @@ def test_prefill_then_append_decode_continuity(lib, csa, c_t, L0, L1):
     assert lib.csa_device_status() == 0
 
     rows = np.arange(L0, L1)
-    res = oracle_prefill(wl, inp, 0, rows, csa=csa)
+    # the oracle's window rows stored as the ring stores them
+    res = oracle_prefill(wl, inp, 0, rows, csa=csa, w_store="fp8" if w_t == "fp8" else None)
     got = np64(out)
     if csa:
         gidx = idx.cpu().numpy()
@@ -88,6 +96,12 @@ def test_prefill_then_append_decode_continuity(lib, csa, c_t, L0, L1):
     if c_t == "mixed":
         gc = np.concatenate([oracle.dequant_fp8(C[0][0].cpu().numpy(), C[2][0].cpu().numpy()), np64(C[1][0])], axis=1)
         assert rel_l2(gc[:full], comp["C"][:full]) < 1e-2
+    elif c_t == "nvfp4":
+        gc, gb, gs, _ = unpack_nvfp4(C[0][0])
+        oc, ob, os_ = comp["C_raw"]
+        assert np.mean(gc[:full] == oc[:full]) >= 0.99 and np.mean(gb[:full] == ob[:full]) >= 0.99
+        np.testing.assert_allclose(gs[:full], os_[:full], rtol=1e-6)
+        assert rel_l2(oracle.dequant_nvfp4(gc, gb, gs)[:full], comp["C"][:full]) < 2e-2
     else:
         np.testing.assert_allclose(np64(C[0][0])[:full], comp["C"][:full], rtol=2 ** -7, atol=4e-6)
     if csa:

@@ -23,7 +23,7 @@ import torch
 import oracle
 import synth
 from _helpers import (attention_on_gpu_selection, check_csa_rows, check_topk_by_score, np32, np64,
-                      oracle_prefill, rel_l2)
+                      oracle_prefill, rel_l2, unpack_nvfp4)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +71,8 @@ def test_quant_fp8_rows_bit_exact(lib):
     dict(L=3001, m=4, act="bf16", kv="mixed", idx="fp8"),
     dict(L=517, m=128, act="bf16", kv="mixed", idx=None),
     dict(L=3, m=4, act="f32", kv="f32", idx="f32"),
+    dict(L=2999, m=4, act="bf16", kv="nvfp4", idx="mxfp4"),
+    dict(L=700, m=128, act="bf16", kv="nvfp4", idx=None),
 ])
 def test_kv_compress(lib, case):
     wl = synth.Workload("t", "csa", B=2, L=case["L"], H=8, seed=11, m=case["m"], q_t=case["act"], c_t=case["kv"],
@@ -92,7 +94,17 @@ def test_kv_compress(lib, case):
                                   wl.m, 64, 1e4, c_store=case["kv"], idx_store=wl.idx_t, q_store=case["act"])
         assert comp["N"] == ncap
         # entries
-        if case["kv"] == "mixed":
+        if case["kv"] == "nvfp4":
+            # the NVFP4 codes of the rotated entries: where the float and double sums fall on
+            # either side of a rounding boundary an element moves by one step of its grid
+            gc, gb, gs, pad = unpack_nvfp4(C[0][b])
+            oc, ob, os_ = comp["C_raw"]
+            assert np.all(pad == 0)
+            assert np.mean(gc == oc) >= 0.99 and np.mean(gb == ob) >= 0.99
+            np.testing.assert_allclose(gs, os_, rtol=1e-6)
+            got = oracle.dequant_nvfp4(gc, gb, gs)
+            assert rel_l2(got, comp["C"]) < 2e-2
+        elif case["kv"] == "mixed":
             got = np.concatenate([oracle.dequant_fp8(C[0][b].cpu().numpy(), C[2][b].cpu().numpy()),
                                   np64(C[1][b])], axis=1)
             # codes can sit one E4M3 step apart where the float sums differ in the last bit
@@ -109,6 +121,9 @@ def test_kv_compress(lib, case):
         if with_ki:
             if wl.idx_t == "f32":
                 np.testing.assert_allclose(np64(KI[0][b]), comp["KI"], rtol=3e-6, atol=1e-6)
+            elif wl.idx_t == "mxfp4":
+                gk = oracle.dequant_mxfp4(KI[0][b].cpu().numpy(), KI[2][b].cpu().numpy())
+                assert np.mean(gk == comp["KI"]) >= 0.99 and rel_l2(gk, comp["KI"]) < 2e-2
             else:
                 gk = oracle.dequant_fp8(KI[0][b].cpu().numpy(), KI[1][b].cpu().numpy())
                 assert rel_l2(gk, comp["KI"]) < 1e-2
@@ -472,17 +487,18 @@ def _oracle_decode(wl, inp, b, csa, gpu_idx=None):
     m = wl.m if csa else wl.m_hca
     kw = dict(d_rope=wl.d_rope, theta=wl.theta, n_win=wl.n_win, scale=wl.scale)
     ctx = int(inp["ctx"][b])
-    C, _ = oracle.store_rows(np64(inp["C"][b]), wl.c_t if wl.c_t == "mixed" else "f64", wl.d_rope)
+    C, _ = oracle.store_rows(np64(inp["C"][b]), wl.c_t if wl.c_t in ("mixed", "nvfp4") else "f64", wl.d_rope)
+    ring, _ = oracle.store_rows(np64(inp["ring"][b]), "fp8" if wl.w_t == "fp8" else "f64")
     if csa:
         KI, _ = oracle.store_rows(np32(inp["KI"][b]), wl.idx_t)
         res = oracle.csa_decode(np64(inp["q"][b]), ctx, C, np32(inp["qI"][b]), KI,
-                                np32(inp["w"][b]), np64(inp["ring"][b]), np64(inp["sink"]), m=m, k=wl.topk,
+                                np32(inp["w"][b]), ring, np64(inp["sink"]), m=m, k=wl.topk,
                                 idx_store=wl.idx_t, **kw)
         if gpu_idx is not None:
             res["o_own"], _ = oracle.decode_one(np64(inp["q"][b]), ctx, C, np.asarray(gpu_idx, np.int32), wl.topk, m,
-                                                np64(inp["ring"][b]), sink=np64(inp["sink"]), **kw)
+                                                ring, sink=np64(inp["sink"]), **kw)
         return res
-    return oracle.hca_decode(np64(inp["q"][b]), ctx, C, np64(inp["ring"][b]), np64(inp["sink"]), m=m, **kw)
+    return oracle.hca_decode(np64(inp["q"][b]), ctx, C, ring, np64(inp["sink"]), m=m, **kw)
 
 
 def _check_decode(wl, inp, layer, out, csa, seqs):
@@ -498,11 +514,14 @@ def _check_decode(wl, inp, layer, out, csa, seqs):
 
 
 @pytest.mark.parametrize("csa", [True, False])
-@pytest.mark.parametrize("c_t,idx_t", [("bf16", "fp8"), ("mixed", "fp8"), ("bf16", "mxfp4")])
-def test_decode(lib, csa, c_t, idx_t):
+@pytest.mark.parametrize("c_t,idx_t,w_t", [("bf16", "fp8", ""), ("mixed", "fp8", ""), ("bf16", "mxfp4", ""),
+                                           ("nvfp4", "fp8", "fp8"), ("nvfp4", "mxfp4", "")])
+def test_decode(lib, csa, c_t, idx_t, w_t):
+    # the last two: the V4.1 cache (NVFP4 entries, FP8 window ring), and NVFP4 entries with the
+    # FP4 indexer and a BF16 ring
     if idx_t == "mxfp4" and not csa:
         pytest.skip("the HCA layer has no indexer")
-    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=8192, topk=256, c_t=c_t, idx_t=idx_t)
+    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=8192, topk=256, c_t=c_t, idx_t=idx_t, w_t=w_t)
     from long_context_compressed_14_b300.pipeline import DecodeLayer
     inp = synth.decode_layer(wl, csa=csa)
     inp["ctx"] = torch.tensor([8192, 1, 77, 5001], dtype=torch.int32)
