@@ -32,11 +32,18 @@
 //               (decode). Decode tiles stored in a low-precision form (MIXED or NVFP4 entries,
 //               an FP8 ring) are widened to BF16 by the producer threads: each thread loads a
 //               group of its chunks, then converts and stores them.
-// Pipelines: key tiles in a 3-buffer ring, S^T and O^T double-buffered in TMEM (O^T by token),
-// P^T double-buffered in shared memory, query rows double-buffered; every wait is bounded.
-// Epilogue: O^T is normalised per head, the RoPE half is rotated back (the two dims of a pair
-// live in different warps and meet in shared memory), staged as BF16 [head][dim] and written
-// with one 16 KB bulk copy per token.
+// Pipelines: key tiles in a 3- or 4-buffer ring, four S^T slots and two O^T slots (by token) in
+// TMEM, P^T double-buffered in shared memory, query rows double-buffered; every wait is bounded.
+// The MMA warp issues the P V of tile n after the S^T of tile n + 2, so S^T work is queued on the
+// tensor pipe while the softmax finishes a tile. The tensor pipe reads its operands from shared
+// memory, whose bandwidth (with the gather's and the softmax's writes) bounds this kernel: an
+// N = 64 MMA is operand-read bound, and the MMA issue loop builds each descriptor by adding a
+// constant to a base descriptor.
+// Epilogue: the per-head sums are reduced right after a token's last tile; the O part waits
+// until the next token's first tile has been handed over (its P V has finished by then): O^T is
+// normalised per head, the RoPE half is rotated back (the two dims of a pair live in different
+// warps and meet in shared memory), staged as BF16 [head][dim] and written with one 16 KB bulk
+// copy per token.
 //
 // Prefill with MIXED or NVFP4 entries first widens every entry to BF16 once (the dequantised
 // value rounded to nearest even) into caller workspace; the gather then reads BF16 rows.
@@ -62,18 +69,20 @@ constexpr int kConvBatch = 8;                 // converted chunks whose loads ar
 // Shared memory (1024-aligned), for NB key-tile buffers:
 //   Q       2 buffers x 16 KB (two 64-dim halves of 8 KB)
 //   keys    NB x 32 KB (two 64-dim halves of 16 KB)
-//   P^T     2 x 16 KB; during a token's epilogue buffer 0 also serves as the RoPE exchange
-//           [2 WG][2 halves][32 heads][32] float (every P V of the token has completed then)
-//   output  staging [64 heads][128 dims] BF16, 16 KB
+//   P^T     2 x 16 KB
+//   output  staging [64 heads][128 dims] BF16, 16 KB; before that, in a token's epilogue, the
+//           RoPE exchange [2 WG][2 halves][32 heads][32] float
 //   top-k   2 rows of topk int32
 constexpr int kQOff = 0;
 constexpr int kKOff = 32768;
 __host__ __device__ constexpr int p_off(int nb) { return kKOff + nb * 32768; }
 __host__ __device__ constexpr int out_off(int nb) { return p_off(nb) + 2 * 16384; }
 __host__ __device__ constexpr int idx_off(int nb) { return out_off(nb) + 16384; }
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0;                 // S^T slots: [0, 64) and [64, 128)
-constexpr uint32_t kOCol = 128;               // O^T slots: [128, 192) and [192, 256)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSSlots = 4;                    // S^T slots in TMEM
+constexpr int kLag = 2;                       // the P V of tile n is issued after the S^T of tile n + kLag
+constexpr uint32_t kSCol = 0;                 // S^T slots: [64 i, 64 i + 64), i < kSSlots
+constexpr uint32_t kOCol = 256;               // O^T slots: [256, 320) and [320, 384)
 constexpr float kOver = 8.0f;                 // log2 of the largest unnormalised weight allowed
 // named barriers (0 is __syncthreads)
 constexpr uint32_t kBarSoftmax = 1, kBarProd = 2, kBarWG0 = 3;  // kBarWG0 + w per warpgroup
@@ -221,13 +230,13 @@ __device__ __forceinline__ float warp_transpose_max16(float (&v)[16], int lane) 
 template <int kNB>
 __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __grid_constant__ CsaTcParams P) {
     using namespace csa_tc;
-    constexpr int kPOff = p_off(kNB), kOutOff = out_off(kNB), kIdxOff = idx_off(kNB), kXOff = kPOff;
+    constexpr int kPOff = p_off(kNB), kOutOff = out_off(kNB), kIdxOff = idx_off(kNB);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // mbarriers
     __shared__ __align__(8) uint64_t b_qraw[2], b_qfull[2], b_qempty[2];
     __shared__ __align__(8) uint64_t b_kfull[kNB], b_kempty[kNB];
-    __shared__ __align__(8) uint64_t b_sfull[2], b_sempty[2], b_pfull[2], b_pempty[2];
+    __shared__ __align__(8) uint64_t b_sfull[kSSlots], b_sempty[kSSlots], b_pfull[2], b_pempty[2];
     __shared__ __align__(8) uint64_t b_ofull[2], b_oempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ TokenMeta meta[2];
@@ -253,8 +262,6 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             // query slot free: the last S^T MMA of its token is done (commit) and the softmax
             // threads have copied the token's metadata
             mbar_init(smem_u32(&b_qempty[i]), 1 + kSoftmax);
-            mbar_init(smem_u32(&b_sfull[i]), 1);
-            mbar_init(smem_u32(&b_sempty[i]), kSoftmax);
             mbar_init(smem_u32(&b_pfull[i]), kSoftmax);
             mbar_init(smem_u32(&b_pempty[i]), 1);
             mbar_init(smem_u32(&b_ofull[i]), 1);
@@ -263,6 +270,10 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         for (int i = 0; i < kNB; ++i) {
             mbar_init(smem_u32(&b_kfull[i]), kProducers);
             mbar_init(smem_u32(&b_kempty[i]), 1);
+        }
+        for (int i = 0; i < kSSlots; ++i) {
+            mbar_init(smem_u32(&b_sfull[i]), 1);
+            mbar_init(smem_u32(&b_sempty[i]), kSoftmax);
         }
         mbar_fence_init();
     }
@@ -502,35 +513,51 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16(128, kH, 0, 0);  // S^T = K Q^T
             const uint32_t idesc_o = idesc_bf16(128, kH, 1, 1);  // O^T = V^T P^T, both MN-major
-            int n = 0;
-            int prev_n = -1, prev_first = 0, prev_last = 0, prev_tok = 0;  // the item whose P V is still to issue
-            auto issue_pv = [&](int pn, bool first, bool last, int tok) -> bool {
+            // descriptors of the buffers' first rows; within a buffer the start-address field
+            // advances by (byte offset >> 4), which never carries out of the field (< 256 KB)
+            const uint64_t dK0 = sdesc_sw128(s_base + kKOff, 16, 1024);     // key tile, K-major (S)
+            const uint64_t dQ0 = sdesc_sw128(s_base + kQOff, 16, 1024);     // query rows, K-major
+            const uint64_t dV0 = sdesc_sw128(s_base + kKOff, 16384, 1024);  // key tile, MN-major (P V)
+            const uint64_t dP0 = sdesc_sw128(s_base + kPOff, 16384, 1024);  // P^T, MN-major
+            // P V items waiting for their P^T, issued kLag = 2 tiles behind the S^T MMAs so that the
+            // tensor pipe holds queued S^T work while the softmax finishes an earlier tile. Items
+            // are consecutive tiles from pv_n on; pend0..2 hold (token << 2 | last << 1 | first).
+            static_assert(kLag == 2, "three pending slots");
+            int pv_n = 0, npend = 0, pend0 = 0, pend1 = 0, pend2 = 0;
+            auto issue_pv = [&]() -> bool {
+                const int pn = pv_n, fl = pend0, tok = pend0 >> 2;
+                pend0 = pend1;
+                pend1 = pend2;
+                --npend;
+                ++pv_n;
+                const bool first = (fl & 1) != 0, last = (fl & 2) != 0;
                 const int pb = pn & 1, ob = tok & 1;
                 if (!mbar_wait(smem_u32(&b_pfull[pb]), (pn >> 1) & 1, kWaitNs, &g_abort)) return false;
                 if (first && tok >= 2 && !mbar_wait(smem_u32(&b_oempty[ob]), ((tok >> 1) - 1) & 1, kWaitNs, &g_abort))
                     return false;
                 tc_fence_after();
-                const uint32_t kb = s_base + kKOff + (pn % kNB) * 32768;
-                const uint32_t pbuf = s_base + kPOff + pb * 16384;
+                const uint64_t ad = dV0 + (uint64_t)(((pn % kNB) * 32768) >> 4);
+                const uint64_t bd = dP0 + (uint64_t)((pb * 16384) >> 4);
+                const uint32_t d = tmem + kOCol + ob * kH;
+                mma_bf16(d, ad, bd, idesc_o, first ? 0u : 1u);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);    // V^T, M = dims
-                    const uint64_t bd = sdesc_sw128(pbuf + kk * 2048, 16384, 1024);  // P^T, N = heads
-                    mma_bf16(tmem + kOCol + ob * kH, ad, bd, idesc_o, (!first || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < 8; ++kk) mma_bf16(d, ad + (kk * 2048 >> 4), bd + (kk * 2048 >> 4), idesc_o, 1u);
                 mma_commit(smem_u32(&b_pempty[pb]));
                 mma_commit(smem_u32(&b_kempty[pn % kNB]));
                 if (last) mma_commit(smem_u32(&b_ofull[ob]));
                 return true;
             };
+            int n = 0;
             for (int it = 0; it < n_tok_cta && ok; ++it) {
                 const int qs = it & 1;
                 if (!mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kWaitNs, &g_abort)) { ok = false; break; }
                 const int n_tiles = meta[qs].n_tiles;
+                const uint64_t bq = dQ0 + (uint64_t)((qs * 16384) >> 4);
                 for (int c = 0; c < n_tiles; ++c, ++n) {
-                    const int kb = n % kNB, sb = n & 1;
+                    const int kb = n % kNB, sb = n % kSSlots;
                     if (!mbar_wait(smem_u32(&b_kfull[kb]), (n / kNB) & 1, kWaitNs, &g_abort)) { ok = false; break; }
-                    if (n >= 2 && !mbar_wait(smem_u32(&b_sempty[sb]), ((n >> 1) - 1) & 1, kWaitNs, &g_abort)) {
+                    if (n >= kSSlots &&
+                        !mbar_wait(smem_u32(&b_sempty[sb]), ((n / kSSlots) - 1) & 1, kWaitNs, &g_abort)) {
                         ok = false;
                         break;
                     }
@@ -538,24 +565,26 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     // the barrier; order them before the tensor core's reads (async proxy)
                     fence_async_smem();
                     tc_fence_after();
-                    const uint32_t kbuf = s_base + kKOff + kb * 32768;
-                    const uint32_t qbuf = s_base + kQOff + qs * 16384;
+                    const uint64_t ak = dK0 + (uint64_t)((kb * 32768) >> 4);
+                    const uint32_t d = tmem + kSCol + sb * kH;
+                    mma_bf16(d, ak, bq, idesc_s, 0u);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = sdesc_sw128(kbuf + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(qbuf + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                        mma_bf16(tmem + kSCol + sb * kH, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 1; kk < 8; ++kk) {
+                        const uint32_t off_k = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        const uint32_t off_q = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                        mma_bf16(d, ak + off_k, bq + off_q, idesc_s, 1u);
                     }
                     mma_commit(smem_u32(&b_sfull[sb]));
                     if (c == n_tiles - 1) mma_commit(smem_u32(&b_qempty[qs]));
-                    if (prev_n >= 0 && !issue_pv(prev_n, prev_first, prev_last, prev_tok)) { ok = false; break; }
-                    prev_n = n;
-                    prev_first = c == 0;
-                    prev_last = c == n_tiles - 1;
-                    prev_tok = it;
+                    const int item = (it << 2) | (c == n_tiles - 1 ? 2 : 0) | (c == 0 ? 1 : 0);
+                    if (npend == 0) pend0 = item;
+                    else if (npend == 1) pend1 = item;
+                    else pend2 = item;
+                    ++npend;
+                    if (npend > kLag && !issue_pv()) { ok = false; break; }
                 }
             }
-            if (ok && prev_n >= 0) ok = issue_pv(prev_n, prev_first, prev_last, prev_tok);
+            while (ok && npend > 0) ok = issue_pv();
             if (!ok) set_timeout();
         }
     } else {
@@ -566,14 +595,82 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         const uint32_t bar_wg = kBarWG0 + wg;
         const int h0 = 32 * wg;
         // Every wait result is kept in okl and acted upon only through an OR-reduction over all
-        // softmax threads, so that all of them leave together and no named barrier is ever left
-        // short of threads.
+        // softmax threads (once per token), so that all of them leave together and no named
+        // barrier is ever left short of threads; a failed wait raises the abort flag at once, so
+        // the remaining waits of the token return early.
         bool okl = true;
-        auto note = [&](bool w) { okl = okl && w; };
+        auto note = [&](bool w) {
+            if (!w && okl) set_timeout();
+            okl = okl && w;
+        };
         float lpart[32];
         int n = 0;
+        // The O part of a token's epilogue (wait for its last P V, normalise, inverse RoPE,
+        // store) is deferred until the next token's first tile has been handed to the MMA warp,
+        // so the softmax threads do not idle while that P V runs. State of the deferred token:
+        int pend_it = -1, pend_t = 0, pend_b = 0, pend_ok = 0;
+        // returns false (in every softmax thread alike) after a failed wait
+        auto o_epilogue = [&]() -> bool {
+            const int ob = pend_it & 1;
+            note(mbar_wait(smem_u32(&b_ofull[ob]), (pend_it >> 1) & 1, kWaitNs, &g_abort));
+            if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) return false;
+            tc_fence_after();
+            float o[32];
+            tmem_ld32_sync(tmem + lane_base + kOCol + ob * kH + h0, o);  // lane kl = output dim
+            tc_fence_before();
+            mbar_arrive(smem_u32(&b_oempty[ob]));
+            if (P.split) {
+                // unnormalised partial O of this item: [head][dim], dims across the warp's lanes
+                float *po = P.part_o + (((int64_t)blockIdx.x + (int64_t)pend_it * gridDim.x) * kH + h0) * 128 + kl;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) __stcg(po + e * 128, o[e]);
+                return true;
+            }
+            {
+                const float4 *f4 = reinterpret_cast<const float4 *>(s_fo + h0);
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 ff = f4[e4];
+                    o[4 * e4] *= ff.x;
+                    o[4 * e4 + 1] *= ff.y;
+                    o[4 * e4 + 2] *= ff.z;
+                    o[4 * e4 + 3] *= ff.w;
+                }
+            }
+            // the staging buffer: the previous token's bulk store must have finished reading it
+            if (tid == 0) bulk_wait_read_all();
+            named_sync(kBarSoftmax, kSoftmax);
+            if (P.d_rope == 64 && kl >= 64) {
+                // dims 64 + i (warp 2) and 96 + i (warp 3) of a pair meet in the staging buffer
+                const int half = (kl >> 5) & 1, i = kl & 31;
+                float *x = reinterpret_cast<float *>(sm + kOutOff) + wg * 2048;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[half * 1024 + e * 32 + i] = o[e];
+                named_sync(kBarWG0 + 2 + wg, 64);  // warps 2 and 3 of this warpgroup
+                const float2 cs = pend_ok ? P.rope[(int64_t)pend_t * 32 + i] : make_float2(1.0f, 0.0f);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float other = x[(half ^ 1) * 1024 + e * 32 + i];
+                    o[e] = half == 0 ? o[e] * cs.x + other * cs.y : -other * cs.y + o[e] * cs.x;
+                }
+            }
+            named_sync(kBarSoftmax, kSoftmax);  // the exchange is read before the staging writes
+            {
+                __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + kOutOff);  // [h][d]
+#pragma unroll
+                for (int e = 0; e < 32; ++e) os[(h0 + e) * 128 + kl] = __float2bfloat16_rn(o[e]);
+            }
+            fence_async_smem();
+            named_sync(kBarSoftmax, kSoftmax);
+            if (tid == 0 && pend_ok) {
+                const int64_t orow = P.decode ? (int64_t)pend_b : (int64_t)pend_b * P.L + pend_t;
+                bulk_store(P.out + orow * kH * 128, s_base + kOutOff, kH * 128 * 2);
+            }
+            return true;
+        };
+        bool failed = false;
         for (int it = 0; it < n_tok_cta; ++it) {
-            const int qs = it & 1, ob = it & 1;
+            const int qs = it & 1;
             note(mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kWaitNs, &g_abort));
             if (tid < kH) s_m[tid] = -INFINITY;
             if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
@@ -582,11 +679,10 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
             const int n_tiles = mt.n_tiles;
 #pragma unroll
             for (int e = 0; e < 32; ++e) lpart[e] = 0.0f;
-            bool failed = false;
             for (int cl = 0; cl < n_tiles; ++cl, ++n) {
                 const int c = mt.c0 + cl;
-                const int sb = n & 1, pb = n & 1;
-                note(mbar_wait(smem_u32(&b_sfull[sb]), (n >> 1) & 1, kWaitNs, &g_abort));
+                const int sb = n % kSSlots, pb = n & 1;
+                note(mbar_wait(smem_u32(&b_sfull[sb]), (n / kSSlots) & 1, kWaitNs, &g_abort));
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_base + kSCol + sb * kH + h0;
                 // key validity of this thread's key (TMEM lane = key within the tile)
@@ -594,11 +690,13 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 if (c < mt.n_ct) valid = c * kTile + kl < mt.n_sel;
                 else valid = kl >= kTile - mt.n_win_t;  // key row kl is position t - 127 + kl
                 // p = exp2(scale * s - m) with the current maxima; the S^T slot stays held until
-                // the P^T row is written, so the rare slow path can read the logits again
+                // the P^T row is written, so the rare slow path can read the logits again. A
+                // token's first tile always takes the slow path (no maximum yet): its speculative
+                // pass is skipped.
                 float p[32];
-                tmem_ld32_sync(s_addr, p);
-                bool over = false;
-                {
+                bool over = cl == 0;
+                if (cl > 0) {
+                    tmem_ld32_sync(s_addr, p);
                     const float4 *m4 = reinterpret_cast<const float4 *>(s_m + h0);
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
@@ -613,13 +711,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     }
                 }
                 if (n >= 2) note(mbar_wait(smem_u32(&b_pempty[pb]), ((n >> 1) - 1) & 1, kWaitNs, &g_abort));
-                if (named_sync_or(kBarSoftmax, kSoftmax, over || !okl)) {
-                    // rare: a first tile, a jump of the maximum, or a failed wait
-                    if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) { failed = true; break; }
-                    over = true;
-                } else {
-                    over = false;
-                }
+                // the warpgroup owns its heads' maxima: the decision is the warpgroup's (rare: a
+                // first tile or a jump of the maximum)
+                over = named_sync_or(bar_wg, 128, over);
                 if (over) {
                     // per-head maximum of this tile over the warpgroup's 128 keys, 16 heads at a time
 #pragma unroll 1
@@ -660,10 +754,10 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
 #pragma unroll 1
                         for (int c0 = 0; c0 < 32; c0 += 16) {
                             float o[16];
-                            tmem_ld16_sync(tmem + lane_base + kOCol + ob * kH + h0 + c0, o);
+                            tmem_ld16_sync(tmem + lane_base + kOCol + (it & 1) * kH + h0 + c0, o);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) o[e] *= s_f[h0 + c0 + e];
-                            tmem_st16(tmem + lane_base + kOCol + ob * kH + h0 + c0, o);
+                            tmem_st16(tmem + lane_base + kOCol + (it & 1) * kH + h0 + c0, o);
                         }
                         tmem_st_wait();
                     }
@@ -698,9 +792,17 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 fence_async_smem();
                 tc_fence_before();
                 mbar_arrive(smem_u32(&b_pfull[pb]));
+                if (cl == 0 && pend_it >= 0) {
+                    if (!o_epilogue()) {
+                        failed = true;
+                        break;
+                    }
+                    pend_it = -1;
+                }
             }
             if (failed) break;
-            // ---- epilogue of the token: reduce the sums, normalise, inverse RoPE, store ----
+            // ---- epilogue of the token: reduce the sums into the per-head output factors; the
+            // O part follows with the next token's first tile (or after the last token) ----
             {
                 const float lsum = warp_transpose_reduce<1>(lpart, lane);
                 s_red[warp][lane] = lsum;
@@ -727,60 +829,12 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                     P.lse[(int64_t)((P.decode ? mt.b : (int64_t)mt.b * P.L + mt.t)) * kH + h] =
                         (m + log2f(l)) * 0.6931471805599453f;
             }
-            note(mbar_wait(smem_u32(&b_ofull[ob]), (it >> 1) & 1, kWaitNs, &g_abort));
-            if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
-            tc_fence_after();
-            float o[32];
-            tmem_ld32_sync(tmem + lane_base + kOCol + ob * kH + h0, o);  // lane kl = output dim
-            tc_fence_before();
-            mbar_arrive(smem_u32(&b_oempty[ob]));
-            if (P.split) {
-                // unnormalised partial O of this item: [head][dim], dims across the warp's lanes
-                float *po = P.part_o + (((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * kH + h0) * 128 + kl;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) __stcg(po + e * 128, o[e]);
-                continue;
-            }
-            {
-                const float4 *f4 = reinterpret_cast<const float4 *>(s_fo + h0);
-#pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 ff = f4[e4];
-                    o[4 * e4] *= ff.x;
-                    o[4 * e4 + 1] *= ff.y;
-                    o[4 * e4 + 2] *= ff.z;
-                    o[4 * e4 + 3] *= ff.w;
-                }
-            }
-            if (P.d_rope == 64 && kl >= 64) {
-                // dims 64 + i (warp 2) and 96 + i (warp 3) of a pair meet in shared memory
-                const int half = (kl >> 5) & 1, i = kl & 31;
-                float *x = reinterpret_cast<float *>(sm + kXOff) + wg * 2048;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[half * 1024 + e * 32 + i] = o[e];
-                named_sync(kBarWG0 + 2 + wg, 64);  // warps 2 and 3 of this warpgroup
-                const float2 cs = mt.pos_ok ? P.rope[(int64_t)mt.t * 32 + i] : make_float2(1.0f, 0.0f);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float other = x[(half ^ 1) * 1024 + e * 32 + i];
-                    o[e] = half == 0 ? o[e] * cs.x + other * cs.y : -other * cs.y + o[e] * cs.x;
-                }
-            }
-            // staging buffer: the previous token's bulk store must have finished reading it
-            if (tid == 0) bulk_wait_read_all();
-            named_sync(kBarSoftmax, kSoftmax);
-            {
-                __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + kOutOff);  // [h][d]
-#pragma unroll
-                for (int e = 0; e < 32; ++e) os[(h0 + e) * 128 + kl] = __float2bfloat16_rn(o[e]);
-            }
-            fence_async_smem();
-            named_sync(kBarSoftmax, kSoftmax);
-            if (tid == 0 && mt.pos_ok) {
-                const int64_t orow = P.decode ? (int64_t)mt.b : (int64_t)mt.b * P.L + mt.t;
-                bulk_store(P.out + orow * kH * 128, s_base + kOutOff, kH * 128 * 2);
-            }
+            pend_it = it;
+            pend_t = mt.t;
+            pend_b = mt.b;
+            pend_ok = mt.pos_ok;
         }
+        if (!failed && pend_it >= 0) o_epilogue();
         if (tid == 0) bulk_wait_all();
         if (!okl) set_timeout();
     }
