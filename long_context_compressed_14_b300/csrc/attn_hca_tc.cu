@@ -20,7 +20,9 @@
 // shared memory through an MN-major descriptor.
 //
 // Roles (192 threads, persistent over work items):
-//   warps 0-3  softmax + epilogue (thread = query row = TMEM lane);
+//   warps 0-3  softmax + epilogue (thread = query row = TMEM lane); the epilogue stages the
+//              item's 128 output rows (BF16, 128-byte swizzle) in the item's query slot, whose
+//              query rows are no longer needed, and writes them with two TMA tensor stores;
 //   warp 4     MMA issue (one thread);
 //   warp 5     producer: query rows by TMA (and RoPE on them, all 32 lanes), key tiles by TMA.
 // S/P is double-buffered in TMEM, so the MMA computes the next tile's scores and the previous
@@ -57,6 +59,7 @@ constexpr float kOver = 8.0f;              // log2 of the largest unnormalised w
 
 struct HcaTcParams {
     CUtensorMap mq;    // q viewed as [B][L*H][128] bf16, box 64 x 128
+    CUtensorMap mo;    // out viewed as [B][L*H][128] bf16, box 64 x 128 (the epilogue's stores)
     CUtensorMap mc;    // BF16 entries [B][ncap][128], box 64 x 128
     CUtensorMap mkv;   // kv_rope [B][L][128] bf16, box 64 x 144
     const float *sink;
@@ -112,7 +115,9 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&b_qraw[i]), 1);
             mbar_init(smem_u32(&b_qfull[i]), 32);
-            mbar_init(smem_u32(&b_qempty[i]), 1);
+            // query slot free: the item's last S MMA is done (commit) and the item's output,
+            // staged in the slot by the epilogue, has been read by its bulk store
+            mbar_init(smem_u32(&b_qempty[i]), 2);
         }
         for (int i = 0; i < kNB; ++i) {
             mbar_init(smem_u32(&b_kfull[i]), 1);
@@ -334,7 +339,8 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 }
                 if (!row_ok) hi = 0;
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&b_sfull[sb]), (n >> 1) & 1, kWaitNs, &g_abort))) {
-                    ok = false;
+                    ok = false;  // (the warps leave together at the item's epilogue barrier)
+                    set_timeout();
                     break;
                 }
                 tc_fence_after();
@@ -373,6 +379,7 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                         // O holds the P V of this item's earlier tiles: let the last one finish
                         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&b_pvdone), (n - 1) & 1, kWaitNs, &g_abort))) {
                             ok = false;
+                            set_timeout();
                             break;
                         }
                         tc_fence_after();
@@ -433,9 +440,10 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 tc_fence_before();
                 mbar_arrive(smem_u32(&b_pfull[sb]));
             }
-            if (!ok) break;
             // ---- epilogue of the item: O / (sum + exp(sink)), inverse RoPE, BF16 store ----
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&b_ofull), it & 1, kWaitNs, &g_abort))) {
+            // (the four warps meet here: a failure anywhere makes all of them leave)
+            const bool got = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&b_ofull), it & 1, kWaitNs, &g_abort));
+            if (named_sync_or(1, kRows, !got)) {
                 ok = false;
                 break;
             }
@@ -451,21 +459,21 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 }
                 if (P.lse) P.lse[((int64_t)I.b * P.L + t) * P.H + h] = (m_run + log2f(l_run)) * 0.6931471805599453f;
             }
+            // staging: the item's query slot as two [128 rows][64 dims] BF16 halves in the 128-byte
+            // swizzle of the output tensor map (row r, 16-byte chunk c at sw128_off(r, c))
+            uint8_t *stage = sm + kQOff + (it & 1) * 32768;
             const uint32_t o_addr = tmem + lane_base + kOCol;
-            __nv_bfloat16 *orow = P.out + (((int64_t)I.b * P.L + (row_ok ? t : 0)) * P.H + h) * 128;
             {
                 // dims 0..63: normalised, no rotation
                 float o[64];
                 tmem_ld64_sync(o_addr, o);
-                if (row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dst[c] = make_uint4(pack_bf16x2(o[8 * c] * f, o[8 * c + 1] * f),
-                                            pack_bf16x2(o[8 * c + 2] * f, o[8 * c + 3] * f),
-                                            pack_bf16x2(o[8 * c + 4] * f, o[8 * c + 5] * f),
-                                            pack_bf16x2(o[8 * c + 6] * f, o[8 * c + 7] * f));
-                }
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(stage + sw128_off(r, c)) =
+                        make_uint4(pack_bf16x2(o[8 * c] * f, o[8 * c + 1] * f),
+                                   pack_bf16x2(o[8 * c + 2] * f, o[8 * c + 3] * f),
+                                   pack_bf16x2(o[8 * c + 4] * f, o[8 * c + 5] * f),
+                                   pack_bf16x2(o[8 * c + 6] * f, o[8 * c + 7] * f));
             }
             {
                 // dims 64..127: normalised, then rotated back at the row's position (pairs 64+i, 96+i)
@@ -473,31 +481,40 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 tmem_ld64_sync(o_addr + 64, o);
                 tc_fence_before();
                 mbar_arrive(smem_u32(&b_oempty));
-                if (row_ok) {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) o[e] *= f;
-                    if (P.d_rope == 64) {
-                        const float4 *rp = reinterpret_cast<const float4 *>(P.rope + (int64_t)t * 32);
+                for (int e = 0; e < 64; ++e) o[e] *= f;
+                if (P.d_rope == 64 && row_ok) {
+                    const float4 *rp = reinterpret_cast<const float4 *>(P.rope + (int64_t)t * 32);
 #pragma unroll
-                        for (int i2 = 0; i2 < 16; ++i2) {
-                            const float4 cs = __ldg(rp + i2);  // (cos, sin) of pairs 2*i2 and 2*i2 + 1
-                            const float x0 = o[2 * i2], y0 = o[32 + 2 * i2];
-                            const float x1 = o[2 * i2 + 1], y1 = o[33 + 2 * i2];
-                            o[2 * i2] = x0 * cs.x + y0 * cs.y;
-                            o[32 + 2 * i2] = -x0 * cs.y + y0 * cs.x;
-                            o[2 * i2 + 1] = x1 * cs.z + y1 * cs.w;
-                            o[33 + 2 * i2] = -x1 * cs.w + y1 * cs.z;
-                        }
+                    for (int i2 = 0; i2 < 16; ++i2) {
+                        const float4 cs = __ldg(rp + i2);  // (cos, sin) of pairs 2*i2 and 2*i2 + 1
+                        const float x0 = o[2 * i2], y0 = o[32 + 2 * i2];
+                        const float x1 = o[2 * i2 + 1], y1 = o[33 + 2 * i2];
+                        o[2 * i2] = x0 * cs.x + y0 * cs.y;
+                        o[32 + 2 * i2] = -x0 * cs.y + y0 * cs.x;
+                        o[2 * i2 + 1] = x1 * cs.z + y1 * cs.w;
+                        o[33 + 2 * i2] = -x1 * cs.w + y1 * cs.z;
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 64);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dst[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
-                                            pack_bf16x2(o[8 * c + 4], o[8 * c + 5]),
-                                            pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
                 }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(stage + 16384 + sw128_off(r, c)) =
+                        make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
+                                   pack_bf16x2(o[8 * c + 4], o[8 * c + 5]), pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+            }
+            fence_async_smem();
+            named_sync(1, kRows);
+            if (tid == 0) {
+                // rows past the sequence end (t >= L) lie outside the tensor map and are not written
+                const uint32_t sb0 = s_base + kQOff + (it & 1) * 32768;
+                tma_store_3d(&P.mo, sb0, 0, I.t0 * P.H, I.b);
+                tma_store_3d(&P.mo, sb0 + 16384, 64, I.t0 * P.H, I.b);
+                bulk_commit();
+                bulk_wait_read0();  // the slot may take the next query rows once the stores have read it
+                mbar_arrive(smem_u32(&b_qempty[it & 1]));
             }
         }
+        if (tid == 0) bulk_wait0();
         if (!ok) set_timeout();
     }
     tc_fence_before();
@@ -529,6 +546,8 @@ bool launch_hca_tc(const AttnArgs &a, cudaStream_t st) {
     const void *entries = widen ? a.ws : a.c_data;
     bool ok = make_map_3d(&P.mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, 128, L * H, B, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map_3d(&P.mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, 128, L * H, B, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map_3d(&P.mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, entries, 128, ncap, B, 64, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map_3d(&P.mkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kv_rope, 128, L, B, 64, kMaxKeys,
