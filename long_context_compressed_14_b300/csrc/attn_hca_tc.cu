@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         bool ok = true;
         int n = 0;
+        int store_slot = -1;  // thread 0: query slot whose output stores are still to be confirmed
         for (int it = 0; it < n_it_cta && ok; ++it) {
             const Item I = item_of(P, (int)blockIdx.x + it * (int)gridDim.x);
             const int t = I.t0 + r / P.H, h = r % P.H;
@@ -402,8 +403,14 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 const float neg_m = -m_run;
                 const bool row_live = m_run != -INFINITY;
                 if (__all_sync(0xffffffffu, row_live)) {
+                    // scale * s - max for two keys per packed FMA, then the hardware exp2
+                    const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2), nm2 = f2_pack(neg_m, neg_m);
 #pragma unroll
-                    for (int e = 0; e < 128; ++e) sv[e] = fast_exp2(fmaf(sv[e], P.scale_log2, neg_m));
+                    for (int e = 0; e < 128; e += 2) {
+                        const float2 x = f2_unpack(f2_fma(f2_pack(sv[e], sv[e + 1]), sc2, nm2));
+                        sv[e] = fast_exp2(x.x);
+                        sv[e + 1] = fast_exp2(x.y);
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 128; ++e) sv[e] = row_live ? fast_exp2(fmaf(sv[e], P.scale_log2, neg_m)) : 0.0f;
@@ -412,14 +419,15 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
 #pragma unroll
                     for (int e = 0; e < 16; ++e) sx[e] = row_live ? fast_exp2(fmaf(sx[e], P.scale_log2, neg_m)) : 0.0f;
                 }
-                // P as BF16 pairs into the first columns of the slot (its scores are in registers)
-                float ls8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                // P as BF16 pairs into the first columns of the slot (its scores are in registers);
+                // the row sum in four packed pair accumulators
+                uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     float w[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        ls8[(e >> 1) & 7] += sv[c0 + e] + sv[c0 + e + 1];
+                        ls2[(e >> 1) & 3] = f2_add(ls2[(e >> 1) & 3], f2_pack(sv[c0 + e], sv[c0 + e + 1]));
                         w[e >> 1] = __uint_as_float(pack_bf16x2(sv[c0 + e], sv[c0 + e + 1]));
                     }
                     tmem_st16(s_addr + (c0 >> 1), w);
@@ -428,17 +436,27 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                     float w[16];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
-                        ls8[e >> 1] += sx[e] + sx[e + 1];
+                        ls2[(e >> 1) & 3] = f2_add(ls2[(e >> 1) & 3], f2_pack(sx[e], sx[e + 1]));
                         w[e >> 1] = __uint_as_float(pack_bf16x2(sx[e], sx[e + 1]));
                     }
 #pragma unroll
                     for (int e = 8; e < 16; ++e) w[e] = 0.0f;  // columns 72..79: beyond the 144 keys' P
                     tmem_st16(s_addr + 64, w);
                 }
-                l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+                {
+                    const float2 a = f2_unpack(f2_add(ls2[0], ls2[1])), b = f2_unpack(f2_add(ls2[2], ls2[3]));
+                    l_run += (a.x + a.y) + (b.x + b.y);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(smem_u32(&b_pfull[sb]));
+                if (store_slot >= 0) {
+                    // the previous item's output stores have long read their staging by now: hand
+                    // that query slot back to the producer
+                    bulk_wait_read0();
+                    mbar_arrive(smem_u32(&b_qempty[store_slot]));
+                    store_slot = -1;
+                }
             }
             // ---- epilogue of the item: O / (sum + exp(sink)), inverse RoPE, BF16 store ----
             // (the four warps meet here: a failure anywhere makes all of them leave)
@@ -510,8 +528,7 @@ __global__ void __launch_bounds__(hca_tc::kThreads, 1) hca_tc_kernel(const __gri
                 tma_store_3d(&P.mo, sb0, 0, I.t0 * P.H, I.b);
                 tma_store_3d(&P.mo, sb0 + 16384, 64, I.t0 * P.H, I.b);
                 bulk_commit();
-                bulk_wait_read0();  // the slot may take the next query rows once the stores have read it
-                mbar_arrive(smem_u32(&b_qempty[it & 1]));
+                store_slot = it & 1;  // released after the next item's first tile
             }
         }
         if (tid == 0) bulk_wait0();
