@@ -185,7 +185,8 @@ int csa_quant_mxfp4_rows(const float *x, int64_t rows, int cols, uint8_t *codes,
  *   kv [B, L, d] act_t;  z [B, L, 2] float;  kI_raw [B, L, d_I] float or NULL;
  *   rope_tab: csa_rope_table with rope_len >= ceil(L/m) * m;
  *   C: entries [B, ceil(L/m), ...];  KI: [B, ceil(L/m), d_I] (ignored if kI_raw is NULL);
- *   kv_rope [B, L, d] act_t or NULL. */
+ *   kv_rope [B, L, d] act_t or NULL. kv, kI_raw, kv_rope and rope_tab must be 16-byte aligned
+ *   (they are read and written in 16-byte chunks); otherwise CSA_ERR_INVALID. */
 int kv_compress(const csa_params *p, const void *kv, const float *z, const float *kI_raw,
                 const float *rope_tab, const csa_entries *C, const csa_index_rows *KI,
                 void *kv_rope, csa_stream_t stream);

@@ -348,10 +348,10 @@ int kv_compress(const csa_params *p, const void *kv, const float *z, const float
     int s = check(p, CSA_OP_HCA_PREFILL);
     if (s) return s;
     if (!kv || !z || !aligned16(kv) || !entries_ok(p, C)) return CSA_ERR_INVALID;
-    if (p->d_rope > 0 && !rope_tab) return CSA_ERR_INVALID;
+    if (p->d_rope > 0 && (!rope_tab || !aligned16(rope_tab))) return CSA_ERR_INVALID;
     if (kI_raw) {
         if (p->idx_t != CSA_F32 && p->idx_t != CSA_FP8E4M3 && p->idx_t != CSA_MXFP4) return CSA_ERR_INVALID;
-        if (!index_rows_ok(p, KI) || p->d_I != kDI) return CSA_ERR_INVALID;
+        if (!index_rows_ok(p, KI) || p->d_I != kDI || !aligned16(kI_raw)) return CSA_ERR_INVALID;
     }
     if (kv_rope && !aligned16(kv_rope)) return CSA_ERR_INVALID;
     CompressArgs a{};

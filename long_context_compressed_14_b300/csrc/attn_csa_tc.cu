@@ -698,15 +698,35 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
                 if (cl > 0) {
                     tmem_ld32_sync(s_addr, p);
                     const float4 *m4 = reinterpret_cast<const float4 *>(s_m + h0);
+                    if (__all_sync(0xffffffffu, valid)) {
+                        // every key of the warp valid: two logits per packed FMA
+                        const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2);
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 mm = m4[e4];
-                        const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 mm = m4[e4];
+                            const float2 x01 = f2_unpack(f2_fma(f2_pack(p[4 * e4], p[4 * e4 + 1]), sc2, f2_pack(-mm.x, -mm.y)));
+                            const float2 x23 =
+                                f2_unpack(f2_fma(f2_pack(p[4 * e4 + 2], p[4 * e4 + 3]), sc2, f2_pack(-mm.z, -mm.w)));
+                            over |= x01.x > kOver;
+                            over |= x01.y > kOver;
+                            over |= x23.x > kOver;
+                            over |= x23.y > kOver;
+                            p[4 * e4] = fast_exp2(x01.x);
+                            p[4 * e4 + 1] = fast_exp2(x01.y);
+                            p[4 * e4 + 2] = fast_exp2(x23.x);
+                            p[4 * e4 + 3] = fast_exp2(x23.y);
+                        }
+                    } else {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float x = valid ? fmaf(p[4 * e4 + q], P.scale_log2, -mv[q]) : -INFINITY;
-                            over |= x > kOver;
-                            p[4 * e4 + q] = fast_exp2(x);
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 mm = m4[e4];
+                            const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float x = valid ? fmaf(p[4 * e4 + q], P.scale_log2, -mv[q]) : -INFINITY;
+                                over |= x > kOver;
+                                p[4 * e4 + q] = fast_exp2(x);
+                            }
                         }
                     }
                 }
@@ -783,8 +803,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int h = 8 * c4 + 2 * e;
-                        lpart[h] += p[h];
-                        lpart[h + 1] += p[h + 1];
+                        const float2 l2 = f2_unpack(f2_add(f2_pack(lpart[h], lpart[h + 1]), f2_pack(p[h], p[h + 1])));
+                        lpart[h] = l2.x;
+                        lpart[h + 1] = l2.y;
                         pk[e] = pack2(p[h], p[h + 1]);
                     }
                     *reinterpret_cast<uint4 *>(prow + sw128_off(kl, 4 * wg + c4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);

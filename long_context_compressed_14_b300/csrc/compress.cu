@@ -71,11 +71,145 @@ void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, f
 // kv_compress: one CTA (4 warps) per entry j of sequence b.
 //   window rows [(j-1)m, (j+1)m) ∩ [0, L); weight of row t = exp(z[t, set] - max) with set 0
 //   for the own block (t >= jm) and set 1 for the previous block; normalised at the end.
-//   Warp g accumulates the rows g, g+4, ...; lane l owns dims {l, l+32, l+64, l+96} of the
-//   KV row (so that RoPE pairs (64+i, 96+i) sit in one lane) and dims {l, l+32} of the
-//   indexer-key row.
+//   Rows are read in 16-byte chunks: a warp instruction covers two BF16 rows (one FP32 row) of
+//   KV and two indexer-key rows; each thread accumulates the 8 (4) dims of its chunk over its
+//   rows, the partial sums meet in shared memory, and warp 0 finishes the entry with lane l
+//   holding dims {l, l+32, l+64, l+96} (RoPE pairs (64+i, 96+i) in one lane) and indexer dims
+//   {l, l+32}. Rows of the own block are also written back rotated at their own position
+//   (kv_rope); the two dims of a RoPE pair sit in chunks 32/V apart and meet by a shuffle.
 // ---------------------------------------------------------------------------------------
 constexpr int kMaxWindow = 2 * 1024;
+
+__device__ __forceinline__ void load16(const float *p, float (&x)[4]) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
+        x[2 * k] = f.x;
+        x[2 * k + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void store16(float *p, const float (&y)[4]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(y[0], y[1], y[2], y[3]);
+}
+__device__ __forceinline__ void store16(__nv_bfloat16 *p, const float (&y)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(y[2 * k], y[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t *>(&b2);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One 16-byte chunk x (dims d0 .. d0 + V - 1) of window row t of one sequence, by every lane of
+// a warp together: acc += wt * x; a row of the entry's own block (own) also goes back rotated at
+// its own position t into kv_rope (the two dims of a RoPE pair sit in chunks 32 / V apart and
+// meet by a shuffle).
+template <typename ActT>
+__device__ __forceinline__ void kv_load(const ActT *__restrict__ kvb, int64_t t, bool have, int d0,
+                                        float (&x)[16 / sizeof(ActT)]) {
+    if (have) {
+        load16(kvb + t * kD + d0, x);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 16 / (int)sizeof(ActT); ++k) x[k] = 0.0f;
+    }
+}
+
+template <typename ActT, bool WITH_KVROPE>
+__device__ __forceinline__ void kv_row_chunk(const float (&x)[16 / sizeof(ActT)], ActT *__restrict__ kvr_b,
+                                             const float2 *__restrict__ rope, int half, int64_t t, bool own, int d0,
+                                             float wt, float (&acc)[16 / sizeof(ActT)]) {
+    constexpr int V = 16 / (int)sizeof(ActT);
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] = fmaf(wt, x[k], acc[k]);
+    if (WITH_KVROPE) {
+        float y[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) y[k] = x[k];
+        if (half == 32) {
+            float other[V];
+#pragma unroll
+            for (int k = 0; k < V; ++k) other[k] = __shfl_xor_sync(0xffffffffu, x[k], 32 / V);
+            if (own && d0 >= 64) {
+                const int ip = (d0 - 64) & 31;  // pair index of the chunk's first dim
+                const float4 *r4 = reinterpret_cast<const float4 *>(rope + t * half + ip);
+#pragma unroll
+                for (int k2 = 0; k2 < V / 2; ++k2) {
+                    const float4 cs = __ldg(r4 + k2);  // (cos, sin) of pairs ip + 2 k2 and ip + 2 k2 + 1
+                    const int k = 2 * k2;
+                    y[k] = d0 < 96 ? x[k] * cs.x - other[k] * cs.y : other[k] * cs.y + x[k] * cs.x;
+                    y[k + 1] = d0 < 96 ? x[k + 1] * cs.z - other[k + 1] * cs.w : other[k + 1] * cs.w + x[k + 1] * cs.z;
+                }
+            }
+        }
+        if (own) store16(kvr_b + t * kD + d0, y);
+    }
+}
+
+// The end of an entry, by one warp holding c[e] = dim lane + 32 e of the weighted sum (before
+// RoPE) and (k0, k1) = indexer dims (lane, lane + 32): RoPE at the entry position (j+1)m - 1 and
+// storage per KV_T and IDX_T.
+template <int KV_T, int IDX_T, bool WITH_KI>
+__device__ __forceinline__ void finish_entry(float (&c)[4], float k0, float k1, int j, int b, int m, int N, int d_rope,
+                                             const float2 *__restrict__ rope, void *__restrict__ c_data,
+                                             __nv_bfloat16 *__restrict__ c_rope, float *__restrict__ c_scale,
+                                             void *__restrict__ ki_data, float *__restrict__ ki_scale,
+                                             uint8_t *__restrict__ ki_e8) {
+    const int lane = threadIdx.x & 31;
+    const int half = d_rope / 2;
+    if (half == 32) {
+        const int64_t pos = (int64_t)(j + 1) * m - 1;
+        const float2 cs = rope[pos * half + lane];
+        const float a = c[2], bb = c[3];
+        c[2] = a * cs.x - bb * cs.y;
+        c[3] = a * cs.y + bb * cs.x;
+    }
+    const int64_t row = (int64_t)b * N + j;
+    if (KV_T == CSA_F32) {
+        float *dst = reinterpret_cast<float *>(c_data) + row * kD;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = c[e];
+    } else if (KV_T == CSA_BF16) {
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(c_data) + row * kD;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(c[e]);
+    } else if (KV_T == CSA_NVFP4) {  // the whole rotated entry in NVFP4 (fp4.cuh)
+        nvfp4_row_store(c, reinterpret_cast<uint8_t *>(c_data) + row * kNvfp4RowBytes);
+    } else {  // MIXED: dims 0..63 FP8 + row scale, dims 64..127 BF16
+        float amax = warp_max(fmaxf(fabsf(c[0]), fabsf(c[1])));
+        const float scale = __fdiv_rn(amax, 448.0f);
+        uint8_t *dst = reinterpret_cast<uint8_t *>(c_data) + row * 64;
+        dst[lane] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(c[0], scale)) : (uint8_t)0;
+        dst[lane + 32] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(c[1], scale)) : (uint8_t)0;
+        if (lane == 0) c_scale[row] = scale;
+        __nv_bfloat16 *rr = c_rope + row * 64;
+        rr[lane] = __float2bfloat16_rn(c[2]);
+        rr[lane + 32] = __float2bfloat16_rn(c[3]);
+    }
+    if (WITH_KI) {
+        if (IDX_T == CSA_F32) {
+            float *dst = reinterpret_cast<float *>(ki_data) + row * kDI;
+            dst[lane] = k0;
+            dst[lane + 32] = k1;
+        } else if (IDX_T == CSA_MXFP4) {
+            mxfp4_row_store(k0, k1, reinterpret_cast<uint8_t *>(ki_data) + row * (kDI / 2), ki_e8 + row * 2);
+        } else {
+            const float amax = warp_max(fmaxf(fabsf(k0), fabsf(k1)));
+            const float scale = __fdiv_rn(amax, 448.0f);
+            uint8_t *dst = reinterpret_cast<uint8_t *>(ki_data) + row * kDI;
+            dst[lane] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(k0, scale)) : (uint8_t)0;
+            dst[lane + 32] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(k1, scale)) : (uint8_t)0;
+            if (lane == 0) ki_scale[row] = scale;
+        }
+    }
+}
 
 template <typename ActT, int KV_T, int IDX_T, bool WITH_KI, bool WITH_KVROPE>
 __global__ void __launch_bounds__(128)
@@ -85,8 +219,12 @@ kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
                    float *__restrict__ c_scale, void *__restrict__ ki_data,
                    float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope, int L,
                    int m, int N, int d_rope) {
+    constexpr int V = 16 / (int)sizeof(ActT);  // dims per 16-byte chunk: 8 (BF16) or 4 (FP32)
+    constexpr int CPR = kD / V;                // chunks per KV row: 16 or 32
+    constexpr int RPW = 32 / CPR;              // KV rows per warp instruction: 2 or 1
+    constexpr int KG = 8;                      // partial-sum groups (4 warps x 2 rows per instruction)
     __shared__ float s_w[kMaxWindow];
-    __shared__ float s_red[4][kD + kDI];
+    __shared__ __align__(16) float s_red[KG][kD + kDI];
     __shared__ float s_scalar[8];
 
     const int j = blockIdx.x, b = blockIdx.y;
@@ -122,40 +260,41 @@ kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
     den = (s_scalar[4] + s_scalar[5]) + (s_scalar[6] + s_scalar[7]);
 
     const int half = d_rope / 2;  // 32 or 0
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float acck[2] = {0.f, 0.f};
     const ActT *kvb = kv + (int64_t)b * L * kD;
-    for (int i = warp; i < n; i += 4) {
-        const int64_t t = lo + i;
-        const float wt = s_w[i];
-        float x[4];
+    // KV rows: thread = chunk cl of row i0 + rl
+    {
+        const int cl = lane % CPR, rl = lane / CPR;
+        const int d0 = cl * V;  // first dim of this thread's chunk
+        float acc[V];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = to_f(kvb[t * kD + lane + 32 * e]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = fmaf(wt, x[e], acc[e]);
-        if (WITH_KI) {
-            const float *kr = kI_raw + ((int64_t)b * L + t) * kDI;
-            acck[0] = fmaf(wt, kr[lane], acck[0]);
-            acck[1] = fmaf(wt, kr[lane + 32], acck[1]);
+        for (int k = 0; k < V; ++k) acc[k] = 0.0f;
+        for (int i0 = warp * RPW; i0 < n; i0 += 4 * RPW) {  // trip count uniform over the warp
+            const int i = i0 + rl;
+            const bool have = i < n;
+            float x[V];
+            kv_load(kvb, lo + i, have, d0, x);
+            kv_row_chunk<ActT, WITH_KVROPE>(x, kv_rope + (int64_t)b * L * kD, rope, half, lo + i,
+                                            have && lo + i >= own0, d0, have ? s_w[i] : 0.0f, acc);
         }
-        if (WITH_KVROPE && t >= own0) {
-            // this raw row belongs to block j: write it rotated at its own position t
-            float y[4] = {x[0], x[1], x[2], x[3]};
-            if (half == 32) {
-                const float2 cs = rope[t * half + lane];
-                y[2] = x[2] * cs.x - x[3] * cs.y;
-                y[3] = x[2] * cs.y + x[3] * cs.x;
-            }
-            ActT *dst = kv_rope + ((int64_t)b * L + t) * kD;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = from_f<ActT>(y[e]);
-        }
+        for (int k = 0; k < V; ++k) s_red[warp * RPW + rl][d0 + k] = acc[k];
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s_red[warp][lane + 32 * e] = acc[e];
+    // indexer-key rows (64 floats = 16 chunks): thread = chunk kc of row i0 + kr
     if (WITH_KI) {
-        s_red[warp][kD + lane] = acck[0];
-        s_red[warp][kD + lane + 32] = acck[1];
+        const int kc = lane & 15, kr = lane >> 4;
+        float acck[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int i0 = warp * 2; i0 < n; i0 += 8) {
+            const int i = i0 + kr;
+            if (i < n) {
+                float x[4];
+                load16(kI_raw + ((int64_t)b * L + lo + i) * kDI + kc * 4, x);
+                const float wt = s_w[i];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acck[k] = fmaf(wt, x[k], acck[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s_red[warp * 2 + kr][kD + kc * 4 + k] = acck[k];
     }
     __syncthreads();
     if (warp != 0) return;
@@ -165,56 +304,112 @@ kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const int dd = lane + 32 * e;
-        c[e] = ((s_red[0][dd] + s_red[1][dd]) + (s_red[2][dd] + s_red[3][dd])) * inv;
-    }
-    if (half == 32) {
-        const int64_t pos = (int64_t)(j + 1) * m - 1;
-        const float2 cs = rope[pos * half + lane];
-        const float a = c[2], bb = c[3];
-        c[2] = a * cs.x - bb * cs.y;
-        c[3] = a * cs.y + bb * cs.x;
-    }
-    const int64_t row = (int64_t)b * N + j;
-    if (KV_T == CSA_F32) {
-        float *dst = reinterpret_cast<float *>(c_data) + row * kD;
+        float sum = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = c[e];
-    } else if (KV_T == CSA_BF16) {
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(c_data) + row * kD;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(c[e]);
-    } else if (KV_T == CSA_NVFP4) {  // the whole rotated entry in NVFP4 (fp4.cuh)
-        nvfp4_row_store(c, reinterpret_cast<uint8_t *>(c_data) + row * kNvfp4RowBytes);
-    } else {  // MIXED: dims 0..63 FP8 + row scale, dims 64..127 BF16
-        float amax = warp_max(fmaxf(fabsf(c[0]), fabsf(c[1])));
-        const float scale = __fdiv_rn(amax, 448.0f);
-        uint8_t *dst = reinterpret_cast<uint8_t *>(c_data) + row * 64;
-        dst[lane] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(c[0], scale)) : (uint8_t)0;
-        dst[lane + 32] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(c[1], scale)) : (uint8_t)0;
-        if (lane == 0) c_scale[row] = scale;
-        __nv_bfloat16 *rr = c_rope + row * 64;
-        rr[lane] = __float2bfloat16_rn(c[2]);
-        rr[lane + 32] = __float2bfloat16_rn(c[3]);
+        for (int g = 0; g < 4 * RPW; ++g) sum += s_red[g][dd];
+        c[e] = sum * inv;
     }
+    float k0 = 0.0f, k1 = 0.0f;
     if (WITH_KI) {
-        float k0 = ((s_red[0][kD + lane] + s_red[1][kD + lane]) + (s_red[2][kD + lane] + s_red[3][kD + lane])) * inv;
-        float k1 = ((s_red[0][kD + lane + 32] + s_red[1][kD + lane + 32]) +
-                    (s_red[2][kD + lane + 32] + s_red[3][kD + lane + 32])) * inv;
-        if (IDX_T == CSA_F32) {
-            float *dst = reinterpret_cast<float *>(ki_data) + row * kDI;
-            dst[lane] = k0;
-            dst[lane + 32] = k1;
-        } else if (IDX_T == CSA_MXFP4) {
-            mxfp4_row_store(k0, k1, reinterpret_cast<uint8_t *>(ki_data) + row * (kDI / 2), ki_e8 + row * 2);
-        } else {
-            const float amax = warp_max(fmaxf(fabsf(k0), fabsf(k1)));
-            const float scale = __fdiv_rn(amax, 448.0f);
-            uint8_t *dst = reinterpret_cast<uint8_t *>(ki_data) + row * kDI;
-            dst[lane] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(k0, scale)) : (uint8_t)0;
-            dst[lane + 32] = scale > 0.0f ? f32_to_e4m3(__fdiv_rn(k1, scale)) : (uint8_t)0;
-            if (lane == 0) ki_scale[row] = scale;
+#pragma unroll
+        for (int g = 0; g < KG; ++g) {
+            k0 += s_red[g][kD + lane];
+            k1 += s_red[g][kD + lane + 32];
+        }
+        k0 *= inv;
+        k1 *= inv;
+    }
+    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, m, N, d_rope, rope, c_data, c_rope, c_scale, ki_data, ki_scale,
+                                       ki_e8);
+}
+
+
+// kv_compress for small m (2m <= 32 window rows): one warp per entry, eight entries per CTA. The
+// window weights live in the lanes (lane i = row i), each KV row is read as 16-byte chunks (two
+// BF16 rows or one FP32 row per warp instruction), and the entry's sums meet in the warp's own
+// shared-memory row for the storage step; no CTA-wide barrier.
+template <typename ActT, int KV_T, int IDX_T, bool WITH_KI, bool WITH_KVROPE>
+__global__ void __launch_bounds__(256)
+kv_compress_warp_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
+                        const float *__restrict__ kI_raw, const float2 *__restrict__ rope,
+                        void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
+                        float *__restrict__ c_scale, void *__restrict__ ki_data,
+                        float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope,
+                        int L, int m, int N, int d_rope) {
+    constexpr int V = 16 / (int)sizeof(ActT);
+    constexpr int CPR = kD / V;
+    constexpr int RPW = 32 / CPR;
+    __shared__ __align__(16) float s_c[8][kD + kDI];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = blockIdx.x * 8 + warp, b = blockIdx.y;
+    if (j >= N) return;  // (the warp leaves as a whole; nothing below is CTA-wide)
+    const int64_t lo = (int64_t)(j - 1) * m < 0 ? 0 : (int64_t)(j - 1) * m;
+    const int64_t hi = (int64_t)(j + 1) * m > L ? (int64_t)L : (int64_t)(j + 1) * m;
+    const int n = (int)(hi - lo);  // <= 32
+    const int64_t own0 = (int64_t)j * m;
+    // softmax weights: lane i holds row i's unnormalised weight
+    float lg = -INFINITY;
+    if (lane < n) {
+        const int64_t t = lo + lane;
+        lg = z[((int64_t)b * L + t) * 2 + (t >= own0 ? 0 : 1)];
+    }
+    const float mx = warp_max(lg);
+    const float e = lane < n ? expf(lg - mx) : 0.0f;
+    const float inv = 1.0f / warp_sum(e);
+    const int half = d_rope / 2;
+    const ActT *kvb = kv + (int64_t)b * L * kD;
+    {
+        const int cl = lane % CPR, rl = lane / CPR;
+        const int d0 = cl * V;
+        float acc[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) acc[k] = 0.0f;
+        for (int i0 = 0; i0 < n; i0 += RPW) {
+            const int i = i0 + rl;
+            const bool have = i < n;
+            const float wt = __shfl_sync(0xffffffffu, e, i & 31);
+            float x[V];
+            kv_load(kvb, lo + i, have, d0, x);
+            kv_row_chunk<ActT, WITH_KVROPE>(x, kv_rope + (int64_t)b * L * kD, rope, half, lo + i,
+                                            have && lo + i >= own0, d0, have ? wt : 0.0f, acc);
+        }
+        if (RPW == 2) {
+#pragma unroll
+            for (int k = 0; k < V; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
+        }
+        if (rl == 0) {
+#pragma unroll
+            for (int k = 0; k < V; ++k) s_c[warp][d0 + k] = acc[k];
         }
     }
+    if (WITH_KI) {
+        const int kc = lane & 15, kr = lane >> 4;
+        float acck[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int i0 = 0; i0 < n; i0 += 2) {
+            const int i = i0 + kr;
+            const float wt = __shfl_sync(0xffffffffu, e, i & 31);
+            if (i < n) {
+                float x[4];
+                load16(kI_raw + ((int64_t)b * L + lo + i) * kDI + kc * 4, x);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acck[k] = fmaf(wt, x[k], acck[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acck[k] += __shfl_xor_sync(0xffffffffu, acck[k], 16);
+        if (kr == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) s_c[warp][kD + kc * 4 + k] = acck[k];
+        }
+    }
+    __syncwarp();
+    float c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = s_c[warp][lane + 32 * q] * inv;
+    const float k0 = WITH_KI ? s_c[warp][kD + lane] * inv : 0.0f;
+    const float k1 = WITH_KI ? s_c[warp][kD + lane + 32] * inv : 0.0f;
+    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, m, N, d_rope, rope, c_data, c_rope, c_scale, ki_data, ki_scale,
+                                       ki_e8);
 }
 
 template <typename ActT, int KV_T, int IDX_T>
@@ -224,10 +419,18 @@ static void launch_compress_t(const CompressArgs &a, cudaStream_t st) {
     ActT *kvr = reinterpret_cast<ActT *>(a.kv_rope);
     const float2 *rope = reinterpret_cast<const float2 *>(a.rope_tab);
     auto *cr = reinterpret_cast<__nv_bfloat16 *>(a.c_rope);
+    // small m: one warp per entry (the window's weights fit the lanes); else one CTA per entry
+    const bool per_warp = 2 * a.m <= 32;
+    const dim3 wgrid((a.N + 7) / 8, a.B);
 #define CSA_LAUNCH(KI, KVR)                                                                          \
-    kv_compress_kernel<ActT, KV_T, IDX_T, KI, KVR><<<grid, 128, 0, st>>>(                            \
-        kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, \
-        a.d_rope)
+    if (per_warp)                                                                                    \
+        kv_compress_warp_kernel<ActT, KV_T, IDX_T, KI, KVR><<<wgrid, 256, 0, st>>>(                  \
+            kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, \
+            a.d_rope);                                                                               \
+    else                                                                                             \
+        kv_compress_kernel<ActT, KV_T, IDX_T, KI, KVR><<<grid, 128, 0, st>>>(                        \
+            kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, \
+            a.d_rope)
     if (a.kI_raw && a.kv_rope) CSA_LAUNCH(true, true);
     else if (a.kI_raw) CSA_LAUNCH(true, false);
     else if (a.kv_rope) CSA_LAUNCH(false, true);
