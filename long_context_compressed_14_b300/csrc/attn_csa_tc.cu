@@ -672,7 +672,9 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
         for (int it = 0; it < n_tok_cta; ++it) {
             const int qs = it & 1;
             note(mbar_wait(smem_u32(&b_qfull[qs]), (it >> 1) & 1, kWaitNs, &g_abort));
-            if (tid < kH) s_m[tid] = -INFINITY;
+            // each warpgroup's first warp resets its own heads' maxima: the same warp read them
+            // last, in the previous token's reduction (the warpgroups are not in step there)
+            if ((warp & 3) == 0) s_m[h0 + lane] = -INFINITY;
             if (named_sync_or(kBarSoftmax, kSoftmax, !okl)) break;
             const TokenMeta mt = meta[qs];
             mbar_arrive(smem_u32(&b_qempty[qs]));

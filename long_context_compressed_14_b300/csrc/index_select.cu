@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(tk::kThreads, 4) cand_select_kernel(IselRowArg
     uint32_t *hist = dyn;                 // [kBins]
     uint32_t *bm_gt = hist + kBins;       // [nw], then bm_eq [nw]
     __shared__ int s_tmp[kWarps];
-    __shared__ int s_res[2];
+    __shared__ int s_res[3];
     const int r = blockIdx.x;
     const int64_t t = (int64_t)a.t0 + r;
     int32_t *out = a.out + ((int64_t)a.b * a.L + t) * a.k;
@@ -483,7 +483,8 @@ __global__ void __launch_bounds__(tk::kThreads, 4) cand_select_kernel(IselRowArg
         idx[u] = live ? (int32_t)v.x : -1;
     }
     // radix rounds over the key bits 31..21, 20..10 and 9..0: the k-th largest key K* and how
-    // many keys equal to it are taken
+    // many keys equal to it are taken. A round whose threshold bin is taken whole ends the
+    // search: the key bits examined so far (under `mask`) already fix the selection.
     uint32_t prefix = 0, mask = 0;
     int need = k;
 #pragma unroll 1
@@ -496,18 +497,20 @@ __global__ void __launch_bounds__(tk::kThreads, 4) cand_select_kernel(IselRowArg
         for (int u = 0; u < kSelPer; ++u)
             if (idx[u] >= 0 && (key[u] & mask) == prefix) atomicAdd(&hist[(key[u] >> shift) & wm], 1u);
         __syncthreads();
-        int bb, above;
-        find_threshold_bin(hist, kBins, need, s_tmp, s_res, &bb, &above);
+        int bb, above, cnt;
+        find_threshold_bin(hist, kBins, need, s_tmp, s_res, &bb, &above, &cnt);
         prefix |= (uint32_t)bb << shift;
         mask |= wm << shift;
         need -= above;
+        if (cnt == need) break;  // (the same in every thread)
     }
 #pragma unroll
     for (int u = 0; u < kSelPer; ++u) {
         if (idx[u] < 0) continue;
         const int i = idx[u];
-        if (key[u] > prefix) atomicOr(&bm_gt[i >> 5], 1u << (i & 31));
-        else if (key[u] == prefix) atomicOr(&bm_eq[i >> 5], 1u << (i & 31));
+        const uint32_t km = key[u] & mask;
+        if (km > prefix) atomicOr(&bm_gt[i >> 5], 1u << (i & 31));
+        else if (km == prefix) atomicOr(&bm_eq[i >> 5], 1u << (i & 31));
     }
     __syncthreads();
     emit_selection(bm_gt, bm_eq, nw, need, k, out, s_tmp);

@@ -83,10 +83,11 @@ __device__ __forceinline__ void for_each_key(const float *S, int n, F &&fn) {
 
 // In a histogram of `nbins` bins (nbins / kThreads per thread), finds the bin b holding the
 // `want`-th largest element (1-based, counted from the top bin down): *bin = b and
-// *above = number of elements in bins above b. Block-wide; every thread gets the result.
+// *above = number of elements in bins above b; with `count`, also the elements in bin b (s_res
+// then needs three ints). Block-wide; every thread gets the result.
 template <int NT = tk::kThreads>
 __device__ __forceinline__ void find_threshold_bin(const uint32_t *hist, int nbins, int want, int *s_tmp,
-                                                   int *s_res, int *bin, int *above) {
+                                                   int *s_res, int *bin, int *above, int *count = nullptr) {
     const int per = nbins / NT;  // 4 (2048 bins) or 1 (<= 512 bins, padded)
     // thread i owns bins [per*i, per*i + per); reverse order so that an exclusive prefix sum
     // in thread order counts the bins above
@@ -102,6 +103,7 @@ __device__ __forceinline__ void find_threshold_bin(const uint32_t *hist, int nbi
             if (run < want && run + h >= want) {
                 s_res[0] = per * owner + q;
                 s_res[1] = run;
+                if (count) s_res[2] = h;
             }
             run += h;
         }
@@ -109,6 +111,7 @@ __device__ __forceinline__ void find_threshold_bin(const uint32_t *hist, int nbi
     __syncthreads();
     *bin = s_res[0];
     *above = s_res[1];
+    if (count) *count = s_res[2];
     __syncthreads();
 }
 
