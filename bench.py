@@ -555,6 +555,7 @@ def run_mine(args, rank, world, local_rank):
     if wl.kind == "pair" and not args.no_decode:
         line["decode"] = measure_decode(lib, args, pk)
         line["decode_v41_cache"] = measure_decode(lib, args, pk, "decode_v41_b16_ctx131072")
+        line["decode_fp4"] = measure_decode(lib, args, pk, "decode_fp4_b16_ctx131072")
     if wl.kind == "pair" and not args.no_projections:
         line["projections"] = measure_projections(lib, args, wl, pk)
     if world == 1 and not args.no_cpu_baseline:

@@ -494,28 +494,37 @@ int csa_decode(const csa_params *p, const void *q, const int32_t *ctx_len, const
     // selection lists: the two counters per row right after the histogram (one memset clears both)
     int *sel_cnt = p->topk > 0 ? reinterpret_cast<int *>(wsc + sbytes + ibytes + hbytes) : nullptr;
     void *part = need > 0 ? wsc + sbytes + ibytes + hbytes + dbytes : nullptr;
-    // MXFP4 indexer operands: their exact FP8 form after the split-KV partials
+    // MXFP4 indexer operands: read as stored by the FP4 scan; otherwise (head counts it does
+    // not take) their exact FP8 form, after the split-KV partials, for the FP8 scan
+    IndexArgs ia{};
+    ia.qI = qI ? qI->data : nullptr; ia.qI_scale = qI ? qI->scale : nullptr; ia.qI_e8 = qI ? qI->mx_scale : nullptr;
+    ia.KI = KI ? KI->data : nullptr; ia.KI_scale = KI ? KI->scale : nullptr; ia.KI_e8 = KI ? KI->mx_scale : nullptr;
+    ia.w = w; ia.ctx = ctx_len; ia.ldS = score_ld(p);
+    ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap; ia.idx_t = p->idx_t;
+    ia.decode = 1;
+    const bool fp4_scan = p->topk > 0 && decode_index_fp4_supported(ia);
     csa_index_rows q8{}, k8{};
-    if (p->topk > 0 && p->idx_t == CSA_MXFP4) {
+    if (p->topk > 0 && p->idx_t == CSA_MXFP4 && !fp4_scan) {
         char *w8 = wsc + sbytes + ibytes + hbytes + dbytes + decode_split_bytes(p, 0);
         mxfp4_rows_to_fp8(qI, (int64_t)p->B * p->H_I, w8, &q8, st);
         mxfp4_rows_to_fp8(KI, (int64_t)p->B * ncap, w8 + fp8_rows_bytes((int64_t)p->B * p->H_I), &k8, st);
-        qI = &q8;
-        KI = &k8;
+        ia.qI = q8.data; ia.qI_scale = q8.scale; ia.KI = k8.data; ia.KI_scale = k8.scale;
+        ia.idx_t = CSA_FP8E4M3;
     }
-    const int idx_t_eff = p->idx_t == CSA_MXFP4 ? (int)CSA_FP8E4M3 : p->idx_t;
     if (p->topk > 0) {
         float *S = reinterpret_cast<float *>(ws);
         idx = topk_out ? topk_out : reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + sbytes);
-        IndexArgs ia{};
-        ia.qI = qI->data; ia.qI_scale = qI->scale; ia.KI = KI->data; ia.KI_scale = KI->scale;
-        ia.w = w; ia.ctx = ctx_len; ia.S = S; ia.ldS = score_ld(p);
-        ia.B = p->B; ia.L = p->L; ia.H_I = p->H_I; ia.m = p->m; ia.ncap = ncap; ia.idx_t = idx_t_eff;
-        ia.decode = 1;
-        // FP8 keys: the tensor-core scan, which also counts each row's keys for the top-k; the
-        // exact FP32 scan (and batches of fewer than 16 query rows) on CUDA cores
+        ia.S = S;
+        // FP8 keys: the tensor-core scan and MXFP4 keys the FP4 scan, which also count each
+        // row's keys for the top-k; the exact FP32 scan (and FP8 batches of fewer than 16 query
+        // rows) on CUDA cores
         bool counted = false;
-        if (decode_index_tc_supported(ia)) {
+        if (fp4_scan) {
+            if (cudaMemsetAsync(hist, 0, hbytes + 2 * sizeof(int) * (size_t)p->B, st) != cudaSuccess)
+                return CSA_ERR_CUDA;
+            counted = launch_decode_index_fp4(ia, hist, st);
+            if (!counted) return CSA_ERR_UNSUPPORTED;
+        } else if (decode_index_tc_supported(ia)) {
             if (cudaMemsetAsync(hist, 0, hbytes + 2 * sizeof(int) * (size_t)p->B, st) != cudaSuccess)
                 return CSA_ERR_CUDA;
             counted = launch_decode_index_tc(ia, hist, st);

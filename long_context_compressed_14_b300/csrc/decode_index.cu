@@ -21,7 +21,10 @@
 //        global memory once per sequence, so the CTAs do not contend for the same counters.
 // D has four 16-column TMEM buffers. Every wait is bounded; a failure sets the device status,
 // raises the abort flag and the CTA frees its TMEM and returns.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
+#include "fp4.cuh"
 #include "kernels.cuh"
 #include "tma_host.cuh"
 #include "topk_common.cuh"
@@ -291,6 +294,119 @@ bool launch_decode_index_tc(const IndexArgs &a, uint32_t *hist, cudaStream_t st)
     if (a.H_I == 4) go(decode_index_tc_kernel<4>);
     else if (a.H_I == 8) go(decode_index_tc_kernel<8>);
     else go(decode_index_tc_kernel<16>);
+    count_launches(1);
+    return true;
+}
+
+// ---------------------------------------------------------------------------------------
+// MXFP4 decode scan: the packed FP4 cache read as stored (32 code bytes + 2 exponent bytes per
+// entry, half the FP8 cache's bytes), on the CUDA cores. Thread = entry. Per head h and block
+// b of 32 dims: the E2M1 products are summed in half precision in four partial sums of eight
+// products each (an E2M1 product is a multiple of 1/4 of magnitude at most 36, so a sum of
+// eight is at most 288 and exact in half precision), the partials are added in float and scaled
+// by the two blocks' powers of two; s = sum_h w[h] ReLU(sum_b ...), stored to the sequence's score
+// row and counted in the CTA's histogram of the top 11 order-key bits (added to the sequence's
+// histogram in global memory when the CTA moves to the next sequence), as the tensor-core scan
+// does for FP8 keys. Each CTA takes a contiguous block of 256-entry items.
+// ---------------------------------------------------------------------------------------
+namespace dix4 {
+constexpr int kThreads = 256;
+constexpr int kJ = 256;   // entries per item
+}
+
+template <int HI>
+__global__ void __launch_bounds__(dix4::kThreads) decode_index_fp4_kernel(IndexArgs a, uint32_t *hist, int tiles) {
+    using namespace dix4;
+    __shared__ __align__(16) __half2 s_q[HI][32];  // the query's E2M1 values as half pairs
+    __shared__ float s_qe[HI][2];                  // its block scales 2^(e8 - 127)
+    __shared__ float s_w[HI];
+    __shared__ uint32_t s_hist[tk::kBins];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int n_items = a.B * tiles;
+    const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int it0 = (int)blockIdx.x * per, it1 = min(n_items, it0 + per);
+    for (int i = tid; i < tk::kBins; i += kThreads) s_hist[i] = 0;
+    int hb = -1;
+    auto flush = [&]() {
+        __syncthreads();
+        for (int i = tid; i < tk::kBins; i += kThreads) {
+            const uint32_t v = s_hist[i];
+            if (v) {
+                atomicAdd(hist + (int64_t)hb * tk::kBins + i, v);
+                s_hist[i] = 0;
+            }
+        }
+    };
+    const uint8_t *kc = reinterpret_cast<const uint8_t *>(a.KI);
+    for (int it = it0; it < it1; ++it) {
+        const int b = it / tiles, et = it % tiles;
+        const int64_t t = (int64_t)__ldg(a.ctx + b) - 1;
+        const int vis = (t < 0 || t >= a.L) ? 0 : visible_entries(t, a.m, a.ncap);
+        if (et * kJ >= vis) continue;  // (uniform over the CTA)
+        if (b != hb) {
+            if (hb >= 0) flush();
+            __syncthreads();  // the previous sequence's query is no longer read
+            hb = b;
+            const uint8_t *qc = reinterpret_cast<const uint8_t *>(a.qI) + (int64_t)b * HI * 32;
+            for (int u = tid; u < HI * 32; u += kThreads) s_q[u / 32][u % 32] = e2m1x2_to_h2(qc[u]);  // dims 2i, 2i+1
+            if (tid < HI * 2) s_qe[tid / 2][tid % 2] = ldexpf(1.0f, (int)a.qI_e8[(int64_t)b * HI * 2 + tid] - 127);
+            if (tid < HI) s_w[tid] = __ldg(a.w + (int64_t)b * HI + tid);
+            __syncthreads();
+        }
+        const int j = et * kJ + tid;
+        const bool live = j < vis;
+        float sc = 0.0f;
+        if (live) {
+            const int64_t row = (int64_t)b * a.ncap + j;
+            const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(kc + row * 32));
+            const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(kc + row * 32) + 1);
+            const float ks[2] = {ldexpf(1.0f, (int)a.KI_e8[row * 2] - 127), ldexpf(1.0f, (int)a.KI_e8[row * 2 + 1] - 127)};
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            __half2 kh[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) kh[i] = e2m1x2_to_h2((uint8_t)(cw[i >> 2] >> (8 * (i & 3))));
+#pragma unroll
+            for (int h = 0; h < HI; ++h) {
+                float dot = 0.0f;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    __half2 p0 = __float2half2_rn(0.0f), p1 = p0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) p0 = __hfma2(s_q[h][16 * blk + i], kh[16 * blk + i], p0);
+#pragma unroll
+                    for (int i = 8; i < 16; ++i) p1 = __hfma2(s_q[h][16 * blk + i], kh[16 * blk + i], p1);
+                    const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+                    const float part = (f0.x + f0.y) + (f1.x + f1.y);
+                    dot = fmaf(part, s_qe[h][blk] * ks[blk], dot);  // exact power-of-two scale
+                }
+                sc = fmaf(s_w[h], fmaxf(dot, 0.0f), sc);
+            }
+            sc += 0.0f;  // -0 -> +0
+            a.S[(int64_t)b * a.ldS + j] = sc;
+        }
+        const uint32_t bin = key_of(sc) >> tk::kBinShift;
+        const unsigned peers = __match_any_sync(0xffffffffu, live ? bin : 0xFFFFFFFFu);
+        if (live && (__ffs(peers) - 1) == lane) atomicAdd(&s_hist[bin], (uint32_t)__popc(peers));
+    }
+    if (hb >= 0) flush();
+}
+
+bool decode_index_fp4_supported(const IndexArgs &a) {
+    return a.decode && a.idx_t == CSA_MXFP4 && (a.H_I == 4 || a.H_I == 8 || a.H_I == 16) && a.qI_e8 && a.KI_e8;
+}
+
+bool launch_decode_index_fp4(const IndexArgs &a, uint32_t *hist, cudaStream_t st) {
+    using namespace dix4;
+    if (!decode_index_fp4_supported(a)) return false;
+    const int tiles = (a.ncap + kJ - 1) / kJ;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int items = a.B * tiles;
+    const int grid = items < 4 * sms ? items : 4 * sms;
+    if (a.H_I == 4) decode_index_fp4_kernel<4><<<grid, kThreads, 0, st>>>(a, hist, tiles);
+    else if (a.H_I == 8) decode_index_fp4_kernel<8><<<grid, kThreads, 0, st>>>(a, hist, tiles);
+    else decode_index_fp4_kernel<16><<<grid, kThreads, 0, st>>>(a, hist, tiles);
     count_launches(1);
     return true;
 }

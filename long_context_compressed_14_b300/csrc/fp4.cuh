@@ -18,6 +18,12 @@ __device__ __forceinline__ uint8_t e2m1x2_from(float lo, float hi) {
     asm("{.reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; mov.b16 %0, {t, 0};}" : "=h"(d) : "f"(hi), "f"(lo));
     return (uint8_t)d;
 }
+// one byte of E2M1 codes to two halves (bits 0-3 -> .x, bits 4-7 -> .y), exact
+__device__ __forceinline__ __half2 e2m1x2_to_h2(uint8_t v) {
+    uint32_t r;
+    asm("{.reg .b8 t; mov.b16 {t, _}, %1; cvt.rn.f16x2.e2m1x2 %0, t;}" : "=r"(r) : "h"((uint16_t)v));
+    return *reinterpret_cast<__half2 *>(&r);
+}
 // one byte of E2M1 codes to two floats (bits 0-3 -> .x, bits 4-7 -> .y)
 __device__ __forceinline__ float2 e2m1x2_to(uint8_t v) {
     uint32_t r;

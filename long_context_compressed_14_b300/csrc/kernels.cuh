@@ -27,10 +27,12 @@ struct CompressArgs {
 // Indexer scores of a block of query rows of ONE sequence (prefill) or of one query per
 // sequence (decode) into S[r][j], r = local row, j < visible(row).
 struct IndexArgs {
-    const void *qI;        // rows [.., H_I, d_I] (F32 float or FP8 codes)
+    const void *qI;        // rows [.., H_I, d_I] (F32 float, FP8 codes or MXFP4 codes)
     const float *qI_scale; // FP8: [.., H_I]
+    const uint8_t *qI_e8;  // MXFP4: [.., H_I, d_I / 32] E8M0 block exponents
     const void *KI;        // [B, ncap, d_I]
     const float *KI_scale; // FP8: [B, ncap]
+    const uint8_t *KI_e8;  // MXFP4: [B, ncap, d_I / 32]
     const float *w;        // [.., H_I]
     const int32_t *ctx;    // decode: [B]
     float *S;              // [rows, ldS]
@@ -176,6 +178,9 @@ void launch_decode_select(const DecSelArgs &a, cudaStream_t st);
 // the layer is outside what it handles (launching nothing)
 bool decode_index_tc_supported(const IndexArgs &a);
 bool launch_decode_index_tc(const IndexArgs &a, uint32_t *hist, cudaStream_t st);
+// the same scan for MXFP4 operands read as stored (packed E2M1 + E8M0), on the CUDA cores
+bool decode_index_fp4_supported(const IndexArgs &a);
+bool launch_decode_index_fp4(const IndexArgs &a, uint32_t *hist, cudaStream_t st);
 void launch_attn_simple(const AttnArgs &a, cudaStream_t st);
 // tensor-core kernels: return false (launching nothing) when the configuration is outside
 // what they handle

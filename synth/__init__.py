@@ -72,6 +72,9 @@ WORKLOADS = {
     # The same decode step on the V4.1 cache: NVFP4 entries, an FP8 window ring.
     "decode_v41_b16_ctx131072": Workload("decode_v41_b16_ctx131072", "decode", B=16, L=131072, H=64, seed=3,
                                          c_t="nvfp4", w_t="fp8"),
+    # ... and with the indexer in FP4 as well (MXFP4 keys and queries): the pages' low-precision formats.
+    "decode_fp4_b16_ctx131072": Workload("decode_fp4_b16_ctx131072", "decode", B=16, L=131072, H=64, seed=3,
+                                         c_t="nvfp4", w_t="fp8", idx_t="mxfp4"),
     # Interleaved CSA + HCA layer pair, L = 262144, mixed-precision KV entries, top-1024.
     "pair_mixed_L262144": Workload("pair_mixed_L262144", "pair", B=1, L=262144, H=64, seed=4,
                                    topk=1024, c_t="mixed"),

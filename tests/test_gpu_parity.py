@@ -615,9 +615,12 @@ def test_pair_mixed_L262144_full_size_sampled(lib):
         torch.cuda.empty_cache()
 
 
-def test_decode_b16_ctx131072_full_size_sampled(lib):
-    # 16 sequences x 131072 cached tokens, one CSA and one HCA decode step; sequences 0 and 15
-    wl = synth.WORKLOADS["decode_b16_ctx131072"]
+@pytest.mark.parametrize("name", ["decode_b16_ctx131072", "decode_fp4_b16_ctx131072"])
+def test_decode_b16_ctx131072_full_size_sampled(lib, name):
+    # 16 sequences x 131072 cached tokens, one CSA and one HCA decode step; sequences 0 and 15;
+    # the second workload in the pages' low-precision formats (MXFP4 indexer keys read as stored
+    # by the FP4 scan, NVFP4 entries, FP8 window ring)
+    wl = synth.WORKLOADS[name]
     from long_context_compressed_14_b300.pipeline import DecodeLayer
     for csa in (True, False):
         inp = synth.decode_layer(wl, 0 if csa else 1, csa=csa)
