@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(csa_tc::kThreads, 1) csa_tc_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_trigger();
+    pdl_wait();
     const uint32_t tmem = tmem_slot;
     bool ok = true;
 
@@ -974,13 +976,14 @@ bool launch_csa_tc(const AttnArgs &a, cudaStream_t st) {
     const int idx_bytes = a.dense ? 0 : 2 * a.topk * 4;
     const int smem4 = 1024 + idx_off(4) + idx_bytes;
     const int smem3 = 1024 + idx_off(3) + idx_bytes;
-    if (smem4 + static_bytes <= smem_max) {
-        cudaFuncSetAttribute(csa_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem4);
-        csa_tc_kernel<4><<<grid, kThreads, smem4, st>>>(P);
-    } else {
-        cudaFuncSetAttribute(csa_tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem3);
-        csa_tc_kernel<3><<<grid, kThreads, smem3, st>>>(P);
-    }
+    // decode: a programmatic dependent launch (it overlaps the previous kernel's tail)
+    auto go = [&](auto kern, int smem) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (a.decode) launch_pdl(kern, grid, kThreads, smem, st, P);
+        else kern<<<grid, kThreads, smem, st>>>(P);
+    };
+    if (smem4 + static_bytes <= smem_max) go(csa_tc_kernel<4>, smem4);
+    else go(csa_tc_kernel<3>, smem3);
     count_launches(1);
     return true;
 }
@@ -1016,6 +1019,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float *__rest
                                                              const float2 *__restrict__ rope,
                                                              __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
                                                              int B, int S, int L, int d_rope) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int kH = csa_tc::kH;
     const int lane = threadIdx.x & 31;
     const int gw = (int)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -1058,9 +1063,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float *__rest
 
 void launch_decode_combine(const AttnArgs &a, cudaStream_t st) {
     const int warps = a.B * csa_tc::kH;
-    decode_combine_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
-        a.part_o, a.part_ml, a.ctx, a.sink, reinterpret_cast<const float2 *>(a.rope_tab),
-        reinterpret_cast<__nv_bfloat16 *>(a.out), a.lse, a.B, a.split_S, a.L, a.d_rope);
+    launch_pdl(decode_combine_kernel, (warps + 7) / 8, 256, 0, st, (const float *)a.part_o,
+               (const float2 *)a.part_ml, a.ctx, a.sink, reinterpret_cast<const float2 *>(a.rope_tab),
+               reinterpret_cast<__nv_bfloat16 *>(a.out), a.lse, a.B, a.split_S, a.L, a.d_rope);
     count_launches(1);
 }
 

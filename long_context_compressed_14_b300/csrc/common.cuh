@@ -21,6 +21,30 @@ extern __device__ int g_status;
 extern __device__ int g_abort;
 
 __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_status, 0, code); }
+
+// Programmatic dependent launch (the decode step's chain of kernels): a kernel launched with
+// launch_pdl may be scheduled while the previous kernel of the stream is still running; it
+// lets its own successor be scheduled at once (pdl_trigger) and waits for the previous kernel's
+// completion and memory (pdl_wait) before it touches global memory. Both are no-ops in a kernel
+// launched the ordinary way.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
 __device__ __forceinline__ void set_timeout() {
     atomicCAS(&g_status, 0, CSA_ERR_TIMEOUT);
     atomicExch(&g_abort, 1);

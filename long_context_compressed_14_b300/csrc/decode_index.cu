@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(dix::kThreads, 2) decode_index_tc_kernel(const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_trigger();
+    pdl_wait();
     const uint32_t tmem = tmem_slot;
     const int n_items = P.B * P.tiles;
     const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;  // contiguous items per CTA
@@ -289,7 +291,7 @@ bool launch_decode_index_tc(const IndexArgs &a, uint32_t *hist, cudaStream_t st)
     const int grid = items < 2 * sms ? items : 2 * sms;  // two CTAs (pipelines) per SM
     auto go = [&](auto kern) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        kern<<<grid, kThreads, kSmemBytes, st>>>(P);
+        launch_pdl(kern, grid, kThreads, kSmemBytes, st, P);
     };
     if (a.H_I == 4) go(decode_index_tc_kernel<4>);
     else if (a.H_I == 8) go(decode_index_tc_kernel<8>);
@@ -326,6 +328,8 @@ __global__ void __launch_bounds__(dix4::kThreads) decode_index_fp4_kernel(IndexA
     const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
     const int it0 = (int)blockIdx.x * per, it1 = min(n_items, it0 + per);
     for (int i = tid; i < tk::kBins; i += kThreads) s_hist[i] = 0;
+    pdl_trigger();
+    pdl_wait();
     int hb = -1;
     auto flush = [&]() {
         __syncthreads();
@@ -404,9 +408,9 @@ bool launch_decode_index_fp4(const IndexArgs &a, uint32_t *hist, cudaStream_t st
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int items = a.B * tiles;
     const int grid = items < 4 * sms ? items : 4 * sms;
-    if (a.H_I == 4) decode_index_fp4_kernel<4><<<grid, kThreads, 0, st>>>(a, hist, tiles);
-    else if (a.H_I == 8) decode_index_fp4_kernel<8><<<grid, kThreads, 0, st>>>(a, hist, tiles);
-    else decode_index_fp4_kernel<16><<<grid, kThreads, 0, st>>>(a, hist, tiles);
+    if (a.H_I == 4) launch_pdl(decode_index_fp4_kernel<4>, grid, kThreads, 0, st, a, hist, tiles);
+    else if (a.H_I == 8) launch_pdl(decode_index_fp4_kernel<8>, grid, kThreads, 0, st, a, hist, tiles);
+    else launch_pdl(decode_index_fp4_kernel<16>, grid, kThreads, 0, st, a, hist, tiles);
     count_launches(1);
     return true;
 }

@@ -389,6 +389,8 @@ __global__ void __launch_bounds__(tk::kThreads) decode_collect_kernel(DecSelArgs
     __shared__ uint32_t hist[kBins];
     __shared__ int s_tmp[kWarps];
     __shared__ int s_res[2];
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x / a.slices, g = blockIdx.x % a.slices;
     const int64_t t = (int64_t)a.ctx[r] - 1;
     int32_t *out = a.out + (int64_t)r * a.k;
@@ -453,6 +455,8 @@ __global__ void __launch_bounds__(tk::kThreads) decode_collect_kernel(DecSelArgs
 __global__ void __launch_bounds__(kDecFinishThreads) decode_finish_kernel(DecSelArgs a) {
     using namespace tk;
     constexpr int NT = kDecFinishThreads;
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ uint32_t dyn[];
     uint32_t *hist = dyn;                                                    // [kBins]
     uint32_t *cand_key = hist + kBins;                                       // [kDecBinCap]
@@ -533,11 +537,11 @@ void launch_decode_select(const DecSelArgs &a, cudaStream_t st) {
     DecSelArgs b = a;
     b.slices = (int)((a.ncap + kDecMaxSlice - 1) / kDecMaxSlice);  // each slice fits the registers
     if (b.slices < 16) b.slices = 16;
-    decode_collect_kernel<<<a.B * b.slices, kThreads, 0, st>>>(b);
+    launch_pdl(decode_collect_kernel, a.B * b.slices, kThreads, 0, st, b);
     const int nw = (a.ncap + 31) / 32;
     const size_t smem = sizeof(uint32_t) * ((size_t)kBins + 2 * (size_t)kDecBinCap + 2 * (size_t)nw);
     cudaFuncSetAttribute(decode_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    decode_finish_kernel<<<a.B, kDecFinishThreads, smem, st>>>(b);
+    launch_pdl(decode_finish_kernel, a.B, kDecFinishThreads, smem, st, b);
     count_launches(2);
 }
 
