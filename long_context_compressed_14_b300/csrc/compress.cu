@@ -9,6 +9,7 @@
 #include "common.cuh"
 #include "fp4.cuh"
 #include "kernels.cuh"
+#include "umma.cuh"
 
 namespace csa {
 
@@ -154,19 +155,18 @@ __device__ __forceinline__ void kv_row_chunk(const float (&x)[16 / sizeof(ActT)]
 }
 
 // The end of an entry, by one warp holding c[e] = dim lane + 32 e of the weighted sum (before
-// RoPE) and (k0, k1) = indexer dims (lane, lane + 32): RoPE at the entry position (j+1)m - 1 and
-// storage per KV_T and IDX_T.
+// RoPE) and (k0, k1) = indexer dims (lane, lane + 32): RoPE at the entry position (j+1)m - 1
+// (rope_pos: that position's row of the table, in global or shared memory; null without RoPE)
+// and storage per KV_T and IDX_T.
 template <int KV_T, int IDX_T, bool WITH_KI>
-__device__ __forceinline__ void finish_entry(float (&c)[4], float k0, float k1, int j, int b, int m, int N, int d_rope,
-                                             const float2 *__restrict__ rope, void *__restrict__ c_data,
+__device__ __forceinline__ void finish_entry(float (&c)[4], float k0, float k1, int j, int b, int N,
+                                             const float2 *rope_pos, void *__restrict__ c_data,
                                              __nv_bfloat16 *__restrict__ c_rope, float *__restrict__ c_scale,
                                              void *__restrict__ ki_data, float *__restrict__ ki_scale,
                                              uint8_t *__restrict__ ki_e8) {
     const int lane = threadIdx.x & 31;
-    const int half = d_rope / 2;
-    if (half == 32) {
-        const int64_t pos = (int64_t)(j + 1) * m - 1;
-        const float2 cs = rope[pos * half + lane];
+    if (rope_pos) {
+        const float2 cs = rope_pos[lane];
         const float a = c[2], bb = c[3];
         c[2] = a * cs.x - bb * cs.y;
         c[3] = a * cs.y + bb * cs.x;
@@ -319,8 +319,8 @@ kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
         k0 *= inv;
         k1 *= inv;
     }
-    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, m, N, d_rope, rope, c_data, c_rope, c_scale, ki_data, ki_scale,
-                                       ki_e8);
+    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, N, d_rope == 64 ? rope + ((int64_t)(j + 1) * m - 1) * 32 : nullptr,
+                                       c_data, c_rope, c_scale, ki_data, ki_scale, ki_e8);
 }
 
 
@@ -408,8 +408,274 @@ kv_compress_warp_kernel(const ActT *__restrict__ kv, const float *__restrict__ z
     for (int q = 0; q < 4; ++q) c[q] = s_c[warp][lane + 32 * q] * inv;
     const float k0 = WITH_KI ? s_c[warp][kD + lane] * inv : 0.0f;
     const float k1 = WITH_KI ? s_c[warp][kD + lane + 32] * inv : 0.0f;
-    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, m, N, d_rope, rope, c_data, c_rope, c_scale, ki_data, ki_scale,
-                                       ki_e8);
+    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, N, d_rope == 64 ? rope + ((int64_t)(j + 1) * m - 1) * 32 : nullptr,
+                                       c_data, c_rope, c_scale, ki_data, ki_scale, ki_e8);
+}
+
+// kv_compress for m <= 8, streamed. One warp walks a run of kStreamE consecutive entries
+// j0 .. j0 + E - 1 block by block (block beta = rows [beta m, (beta + 1) m)), from block j0 - 1
+// (the run's halo: it only feeds entry j0) to block j0 + E - 1. Each block's KV rows,
+// indexer-key rows and RoPE-table rows (contiguous in memory) are copied into the warp's ring of
+// shared-memory slots kStreamD - 1 blocks ahead of their use by three bulk copies that complete
+// on the slot's mbarrier, so every raw row is read from HBM once (plus one halo block per run)
+// with several blocks in flight per warp. A block
+// feeds two entries: entry beta (its own block, logits of set 0) and entry beta + 1 (its previous
+// block, set 1). The warp keeps the two running sums; after block beta, entry beta is complete
+// and is stored by finish_entry. The window weights of the run's entries are computed first,
+// lane i for entry j0 + i.
+constexpr int kStreamE = 16;     // entries per warp
+constexpr int kStreamWarps = 4;  // warps per CTA
+constexpr int kStreamD = 3;      // ring slots per warp (blocks in flight: kStreamD - 1)
+constexpr int kStreamMaxM = 8;
+
+__device__ __forceinline__ void lds16(const float *p, float (&x)[4]) {
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void lds16(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
+        x[2 * k] = f.x;
+        x[2 * k + 1] = f.y;
+    }
+}
+
+// bytes of one ring slot (one block of m rows)
+__host__ __device__ __forceinline__ int stream_slot_bytes(int m, int act_bytes, bool with_ki, bool rot) {
+    return m * (kD * act_bytes + (with_ki ? kDI * 4 : 0) + (rot ? 32 * 8 : 0));
+}
+
+template <typename ActT, int KV_T, int IDX_T, bool WITH_KI, bool WITH_KVROPE>
+__global__ void __launch_bounds__(kStreamWarps * 32)
+kv_compress_stream_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
+                          const float *__restrict__ kI_raw, const float2 *__restrict__ rope,
+                          void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
+                          float *__restrict__ c_scale, void *__restrict__ ki_data,
+                          float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope,
+                          int L, int m, int N, int d_rope) {
+    using namespace umma;
+    constexpr int V = 16 / (int)sizeof(ActT);    // dims per 16-byte chunk
+    constexpr int CPR = kD / V;                  // chunks per KV row
+    constexpr int RPW = 32 / CPR;                // KV rows per warp instruction
+    constexpr int KVB = kD * (int)sizeof(ActT);  // bytes per KV row
+    constexpr int KIB = kDI * 4;                 // bytes per indexer-key row
+    extern __shared__ __align__(16) uint8_t s_ring[];
+    __shared__ float s_e[kStreamWarps][kStreamE][2 * kStreamMaxM];
+    __shared__ float s_inv[kStreamWarps][kStreamE];
+    __shared__ __align__(16) float s_c[kStreamWarps][kD + kDI];
+    __shared__ __align__(8) uint64_t s_bar[kStreamWarps][kStreamD];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int j0 = (blockIdx.x * kStreamWarps + warp) * kStreamE;
+    if (j0 >= N) return;  // (the warp leaves as a whole; nothing below is CTA-wide)
+    const int jn = min(N, j0 + kStreamE);
+    const bool rot = d_rope == 64;
+    // slot: KV rows [m][KVB], indexer-key rows [m][KIB], RoPE rows [m][32 float2]
+    const int kv_bytes = m * KVB, ki_bytes = WITH_KI ? m * KIB : 0;
+    const int slot_bytes = stream_slot_bytes(m, (int)sizeof(ActT), WITH_KI, rot);
+    uint8_t *ring = s_ring + (size_t)warp * kStreamD * slot_bytes;
+    const uint32_t ring_u32 = smem_u32(ring);
+    const ActT *kvb = kv + (int64_t)b * L * kD;
+    const float *kib = WITH_KI ? kI_raw + (int64_t)b * L * kDI : nullptr;
+    ActT *kvrb = WITH_KVROPE ? kv_rope + (int64_t)b * L * kD : nullptr;
+    if (lane == 0) {
+        for (int s = 0; s < kStreamD; ++s) mbar_init(smem_u32(&s_bar[warp][s]), 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+
+    // blocks of the run: beta = jb0 .. jn - 1, block i into slot i % kStreamD by three bulk copies
+    // (lane 0) completing on the slot's barrier; rows past L are not copied and never read
+    const int jb0 = j0 > 0 ? j0 - 1 : 0;
+    const int nblk = jn - jb0;
+    auto issue = [&](int i) {
+        if (lane == 0 && i < nblk) {
+            const int64_t t0 = (int64_t)(jb0 + i) * m;
+            const int rows = (int)min((int64_t)m, (int64_t)L - t0);  // >= 1
+            const uint32_t dst = ring_u32 + (uint32_t)((i % kStreamD) * slot_bytes);
+            const uint32_t bar = smem_u32(&s_bar[warp][i % kStreamD]);
+            mbar_expect_tx(bar, (uint32_t)(rows * KVB + (WITH_KI ? rows * KIB : 0) + (rot ? m * 256 : 0)));
+            bulk_load(dst, kvb + t0 * kD, (uint32_t)(rows * KVB), bar);
+            if (WITH_KI) bulk_load(dst + kv_bytes, kib + t0 * kDI, (uint32_t)(rows * KIB), bar);
+            // the table holds every position below ceil(L / m) m
+            if (rot) bulk_load(dst + kv_bytes + ki_bytes, rope + t0 * 32, (uint32_t)(m * 256), bar);
+        }
+    };
+#pragma unroll
+    for (int i = 0; i < kStreamD - 1; ++i) issue(i);
+
+    // window weights of entry j0 + lane: s_e[.][r] = exp(logit - max) for window row r (r < m:
+    // the previous block, set 1; r >= m: the own block, set 0); rows outside [0, L) weigh 0
+    if (lane < kStreamE) {
+        const int j = j0 + lane;
+        float lg[2 * kStreamMaxM];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < 2 * kStreamMaxM; ++r) {
+            const int64_t t = (int64_t)(j - 1) * m + r;
+            const bool in = j < N && r < 2 * m && t >= 0 && t < L;
+            lg[r] = in ? z[((int64_t)b * L + t) * 2 + (r < m ? 1 : 0)] : -INFINITY;
+            mx = fmaxf(mx, lg[r]);
+        }
+        float den = 0.0f;
+#pragma unroll
+        for (int r = 0; r < 2 * kStreamMaxM; ++r) {
+            const int64_t t = (int64_t)(j - 1) * m + r;
+            const bool in = j < N && r < 2 * m && t >= 0 && t < L;
+            const float e = in ? expf(lg[r] - mx) : 0.0f;
+            den += e;
+            s_e[warp][lane][r] = e;
+        }
+        s_inv[warp][lane] = 1.0f / den;
+    }
+
+    const int cl = lane % CPR, rl = lane / CPR, d0 = cl * V;
+    const int kc = lane & 15, kr = lane >> 4;
+    // running sums as float pairs (packed FMA): acc for entry beta, nxt for entry beta + 1
+    uint64_t acc[V / 2], nxt[V / 2], ak[2], nk[2];
+#pragma unroll
+    for (int k = 0; k < V / 2; ++k) acc[k] = nxt[k] = 0ull;
+    ak[0] = ak[1] = nk[0] = nk[1] = 0ull;
+    // an indexer-key row chunk of window row r into the two sums
+    auto ki_row = [&](const uint8_t *slot, int64_t t0, int r, float wo, float wn) {
+        if (r < m && t0 + r < L) {
+            const float4 x = *reinterpret_cast<const float4 *>(slot + kv_bytes + r * KIB + kc * 16);
+            const uint64_t wo2 = f2_pack(wo, wo), wn2 = f2_pack(wn, wn);
+            const uint64_t x01 = f2_pack(x.x, x.y), x23 = f2_pack(x.z, x.w);
+            ak[0] = f2_fma(wo2, x01, ak[0]);
+            ak[1] = f2_fma(wo2, x23, ak[1]);
+            nk[0] = f2_fma(wn2, x01, nk[0]);
+            nk[1] = f2_fma(wn2, x23, nk[1]);
+        }
+    };
+
+    bool ok = true;
+    int i = 0;
+    for (; i < nblk; ++i) {
+        issue(i + kStreamD - 1);
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_bar[warp][i % kStreamD]), (i / kStreamD) & 1, kWaitNs,
+                                               &g_abort))) {
+            ok = false;
+            break;
+        }
+        const int beta = jb0 + i;
+        const uint8_t *slot = ring + (size_t)(i % kStreamD) * slot_bytes;
+        const float2 *slot_rope = reinterpret_cast<const float2 *>(slot + kv_bytes + ki_bytes);
+        const bool own = beta >= j0;          // entry beta is in the run (else: the halo block)
+        const bool has_next = beta + 1 < jn;  // entry beta + 1 is in the run
+        const float *e_own = s_e[warp][own ? beta - j0 : 0] + m;
+        const float *e_nxt = s_e[warp][has_next ? beta + 1 - j0 : 0];
+        const int64_t t0 = (int64_t)beta * m;
+        for (int r0 = 0; r0 < m; r0 += RPW) {
+            const int r = r0 + rl;
+            const bool have = r < m && t0 + r < L;
+            float x[V];
+            if (have) {
+                lds16(reinterpret_cast<const ActT *>(slot + r * KVB) + d0, x);
+            } else {
+#pragma unroll
+                for (int k = 0; k < V; ++k) x[k] = 0.0f;
+            }
+            const float wo = own && have ? e_own[r] : 0.0f;
+            const float wn = has_next && have ? e_nxt[r] : 0.0f;
+            const uint64_t wo2 = f2_pack(wo, wo), wn2 = f2_pack(wn, wn);
+#pragma unroll
+            for (int k = 0; k < V / 2; ++k) {
+                const uint64_t x2 = f2_pack(x[2 * k], x[2 * k + 1]);
+                acc[k] = f2_fma(wo2, x2, acc[k]);
+                nxt[k] = f2_fma(wn2, x2, nxt[k]);
+            }
+            // BF16 rows: the indexer-key row of the same window row sits in the same lanes' half
+            if (WITH_KI && RPW == 2) ki_row(slot, t0, r, wo, wn);
+            if (WITH_KVROPE && own) {  // the row back, rotated at its own position t0 + r
+                float y[V];
+#pragma unroll
+                for (int k = 0; k < V; ++k) y[k] = x[k];
+                if (rot) {
+                    float other[V];
+#pragma unroll
+                    for (int k = 0; k < V; ++k) other[k] = __shfl_xor_sync(0xffffffffu, x[k], 32 / V);
+                    if (have && d0 >= 64) {
+                        // dims 64 + i (first of the pair): x cos - x' sin; 96 + i: x cos + x' sin
+                        const float sg = d0 < 96 ? -1.0f : 1.0f;
+                        const int ip = (d0 - 64) & 31;  // pair index of the chunk's first dim
+                        const float4 *r4 = reinterpret_cast<const float4 *>(slot_rope + r * 32 + ip);
+#pragma unroll
+                        for (int k2 = 0; k2 < V / 2; ++k2) {
+                            const float4 cs = r4[k2];  // (cos, sin) of pairs ip + 2 k2 and ip + 2 k2 + 1
+                            y[2 * k2] = fmaf(sg * other[2 * k2], cs.y, x[2 * k2] * cs.x);
+                            y[2 * k2 + 1] = fmaf(sg * other[2 * k2 + 1], cs.w, x[2 * k2 + 1] * cs.z);
+                        }
+                    }
+                }
+                if (have) store16(kvrb + (t0 + r) * kD + d0, y);
+            }
+        }
+        if (WITH_KI && RPW == 1) {
+            for (int r0 = 0; r0 < m; r0 += 2) {
+                const int r = r0 + kr;
+                const bool have = r < m && t0 + r < L;
+                ki_row(slot, t0, r, own && have ? e_own[r] : 0.0f, has_next && have ? e_nxt[r] : 0.0f);
+            }
+        }
+        if (own) {  // entry beta is complete
+            float a[V];
+#pragma unroll
+            for (int k = 0; k < V / 2; ++k) {
+                const float2 f = f2_unpack(acc[k]);
+                a[2 * k] = f.x;
+                a[2 * k + 1] = f.y;
+            }
+            if (RPW == 2) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) a[k] += __shfl_xor_sync(0xffffffffu, a[k], 16);
+            }
+            if (rl == 0) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) s_c[warp][d0 + k] = a[k];
+            }
+            if (WITH_KI) {
+                float q[4];
+                const float2 f0 = f2_unpack(ak[0]), f1 = f2_unpack(ak[1]);
+                q[0] = f0.x; q[1] = f0.y; q[2] = f1.x; q[3] = f1.y;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[k] += __shfl_xor_sync(0xffffffffu, q[k], 16);
+                if (kr == 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) s_c[warp][kD + kc * 4 + k] = q[k];
+                }
+            }
+            __syncwarp();
+            const float inv = s_inv[warp][beta - j0];
+            float c[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) c[q] = s_c[warp][lane + 32 * q] * inv;
+            const float k0 = WITH_KI ? s_c[warp][kD + lane] * inv : 0.0f;
+            const float k1 = WITH_KI ? s_c[warp][kD + lane + 32] * inv : 0.0f;
+            // the entry position (beta + 1) m - 1 is the block's last row: its RoPE row is in the slot
+            finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, beta, b, N, rot ? slot_rope + (m - 1) * 32 : nullptr,
+                                               c_data, c_rope, c_scale, ki_data, ki_scale, ki_e8);
+        }
+#pragma unroll
+        for (int k = 0; k < V / 2; ++k) {
+            acc[k] = nxt[k];
+            nxt[k] = 0ull;
+        }
+        ak[0] = nk[0]; ak[1] = nk[1];
+        nk[0] = nk[1] = 0ull;
+        __syncwarp();  // slot i and s_c are free for reuse
+    }
+    if (!ok) {
+        set_timeout();
+        // copies still in flight land before the warp leaves (bounded)
+        if (lane == 0)
+            for (int f = i; f < min(nblk, i + kStreamD); ++f)
+                mbar_wait(smem_u32(&s_bar[warp][f % kStreamD]), (f / kStreamD) & 1, kDrainNs);
+        __syncwarp();
+    }
 }
 
 template <typename ActT, int KV_T, int IDX_T>
@@ -419,11 +685,21 @@ static void launch_compress_t(const CompressArgs &a, cudaStream_t st) {
     ActT *kvr = reinterpret_cast<ActT *>(a.kv_rope);
     const float2 *rope = reinterpret_cast<const float2 *>(a.rope_tab);
     auto *cr = reinterpret_cast<__nv_bfloat16 *>(a.c_rope);
-    // small m: one warp per entry (the window's weights fit the lanes); else one CTA per entry
+    // m <= 8: the streamed kernel; other small m: one warp per entry (the window's weights fit
+    // the lanes); else one CTA per entry
+    const bool stream = a.m <= kStreamMaxM;
+    const int ssmem = kStreamWarps * kStreamD *
+                      stream_slot_bytes(a.m, (int)sizeof(ActT), a.kI_raw != nullptr, a.d_rope == 64);
+    const dim3 sgrid((a.N + kStreamE * kStreamWarps - 1) / (kStreamE * kStreamWarps), a.B);
     const bool per_warp = 2 * a.m <= 32;
     const dim3 wgrid((a.N + 7) / 8, a.B);
 #define CSA_LAUNCH(KI, KVR)                                                                          \
-    if (per_warp)                                                                                    \
+    if (stream) {                                                                                    \
+        auto kern = kv_compress_stream_kernel<ActT, KV_T, IDX_T, KI, KVR>;                           \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem);              \
+        kern<<<sgrid, kStreamWarps * 32, ssmem, st>>>(kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, \
+                                                       a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope); \
+    } else if (per_warp)                                                                             \
         kv_compress_warp_kernel<ActT, KV_T, IDX_T, KI, KVR><<<wgrid, 256, 0, st>>>(                  \
             kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, \
             a.d_rope);                                                                               \
