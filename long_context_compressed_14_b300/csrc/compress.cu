@@ -69,32 +69,14 @@ void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, f
 }
 
 // ---------------------------------------------------------------------------------------
-// kv_compress: one CTA (4 warps) per entry j of sequence b.
-//   window rows [(j-1)m, (j+1)m) ∩ [0, L); weight of row t = exp(z[t, set] - max) with set 0
-//   for the own block (t >= jm) and set 1 for the previous block; normalised at the end.
-//   Rows are read in 16-byte chunks: a warp instruction covers two BF16 rows (one FP32 row) of
-//   KV and two indexer-key rows; each thread accumulates the 8 (4) dims of its chunk over its
-//   rows, the partial sums meet in shared memory, and warp 0 finishes the entry with lane l
-//   holding dims {l, l+32, l+64, l+96} (RoPE pairs (64+i, 96+i) in one lane) and indexer dims
-//   {l, l+32}. Rows of the own block are also written back rotated at their own position
-//   (kv_rope); the two dims of a RoPE pair sit in chunks 32/V apart and meet by a shuffle.
+// kv_compress: entry j of sequence b is the softmax-weighted sum of the window rows
+//   [(j-1)m, (j+1)m) ∩ [0, L), weight of row t = exp(z[t, set] - max) with set 0 for the own
+//   block (t >= jm) and set 1 for the previous block, normalised at the end; then RoPE at the
+//   entry position (j+1)m - 1 and the storage format. Rows of the own block are also written
+//   back rotated at their own position (kv_rope; the two dims of a RoPE pair sit in 16-byte
+//   chunks 32 / V apart and meet by a shuffle). Consecutive entries share a block, so both
+//   kernels below walk runs of consecutive entries block by block and read each raw row once.
 // ---------------------------------------------------------------------------------------
-constexpr int kMaxWindow = 2 * 1024;
-
-__device__ __forceinline__ void load16(const float *p, float (&x)[4]) {
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-}
-__device__ __forceinline__ void load16(const __nv_bfloat16 *p, float (&x)[8]) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
-        x[2 * k] = f.x;
-        x[2 * k + 1] = f.y;
-    }
-}
 __device__ __forceinline__ void store16(float *p, const float (&y)[4]) {
     *reinterpret_cast<float4 *>(p) = make_float4(y[0], y[1], y[2], y[3]);
 }
@@ -106,52 +88,6 @@ __device__ __forceinline__ void store16(__nv_bfloat16 *p, const float (&y)[8]) {
         w[k] = *reinterpret_cast<uint32_t *>(&b2);
     }
     *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// One 16-byte chunk x (dims d0 .. d0 + V - 1) of window row t of one sequence, by every lane of
-// a warp together: acc += wt * x; a row of the entry's own block (own) also goes back rotated at
-// its own position t into kv_rope (the two dims of a RoPE pair sit in chunks 32 / V apart and
-// meet by a shuffle).
-template <typename ActT>
-__device__ __forceinline__ void kv_load(const ActT *__restrict__ kvb, int64_t t, bool have, int d0,
-                                        float (&x)[16 / sizeof(ActT)]) {
-    if (have) {
-        load16(kvb + t * kD + d0, x);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 16 / (int)sizeof(ActT); ++k) x[k] = 0.0f;
-    }
-}
-
-template <typename ActT, bool WITH_KVROPE>
-__device__ __forceinline__ void kv_row_chunk(const float (&x)[16 / sizeof(ActT)], ActT *__restrict__ kvr_b,
-                                             const float2 *__restrict__ rope, int half, int64_t t, bool own, int d0,
-                                             float wt, float (&acc)[16 / sizeof(ActT)]) {
-    constexpr int V = 16 / (int)sizeof(ActT);
-#pragma unroll
-    for (int k = 0; k < V; ++k) acc[k] = fmaf(wt, x[k], acc[k]);
-    if (WITH_KVROPE) {
-        float y[V];
-#pragma unroll
-        for (int k = 0; k < V; ++k) y[k] = x[k];
-        if (half == 32) {
-            float other[V];
-#pragma unroll
-            for (int k = 0; k < V; ++k) other[k] = __shfl_xor_sync(0xffffffffu, x[k], 32 / V);
-            if (own && d0 >= 64) {
-                const int ip = (d0 - 64) & 31;  // pair index of the chunk's first dim
-                const float4 *r4 = reinterpret_cast<const float4 *>(rope + t * half + ip);
-#pragma unroll
-                for (int k2 = 0; k2 < V / 2; ++k2) {
-                    const float4 cs = __ldg(r4 + k2);  // (cos, sin) of pairs ip + 2 k2 and ip + 2 k2 + 1
-                    const int k = 2 * k2;
-                    y[k] = d0 < 96 ? x[k] * cs.x - other[k] * cs.y : other[k] * cs.y + x[k] * cs.x;
-                    y[k + 1] = d0 < 96 ? x[k + 1] * cs.z - other[k + 1] * cs.w : other[k + 1] * cs.w + x[k + 1] * cs.z;
-                }
-            }
-        }
-        if (own) store16(kvr_b + t * kD + d0, y);
-    }
 }
 
 // The end of an entry, by one warp holding c[e] = dim lane + 32 e of the weighted sum (before
@@ -209,207 +145,6 @@ __device__ __forceinline__ void finish_entry(float (&c)[4], float k0, float k1, 
             if (lane == 0) ki_scale[row] = scale;
         }
     }
-}
-
-template <typename ActT, int KV_T, int IDX_T, bool WITH_KI, bool WITH_KVROPE>
-__global__ void __launch_bounds__(128)
-kv_compress_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
-                   const float *__restrict__ kI_raw, const float2 *__restrict__ rope,
-                   void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
-                   float *__restrict__ c_scale, void *__restrict__ ki_data,
-                   float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope, int L,
-                   int m, int N, int d_rope) {
-    constexpr int V = 16 / (int)sizeof(ActT);  // dims per 16-byte chunk: 8 (BF16) or 4 (FP32)
-    constexpr int CPR = kD / V;                // chunks per KV row: 16 or 32
-    constexpr int RPW = 32 / CPR;              // KV rows per warp instruction: 2 or 1
-    constexpr int KG = 8;                      // partial-sum groups (4 warps x 2 rows per instruction)
-    __shared__ float s_w[kMaxWindow];
-    __shared__ __align__(16) float s_red[KG][kD + kDI];
-    __shared__ float s_scalar[8];
-
-    const int j = blockIdx.x, b = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t lo = (int64_t)(j - 1) * m < 0 ? 0 : (int64_t)(j - 1) * m;
-    const int64_t hi = (int64_t)(j + 1) * m > L ? (int64_t)L : (int64_t)(j + 1) * m;
-    const int n = (int)(hi - lo);
-    const int64_t own0 = (int64_t)j * m;
-    const float *zb = z + (int64_t)b * L * 2;
-
-    // softmax weights of the window
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < n; i += 128) {
-        const int64_t t = lo + i;
-        const float l = zb[2 * t + (t >= own0 ? 0 : 1)];
-        s_w[i] = l;
-        mx = fmaxf(mx, l);
-    }
-    mx = warp_max(mx);
-    if (lane == 0) s_scalar[warp] = mx;
-    __syncthreads();
-    mx = fmaxf(fmaxf(s_scalar[0], s_scalar[1]), fmaxf(s_scalar[2], s_scalar[3]));
-    float den = 0.0f;
-    for (int i = threadIdx.x; i < n; i += 128) {
-        const float e = expf(s_w[i] - mx);
-        s_w[i] = e;
-        den += e;
-    }
-    den = warp_sum(den);
-    __syncthreads();
-    if (lane == 0) s_scalar[4 + warp] = den;
-    __syncthreads();
-    den = (s_scalar[4] + s_scalar[5]) + (s_scalar[6] + s_scalar[7]);
-
-    const int half = d_rope / 2;  // 32 or 0
-    const ActT *kvb = kv + (int64_t)b * L * kD;
-    // KV rows: thread = chunk cl of row i0 + rl
-    {
-        const int cl = lane % CPR, rl = lane / CPR;
-        const int d0 = cl * V;  // first dim of this thread's chunk
-        float acc[V];
-#pragma unroll
-        for (int k = 0; k < V; ++k) acc[k] = 0.0f;
-        for (int i0 = warp * RPW; i0 < n; i0 += 4 * RPW) {  // trip count uniform over the warp
-            const int i = i0 + rl;
-            const bool have = i < n;
-            float x[V];
-            kv_load(kvb, lo + i, have, d0, x);
-            kv_row_chunk<ActT, WITH_KVROPE>(x, kv_rope + (int64_t)b * L * kD, rope, half, lo + i,
-                                            have && lo + i >= own0, d0, have ? s_w[i] : 0.0f, acc);
-        }
-#pragma unroll
-        for (int k = 0; k < V; ++k) s_red[warp * RPW + rl][d0 + k] = acc[k];
-    }
-    // indexer-key rows (64 floats = 16 chunks): thread = chunk kc of row i0 + kr
-    if (WITH_KI) {
-        const int kc = lane & 15, kr = lane >> 4;
-        float acck[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int i0 = warp * 2; i0 < n; i0 += 8) {
-            const int i = i0 + kr;
-            if (i < n) {
-                float x[4];
-                load16(kI_raw + ((int64_t)b * L + lo + i) * kDI + kc * 4, x);
-                const float wt = s_w[i];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) acck[k] = fmaf(wt, x[k], acck[k]);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) s_red[warp * 2 + kr][kD + kc * 4 + k] = acck[k];
-    }
-    __syncthreads();
-    if (warp != 0) return;
-
-    const float inv = 1.0f / den;
-    float c[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int dd = lane + 32 * e;
-        float sum = 0.0f;
-#pragma unroll
-        for (int g = 0; g < 4 * RPW; ++g) sum += s_red[g][dd];
-        c[e] = sum * inv;
-    }
-    float k0 = 0.0f, k1 = 0.0f;
-    if (WITH_KI) {
-#pragma unroll
-        for (int g = 0; g < KG; ++g) {
-            k0 += s_red[g][kD + lane];
-            k1 += s_red[g][kD + lane + 32];
-        }
-        k0 *= inv;
-        k1 *= inv;
-    }
-    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, N, d_rope == 64 ? rope + ((int64_t)(j + 1) * m - 1) * 32 : nullptr,
-                                       c_data, c_rope, c_scale, ki_data, ki_scale, ki_e8);
-}
-
-
-// kv_compress for small m (2m <= 32 window rows): one warp per entry, eight entries per CTA. The
-// window weights live in the lanes (lane i = row i), each KV row is read as 16-byte chunks (two
-// BF16 rows or one FP32 row per warp instruction), and the entry's sums meet in the warp's own
-// shared-memory row for the storage step; no CTA-wide barrier.
-template <typename ActT, int KV_T, int IDX_T, bool WITH_KI, bool WITH_KVROPE>
-__global__ void __launch_bounds__(256)
-kv_compress_warp_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
-                        const float *__restrict__ kI_raw, const float2 *__restrict__ rope,
-                        void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
-                        float *__restrict__ c_scale, void *__restrict__ ki_data,
-                        float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope,
-                        int L, int m, int N, int d_rope) {
-    constexpr int V = 16 / (int)sizeof(ActT);
-    constexpr int CPR = kD / V;
-    constexpr int RPW = 32 / CPR;
-    __shared__ __align__(16) float s_c[8][kD + kDI];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j = blockIdx.x * 8 + warp, b = blockIdx.y;
-    if (j >= N) return;  // (the warp leaves as a whole; nothing below is CTA-wide)
-    const int64_t lo = (int64_t)(j - 1) * m < 0 ? 0 : (int64_t)(j - 1) * m;
-    const int64_t hi = (int64_t)(j + 1) * m > L ? (int64_t)L : (int64_t)(j + 1) * m;
-    const int n = (int)(hi - lo);  // <= 32
-    const int64_t own0 = (int64_t)j * m;
-    // softmax weights: lane i holds row i's unnormalised weight
-    float lg = -INFINITY;
-    if (lane < n) {
-        const int64_t t = lo + lane;
-        lg = z[((int64_t)b * L + t) * 2 + (t >= own0 ? 0 : 1)];
-    }
-    const float mx = warp_max(lg);
-    const float e = lane < n ? expf(lg - mx) : 0.0f;
-    const float inv = 1.0f / warp_sum(e);
-    const int half = d_rope / 2;
-    const ActT *kvb = kv + (int64_t)b * L * kD;
-    {
-        const int cl = lane % CPR, rl = lane / CPR;
-        const int d0 = cl * V;
-        float acc[V];
-#pragma unroll
-        for (int k = 0; k < V; ++k) acc[k] = 0.0f;
-        for (int i0 = 0; i0 < n; i0 += RPW) {
-            const int i = i0 + rl;
-            const bool have = i < n;
-            const float wt = __shfl_sync(0xffffffffu, e, i & 31);
-            float x[V];
-            kv_load(kvb, lo + i, have, d0, x);
-            kv_row_chunk<ActT, WITH_KVROPE>(x, kv_rope + (int64_t)b * L * kD, rope, half, lo + i,
-                                            have && lo + i >= own0, d0, have ? wt : 0.0f, acc);
-        }
-        if (RPW == 2) {
-#pragma unroll
-            for (int k = 0; k < V; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
-        }
-        if (rl == 0) {
-#pragma unroll
-            for (int k = 0; k < V; ++k) s_c[warp][d0 + k] = acc[k];
-        }
-    }
-    if (WITH_KI) {
-        const int kc = lane & 15, kr = lane >> 4;
-        float acck[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int i0 = 0; i0 < n; i0 += 2) {
-            const int i = i0 + kr;
-            const float wt = __shfl_sync(0xffffffffu, e, i & 31);
-            if (i < n) {
-                float x[4];
-                load16(kI_raw + ((int64_t)b * L + lo + i) * kDI + kc * 4, x);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) acck[k] = fmaf(wt, x[k], acck[k]);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acck[k] += __shfl_xor_sync(0xffffffffu, acck[k], 16);
-        if (kr == 0) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) s_c[warp][kD + kc * 4 + k] = acck[k];
-        }
-    }
-    __syncwarp();
-    float c[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) c[q] = s_c[warp][lane + 32 * q] * inv;
-    const float k0 = WITH_KI ? s_c[warp][kD + lane] * inv : 0.0f;
-    const float k1 = WITH_KI ? s_c[warp][kD + lane + 32] * inv : 0.0f;
-    finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, j, b, N, d_rope == 64 ? rope + ((int64_t)(j + 1) * m - 1) * 32 : nullptr,
-                                       c_data, c_rope, c_scale, ki_data, ki_scale, ki_e8);
 }
 
 // kv_compress for m <= 8, streamed. One warp walks a run of kStreamE consecutive entries
@@ -678,35 +413,300 @@ kv_compress_stream_kernel(const ActT *__restrict__ kv, const float *__restrict__
     }
 }
 
+// kv_compress for m > 8, streamed by CTAs. A CTA of kRunThreads walks a run of kRunE
+// consecutive entries j0 .. j0 + E - 1 over blocks j0 - 1 .. j0 + E - 1 (block beta = rows
+// [beta m, (beta + 1) m); block j0 - 1 is the run's halo and only feeds entry j0), in stages of
+// kRunG rows: thread 0 bulk-copies a stage's KV rows, indexer-key rows and (outside the halo)
+// RoPE-table rows into a ring of kRunS shared-memory slots kRunS - 1 stages ahead, completing on
+// the slot's mbarrier. Every thread adds its 16-byte chunks of the stage's rows into two running
+// sums (entry beta with the set-0 weights of its own block, entry beta + 1 with the set-1 weights
+// of its previous block) and writes its rows of the own blocks back rotated (kv_rope). After a
+// block's last stage the partial sums meet in shared memory and warp 0 stores entry beta. The
+// window weights of the run's entries are computed first, one warp per entry.
+constexpr int kRunThreads = 256;
+constexpr int kRunWarps = kRunThreads / 32;
+constexpr int kRunE = 4;   // entries per CTA
+constexpr int kRunG = 64;  // rows per stage
+constexpr int kRunS = 3;   // ring slots (stages in flight: kRunS - 1)
+
+__host__ __device__ __forceinline__ int run_stage_bytes(int act_bytes, bool with_ki, bool rot) {
+    return kRunG * (kD * act_bytes + (with_ki ? kDI * 4 : 0) + (rot ? 32 * 8 : 0));
+}
+__host__ __device__ __forceinline__ int run_smem_bytes(int m, int act_bytes, bool with_ki, bool rot) {
+    return kRunS * run_stage_bytes(act_bytes, with_ki, rot) + kRunE * 2 * m * 4 + kRunE * 4 +
+           kRunWarps * (kD + kDI) * 4;
+}
+
+template <typename ActT, int KV_T, int IDX_T, bool WITH_KI, bool WITH_KVROPE>
+__global__ void __launch_bounds__(kRunThreads)
+kv_compress_run_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
+                       const float *__restrict__ kI_raw, const float2 *__restrict__ rope,
+                       void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
+                       float *__restrict__ c_scale, void *__restrict__ ki_data,
+                       float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope,
+                       int L, int m, int N, int d_rope) {
+    using namespace umma;
+    constexpr int V = 16 / (int)sizeof(ActT);    // dims per 16-byte chunk
+    constexpr int CPR = kD / V;                  // chunks per KV row
+    constexpr int RPW = 32 / CPR;                // KV rows per warp instruction
+    constexpr int KVB = kD * (int)sizeof(ActT);  // bytes per KV row
+    constexpr int KIB = kDI * 4;                 // bytes per indexer-key row
+    constexpr int RG = kRunWarps * RPW;          // KV rows per CTA pass (row groups)
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t s_bar[kRunS];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.y;
+    const int j0 = blockIdx.x * kRunE;
+    const int jn = min(N, j0 + kRunE);
+    const bool rot = d_rope == 64;
+    const int kv_bytes = kRunG * KVB, ki_bytes = WITH_KI ? kRunG * KIB : 0;
+    const int stage_bytes = run_stage_bytes((int)sizeof(ActT), WITH_KI, rot);
+    uint8_t *ring = smem_raw;
+    float *s_e = reinterpret_cast<float *>(smem_raw + kRunS * stage_bytes);  // [kRunE][2m]
+    float *s_inv = s_e + kRunE * 2 * m;                                       // [kRunE]
+    float *s_red = s_inv + kRunE;  // [kRunWarps][kD]: KV partial sums, then [kRunWarps][kDI] keys
+    float *s_redk = s_red + kRunWarps * kD;
+    const ActT *kvb = kv + (int64_t)b * L * kD;
+    const float *kib = WITH_KI ? kI_raw + (int64_t)b * L * kDI : nullptr;
+    ActT *kvrb = WITH_KVROPE ? kv_rope + (int64_t)b * L * kD : nullptr;
+    if (tid == 0) {
+        for (int q = 0; q < kRunS; ++q) mbar_init(smem_u32(&s_bar[q]), 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    // stages: block jb0 + q / ns, rows [(q % ns) G, min((q % ns + 1) G, m)) of it
+    const int jb0 = j0 > 0 ? j0 - 1 : 0;
+    const int ns = (m + kRunG - 1) / kRunG;
+    const int nq = (jn - jb0) * ns;
+    auto issue = [&](int q) {  // by thread 0
+        if (q < nq) {
+            const int beta = jb0 + q / ns, s0 = (q % ns) * kRunG;
+            const int64_t t0 = (int64_t)beta * m + s0;
+            // rows of the stage below L (a stage of the last block may have none: its barrier
+            // phase then completes by a plain arrival)
+            const int rows = (int)min((int64_t)min(kRunG, m - s0), (int64_t)L - t0);
+            const uint32_t bar = smem_u32(&s_bar[q % kRunS]);
+            if (rows <= 0) {
+                mbar_arrive(bar);
+                return;
+            }
+            const bool rr = rot && beta >= j0;  // RoPE rows: own blocks only
+            const uint32_t dst = smem_u32(ring + (q % kRunS) * stage_bytes);
+            mbar_expect_tx(bar, (uint32_t)(rows * KVB + (WITH_KI ? rows * KIB : 0) + (rr ? rows * 256 : 0)));
+            bulk_load(dst, kvb + t0 * kD, (uint32_t)(rows * KVB), bar);
+            if (WITH_KI) bulk_load(dst + kv_bytes, kib + t0 * kDI, (uint32_t)(rows * KIB), bar);
+            if (rr) bulk_load(dst + kv_bytes + ki_bytes, rope + t0 * 32, (uint32_t)(rows * 256), bar);
+        }
+    };
+    if (tid == 0)
+        for (int q = 0; q < kRunS - 1; ++q) issue(q);
+
+    // window weights: s_e[e][r] = exp(logit - max) of window row r of entry j0 + e (r < m: the
+    // previous block, set 1; r >= m: the own block, set 0); rows outside [0, L) weigh 0. Logits
+    // of the rows [(j0 - 1) m, jn m) first, by every thread: row i of that range (block
+    // j0 - 1 + i / m) is an own row of entry j0 + i / m - 1 and a previous row of the next one.
+    const int ne = jn - j0;
+    const int nrow = (ne + 1) * m;
+#pragma unroll 4
+    for (int i = tid; i < nrow; i += kRunThreads) {
+        const int64_t t = (int64_t)(j0 - 1) * m + i;
+        const bool in = t >= 0 && t < L;
+        const float z0 = in ? z[((int64_t)b * L + t) * 2] : -INFINITY;
+        const float z1 = in ? z[((int64_t)b * L + t) * 2 + 1] : -INFINITY;
+        const int e = i / m - 1, rb = i - (i / m) * m;  // e = -1: the halo block
+        if (e >= 0) s_e[e * 2 * m + m + rb] = z0;
+        if (e + 1 < ne) s_e[(e + 1) * 2 * m + rb] = z1;
+    }
+    __syncthreads();
+    for (int e = warp; e < ne; e += kRunWarps) {
+        float *we = s_e + e * 2 * m;
+        float mx = -INFINITY;
+        for (int r = lane; r < 2 * m; r += 32) mx = fmaxf(mx, we[r]);
+        mx = warp_max(mx);
+        float den = 0.0f;
+        for (int r = lane; r < 2 * m; r += 32) {
+            const float w = we[r] == -INFINITY ? 0.0f : expf(we[r] - mx);
+            we[r] = w;
+            den += w;
+        }
+        den = warp_sum(den);
+        if (lane == 0) s_inv[e] = 1.0f / den;
+    }
+    __syncthreads();
+
+    const int cl = lane % CPR, rl = lane / CPR, d0 = cl * V;
+    const int kc = lane & 15, kr = lane >> 4;
+    uint64_t acc[V / 2], nxt[V / 2], ak[2], nk[2];
+#pragma unroll
+    for (int k = 0; k < V / 2; ++k) acc[k] = nxt[k] = 0ull;
+    ak[0] = ak[1] = nk[0] = nk[1] = 0ull;
+    bool ok = true;
+    int q = 0;
+    for (; q < nq; ++q) {
+        if (tid == 0) issue(q + kRunS - 1);
+        const bool got = mbar_wait(smem_u32(&s_bar[q % kRunS]), (q / kRunS) & 1, kWaitNs, &g_abort);
+        if (!__syncthreads_and(got)) {
+            ok = false;
+            break;
+        }
+        const int beta = jb0 + q / ns, s0 = (q % ns) * kRunG;
+        const int64_t t0 = (int64_t)beta * m + s0;
+        const int rows = (int)min((int64_t)min(kRunG, m - s0), (int64_t)L - t0);
+        const uint8_t *slot = ring + (q % kRunS) * stage_bytes;
+        const float2 *slot_rope = reinterpret_cast<const float2 *>(slot + kv_bytes + ki_bytes);
+        const bool own = beta >= j0, has_next = beta + 1 < jn;
+        const float *e_own = s_e + (own ? beta - j0 : 0) * 2 * m + m + s0;
+        const float *e_nxt = s_e + (has_next ? beta + 1 - j0 : 0) * 2 * m + s0;
+        for (int r0 = warp * RPW; r0 < rows; r0 += RG) {  // (uniform over the warp)
+            const int r = r0 + rl;
+            const bool have = r < rows;
+            float x[V];
+            if (have) {
+                lds16(reinterpret_cast<const ActT *>(slot + r * KVB) + d0, x);
+            } else {
+#pragma unroll
+                for (int k = 0; k < V; ++k) x[k] = 0.0f;
+            }
+            const float wo = own && have ? e_own[r] : 0.0f, wn = has_next && have ? e_nxt[r] : 0.0f;
+            const uint64_t wo2 = f2_pack(wo, wo), wn2 = f2_pack(wn, wn);
+#pragma unroll
+            for (int k = 0; k < V / 2; ++k) {
+                const uint64_t x2 = f2_pack(x[2 * k], x[2 * k + 1]);
+                acc[k] = f2_fma(wo2, x2, acc[k]);
+                nxt[k] = f2_fma(wn2, x2, nxt[k]);
+            }
+            if (WITH_KVROPE && own) {  // the row back, rotated at its own position t0 + r
+                float y[V];
+#pragma unroll
+                for (int k = 0; k < V; ++k) y[k] = x[k];
+                if (rot) {
+                    float other[V];  // the partner chunk (dims 32 apart): lane ^ (32 / V)
+#pragma unroll
+                    for (int k = 0; k < V; ++k) other[k] = __shfl_xor_sync(0xffffffffu, x[k], 32 / V);
+                    if (have && d0 >= 64) {
+                        const float sg = d0 < 96 ? -1.0f : 1.0f;
+                        const int ip = (d0 - 64) & 31;
+                        const float4 *r4 = reinterpret_cast<const float4 *>(slot_rope + r * 32 + ip);
+#pragma unroll
+                        for (int k2 = 0; k2 < V / 2; ++k2) {
+                            const float4 cs = r4[k2];
+                            y[2 * k2] = fmaf(sg * other[2 * k2], cs.y, x[2 * k2] * cs.x);
+                            y[2 * k2 + 1] = fmaf(sg * other[2 * k2 + 1], cs.w, x[2 * k2 + 1] * cs.z);
+                        }
+                    }
+                }
+                if (have) store16(kvrb + (t0 + r) * kD + d0, y);
+            }
+        }
+        if (WITH_KI) {
+            for (int r = warp * 2 + kr; r < rows; r += kRunWarps * 2) {
+                const float4 x = *reinterpret_cast<const float4 *>(slot + kv_bytes + r * KIB + kc * 16);
+                const float wo = own ? e_own[r] : 0.0f, wn = has_next ? e_nxt[r] : 0.0f;
+                const uint64_t wo2 = f2_pack(wo, wo), wn2 = f2_pack(wn, wn);
+                const uint64_t x01 = f2_pack(x.x, x.y), x23 = f2_pack(x.z, x.w);
+                ak[0] = f2_fma(wo2, x01, ak[0]);
+                ak[1] = f2_fma(wo2, x23, ak[1]);
+                nk[0] = f2_fma(wn2, x01, nk[0]);
+                nk[1] = f2_fma(wn2, x23, nk[1]);
+            }
+        }
+        if (own && q % ns == ns - 1) {  // entry beta is complete: partial sums meet, warp 0 stores it
+            float a[V];
+#pragma unroll
+            for (int k = 0; k < V / 2; ++k) {
+                const float2 f = f2_unpack(acc[k]);
+                a[2 * k] = f.x;
+                a[2 * k + 1] = f.y;
+            }
+            if (RPW == 2) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) a[k] += __shfl_xor_sync(0xffffffffu, a[k], 16);
+            }
+            if (rl == 0) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) s_red[warp * kD + d0 + k] = a[k];
+            }
+            if (WITH_KI) {
+                const float2 f0 = f2_unpack(ak[0]), f1 = f2_unpack(ak[1]);
+                float qk[4] = {f0.x, f0.y, f1.x, f1.y};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) qk[k] += __shfl_xor_sync(0xffffffffu, qk[k], 16);
+                if (kr == 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) s_redk[warp * kDI + kc * 4 + k] = qk[k];
+                }
+            }
+            __syncthreads();
+            if (warp == 0) {
+                const float inv = s_inv[beta - j0];
+                float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float k0 = 0.0f, k1 = 0.0f;
+                for (int w = 0; w < kRunWarps; ++w) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) c[e] += s_red[w * kD + lane + 32 * e];
+                    if (WITH_KI) {
+                        k0 += s_redk[w * kDI + lane];
+                        k1 += s_redk[w * kDI + lane + 32];
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c[e] *= inv;
+                k0 *= inv;
+                k1 *= inv;
+                // the entry position (beta + 1) m - 1: the last row of the block
+                finish_entry<KV_T, IDX_T, WITH_KI>(c, k0, k1, beta, b, N,
+                                                   rot ? rope + ((int64_t)(beta + 1) * m - 1) * 32 : nullptr, c_data,
+                                                   c_rope, c_scale, ki_data, ki_scale, ki_e8);
+            }
+        }
+        if (q % ns == ns - 1) {  // the next block: entry beta + 1's sum so far, a new one after it
+#pragma unroll
+            for (int k = 0; k < V / 2; ++k) {
+                acc[k] = nxt[k];
+                nxt[k] = 0ull;
+            }
+            ak[0] = nk[0]; ak[1] = nk[1];
+            nk[0] = nk[1] = 0ull;
+        }
+        __syncthreads();  // slot q and the partial sums are free for reuse
+    }
+    if (!ok) {
+        if (tid == 0) {
+            set_timeout();
+            // copies still in flight land before the CTA leaves (bounded)
+            for (int f = q; f < min(nq, q + kRunS); ++f) mbar_wait(smem_u32(&s_bar[f % kRunS]), (f / kRunS) & 1, kDrainNs);
+        }
+        __syncthreads();
+    }
+}
+
 template <typename ActT, int KV_T, int IDX_T>
 static void launch_compress_t(const CompressArgs &a, cudaStream_t st) {
-    dim3 grid(a.N, a.B);
     const ActT *kv = reinterpret_cast<const ActT *>(a.kv);
     ActT *kvr = reinterpret_cast<ActT *>(a.kv_rope);
     const float2 *rope = reinterpret_cast<const float2 *>(a.rope_tab);
     auto *cr = reinterpret_cast<__nv_bfloat16 *>(a.c_rope);
-    // m <= 8: the streamed kernel; other small m: one warp per entry (the window's weights fit
-    // the lanes); else one CTA per entry
-    const bool stream = a.m <= kStreamMaxM;
-    const int ssmem = kStreamWarps * kStreamD *
-                      stream_slot_bytes(a.m, (int)sizeof(ActT), a.kI_raw != nullptr, a.d_rope == 64);
-    const dim3 sgrid((a.N + kStreamE * kStreamWarps - 1) / (kStreamE * kStreamWarps), a.B);
-    const bool per_warp = 2 * a.m <= 32;
-    const dim3 wgrid((a.N + 7) / 8, a.B);
-#define CSA_LAUNCH(KI, KVR)                                                                          \
-    if (stream) {                                                                                    \
-        auto kern = kv_compress_stream_kernel<ActT, KV_T, IDX_T, KI, KVR>;                           \
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem);              \
-        kern<<<sgrid, kStreamWarps * 32, ssmem, st>>>(kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, \
-                                                       a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope); \
-    } else if (per_warp)                                                                             \
-        kv_compress_warp_kernel<ActT, KV_T, IDX_T, KI, KVR><<<wgrid, 256, 0, st>>>(                  \
-            kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, \
-            a.d_rope);                                                                               \
-    else                                                                                             \
-        kv_compress_kernel<ActT, KV_T, IDX_T, KI, KVR><<<grid, 128, 0, st>>>(                        \
-            kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, \
-            a.d_rope)
+    // m <= 8: runs of entries per warp; larger m: runs of entries per CTA
+    const bool rot = a.d_rope == 64, with_ki = a.kI_raw != nullptr;
+    const int wsmem = kStreamWarps * kStreamD * stream_slot_bytes(a.m, (int)sizeof(ActT), with_ki, rot);
+    const dim3 wgrid((a.N + kStreamE * kStreamWarps - 1) / (kStreamE * kStreamWarps), a.B);
+    const int csmem = run_smem_bytes(a.m, (int)sizeof(ActT), with_ki, rot);
+    const dim3 cgrid((a.N + kRunE - 1) / kRunE, a.B);
+#define CSA_LAUNCH(KI, KVR)                                                                                   \
+    do {                                                                                                      \
+    if (a.m <= kStreamMaxM) {                                                                                 \
+        auto kern = kv_compress_stream_kernel<ActT, KV_T, IDX_T, KI, KVR>;                                    \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem);                       \
+        kern<<<wgrid, kStreamWarps * 32, wsmem, st>>>(kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, \
+                                                       a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope);      \
+    } else {                                                                                                  \
+        auto kern = kv_compress_run_kernel<ActT, KV_T, IDX_T, KI, KVR>;                                       \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem);                       \
+        kern<<<cgrid, kRunThreads, csmem, st>>>(kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data,   \
+                                                a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope);             \
+    }                                                                                                         \
+    } while (0)
     if (a.kI_raw && a.kv_rope) CSA_LAUNCH(true, true);
     else if (a.kI_raw) CSA_LAUNCH(true, false);
     else if (a.kv_rope) CSA_LAUNCH(false, true);

@@ -73,6 +73,11 @@ def test_quant_fp8_rows_bit_exact(lib):
     dict(L=3, m=4, act="f32", kv="f32", idx="f32"),
     dict(L=2999, m=4, act="bf16", kv="nvfp4", idx="mxfp4"),
     dict(L=700, m=128, act="bf16", kv="nvfp4", idx=None),
+    # the per-warp runs at their largest m, and per-CTA runs with one and with two stages per block
+    dict(L=1030, m=8, act="bf16", kv="mixed", idx="fp8"),
+    dict(L=1000, m=16, act="bf16", kv="bf16", idx="fp8"),
+    dict(L=777, m=48, act="f32", kv="f32", idx="f32"),
+    dict(L=1301, m=128, act="bf16", kv="mixed", idx="fp8"),
 ])
 def test_kv_compress(lib, case):
     wl = synth.Workload("t", "csa", B=2, L=case["L"], H=8, seed=11, m=case["m"], q_t=case["act"], c_t=case["kv"],
