@@ -59,8 +59,52 @@ __global__ void quant_rows_kernel(const float *__restrict__ x, int64_t rows, int
     }
 }
 
+// Rows of 64 (the indexer's query rows): a half-warp per row, each lane one 16-byte chunk of four
+// values, two rows per warp instruction and kQ64Unroll row pairs per warp in flight; the same
+// arithmetic as quant_rows_kernel (float scale amax / 448, float division per element).
+constexpr int kQ64Unroll = 4;
+__global__ void __launch_bounds__(256) quant_rows64_kernel(const float4 *__restrict__ x, int64_t rows,
+                                                           uint32_t *__restrict__ codes, float *__restrict__ scales) {
+    const int lane = threadIdx.x & 31, c = lane & 15, h = lane >> 4;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t gw = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (int64_t r0 = gw * 2 * kQ64Unroll; r0 < rows; r0 += warps * 2 * kQ64Unroll) {
+        float4 v[kQ64Unroll];
+#pragma unroll
+        for (int u = 0; u < kQ64Unroll; ++u) {
+            const int64_t r = r0 + 2 * u + h;
+            v[u] = r < rows ? __ldcs(x + r * 16 + c) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < kQ64Unroll; ++u) {
+            const int64_t r = r0 + 2 * u + h;
+            float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float scale = __fdiv_rn(amax, 448.0f);
+            uint32_t w = 0;
+            if (scale > 0.0f)
+                w = (uint32_t)f32_to_e4m3(__fdiv_rn(v[u].x, scale)) | ((uint32_t)f32_to_e4m3(__fdiv_rn(v[u].y, scale)) << 8) |
+                    ((uint32_t)f32_to_e4m3(__fdiv_rn(v[u].z, scale)) << 16) |
+                    ((uint32_t)f32_to_e4m3(__fdiv_rn(v[u].w, scale)) << 24);
+            if (r < rows) {
+                codes[r * 16 + c] = w;
+                if (c == 0) scales[r] = scale;
+            }
+        }
+    }
+}
+
 void launch_quant_rows(const float *x, int64_t rows, int cols, uint8_t *codes, float *scales,
                        cudaStream_t st) {
+    if (cols == 64 && reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(codes) % 4 == 0) {
+        int64_t blocks = (rows + 8 * 2 * kQ64Unroll - 1) / (8 * 2 * kQ64Unroll);
+        if (blocks > 148 * 8) blocks = 148 * 8;
+        quant_rows64_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const float4 *>(x), rows,
+                                                         reinterpret_cast<uint32_t *>(codes), scales);
+        count_launches(1);
+        return;
+    }
     int64_t blocks = (rows + 7) / 8;
     if (blocks > 148 * 32) blocks = 148 * 32;
     if (blocks < 1) blocks = 1;

@@ -406,22 +406,27 @@ __global__ void __launch_bounds__(tk::kThreads) decode_collect_kernel(DecSelArgs
             for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
         return;
     }
-    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = __ldcg(a.hist + (int64_t)r * kBins + i);
-    __syncthreads();
-    int bstar, above;
-    find_threshold_bin(hist, kBins, k, s_tmp, s_res, &bstar, &above);
     const int per = (n + a.slices - 1) / a.slices;
     const int i0 = g * per, i1 = min(n, i0 + per);
     const float *S = a.S + (int64_t)r * a.ldS;
-    // the slice's keys stay in registers: one pass counts (per thread, then a block scan, then
-    // one atomic per list per CTA), the second writes at the positions found
+    // the slice's keys stay in registers (loaded first, so that their reads overlap the
+    // histogram's): one pass counts (per thread, then a block scan, then one atomic per list per
+    // CTA), the second writes at the positions found
     constexpr int kPer = (kDecMaxSlice + kThreads - 1) / kThreads;
     uint32_t key[kPer];
-    int ngt = 0, neq = 0;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
         const int i = i0 + u * kThreads + (int)threadIdx.x;
         key[u] = i < i1 ? key_of(__ldcg(S + i)) : 0u;
+    }
+    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = __ldcg(a.hist + (int64_t)r * kBins + i);
+    __syncthreads();
+    int bstar, above;
+    find_threshold_bin(hist, kBins, k, s_tmp, s_res, &bstar, &above);
+    int ngt = 0, neq = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = i0 + u * kThreads + (int)threadIdx.x;
         const int bin = i < i1 ? (int)(key[u] >> kBinShift) : -1;
         ngt += bin > bstar;
         neq += bin == bstar;

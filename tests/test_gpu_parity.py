@@ -51,13 +51,16 @@ def test_rope_table(lib):
             assert abs(tab[pp, i, 0] - c) <= 6e-8 and abs(tab[pp, i, 1] - s) <= 6e-8, (pp, i)
 
 
-def test_quant_fp8_rows_bit_exact(lib):
+@pytest.mark.parametrize("rows,cols", [(2000, 64), (2003, 64), (37, 48)])
+def test_quant_fp8_rows_bit_exact(lib, rows, cols):
+    # rows of 64 take the half-warp-per-row kernel (a ragged last group at 2003), others the
+    # warp-per-row one
     g = torch.Generator().manual_seed(5)
-    x = torch.randn((2000, 64), generator=g) * torch.exp(torch.randn((2000, 1), generator=g) * 3)
+    x = torch.randn((rows, cols), generator=g) * torch.exp(torch.randn((rows, 1), generator=g) * 3)
     x[7] = 0.0
     x[8, 3] = 1e30
-    codes = torch.empty((2000, 64), dtype=torch.uint8, device=DEV)
-    scales = torch.empty(2000, dtype=torch.float32, device=DEV)
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=DEV)
+    scales = torch.empty(rows, dtype=torch.float32, device=DEV)
     lib.csa_quant_fp8_rows(x.to(DEV), codes, scales)
     oc, osc = oracle.quant_rows_fp8(x.numpy())
     np.testing.assert_array_equal(scales.cpu().numpy(), osc)
