@@ -191,7 +191,7 @@ __device__ __forceinline__ void finish_entry(float (&c)[4], float k0, float k1, 
     }
 }
 
-// kv_compress for m <= 8, streamed. One warp walks a run of kStreamE consecutive entries
+// kv_compress for m <= 8, streamed. One warp walks a run of up to kStreamE consecutive entries
 // j0 .. j0 + E - 1 block by block (block beta = rows [beta m, (beta + 1) m)), from block j0 - 1
 // (the run's halo: it only feeds entry j0) to block j0 + E - 1. Each block's KV rows,
 // indexer-key rows and RoPE-table rows (contiguous in memory) are copied into the warp's ring of
@@ -202,7 +202,7 @@ __device__ __forceinline__ void finish_entry(float (&c)[4], float k0, float k1, 
 // block, set 1). The warp keeps the two running sums; after block beta, entry beta is complete
 // and is stored by finish_entry. The window weights of the run's entries are computed first,
 // lane i for entry j0 + i.
-constexpr int kStreamE = 16;     // entries per warp
+constexpr int kStreamE = 16;     // entries per warp at most (ew: the launch's run length)
 constexpr int kStreamWarps = 4;  // warps per CTA
 constexpr int kStreamD = 3;      // ring slots per warp (blocks in flight: kStreamD - 1)
 constexpr int kStreamMaxM = 8;
@@ -228,13 +228,13 @@ __host__ __device__ __forceinline__ int stream_slot_bytes(int m, int act_bytes, 
 }
 
 template <typename ActT, int KV_T, int IDX_T, bool WITH_KI, bool WITH_KVROPE>
-__global__ void __launch_bounds__(kStreamWarps * 32)
+__global__ void __launch_bounds__(kStreamWarps * 32, 5)
 kv_compress_stream_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
                           const float *__restrict__ kI_raw, const float2 *__restrict__ rope,
                           void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
                           float *__restrict__ c_scale, void *__restrict__ ki_data,
                           float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope,
-                          int L, int m, int N, int d_rope) {
+                          int L, int m, int N, int d_rope, int ew) {
     using namespace umma;
     constexpr int V = 16 / (int)sizeof(ActT);    // dims per 16-byte chunk
     constexpr int CPR = kD / V;                  // chunks per KV row
@@ -248,9 +248,9 @@ kv_compress_stream_kernel(const ActT *__restrict__ kv, const float *__restrict__
     __shared__ __align__(8) uint64_t s_bar[kStreamWarps][kStreamD];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
-    const int j0 = (blockIdx.x * kStreamWarps + warp) * kStreamE;
+    const int j0 = (blockIdx.x * kStreamWarps + warp) * ew;
     if (j0 >= N) return;  // (the warp leaves as a whole; nothing below is CTA-wide)
-    const int jn = min(N, j0 + kStreamE);
+    const int jn = min(N, j0 + ew);
     const bool rot = d_rope == 64;
     // slot: KV rows [m][KVB], indexer-key rows [m][KIB], RoPE rows [m][32 float2]
     const int kv_bytes = m * KVB, ki_bytes = WITH_KI ? m * KIB : 0;
@@ -288,7 +288,7 @@ kv_compress_stream_kernel(const ActT *__restrict__ kv, const float *__restrict__
 
     // window weights of entry j0 + lane: s_e[.][r] = exp(logit - max) for window row r (r < m:
     // the previous block, set 1; r >= m: the own block, set 0); rows outside [0, L) weigh 0
-    if (lane < kStreamE) {
+    if (lane < ew) {
         const int j = j0 + lane;
         float lg[2 * kStreamMaxM];
         float mx = -INFINITY;
@@ -457,7 +457,7 @@ kv_compress_stream_kernel(const ActT *__restrict__ kv, const float *__restrict__
     }
 }
 
-// kv_compress for m > 8, streamed by CTAs. A CTA of kRunThreads walks a run of kRunE
+// kv_compress for m > 8, streamed by CTAs. A CTA of kRunThreads walks a run of up to kRunE
 // consecutive entries j0 .. j0 + E - 1 over blocks j0 - 1 .. j0 + E - 1 (block beta = rows
 // [beta m, (beta + 1) m); block j0 - 1 is the run's halo and only feeds entry j0), in stages of
 // kRunG rows: thread 0 bulk-copies a stage's KV rows, indexer-key rows and (outside the halo)
@@ -469,7 +469,7 @@ kv_compress_stream_kernel(const ActT *__restrict__ kv, const float *__restrict__
 // window weights of the run's entries are computed first, one warp per entry.
 constexpr int kRunThreads = 256;
 constexpr int kRunWarps = kRunThreads / 32;
-constexpr int kRunE = 4;   // entries per CTA
+constexpr int kRunE = 4;   // entries per CTA at most (ec: the launch's run length)
 constexpr int kRunG = 64;  // rows per stage
 constexpr int kRunS = 3;   // ring slots (stages in flight: kRunS - 1)
 
@@ -488,7 +488,7 @@ kv_compress_run_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
                        void *__restrict__ c_data, __nv_bfloat16 *__restrict__ c_rope,
                        float *__restrict__ c_scale, void *__restrict__ ki_data,
                        float *__restrict__ ki_scale, uint8_t *__restrict__ ki_e8, ActT *__restrict__ kv_rope,
-                       int L, int m, int N, int d_rope) {
+                       int L, int m, int N, int d_rope, int ec) {
     using namespace umma;
     constexpr int V = 16 / (int)sizeof(ActT);    // dims per 16-byte chunk
     constexpr int CPR = kD / V;                  // chunks per KV row
@@ -500,8 +500,8 @@ kv_compress_run_kernel(const ActT *__restrict__ kv, const float *__restrict__ z,
     __shared__ __align__(8) uint64_t s_bar[kRunS];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.y;
-    const int j0 = blockIdx.x * kRunE;
-    const int jn = min(N, j0 + kRunE);
+    const int j0 = blockIdx.x * ec;
+    const int jn = min(N, j0 + ec);
     const bool rot = d_rope == 64;
     const int kv_bytes = kRunG * KVB, ki_bytes = WITH_KI ? kRunG * KIB : 0;
     const int stage_bytes = run_stage_bytes((int)sizeof(ActT), WITH_KI, rot);
@@ -734,21 +734,25 @@ static void launch_compress_t(const CompressArgs &a, cudaStream_t st) {
     // m <= 8: runs of entries per warp; larger m: runs of entries per CTA
     const bool rot = a.d_rope == 64, with_ki = a.kI_raw != nullptr;
     const int wsmem = kStreamWarps * kStreamD * stream_slot_bytes(a.m, (int)sizeof(ActT), with_ki, rot);
-    const dim3 wgrid((a.N + kStreamE * kStreamWarps - 1) / (kStreamE * kStreamWarps), a.B);
+    // run lengths: the longest (fewest halo blocks) that still gives every SM a few CTAs
+    const int64_t units = (int64_t)a.N * a.B;
+    const int ew = (int)std::max<int64_t>(1, std::min<int64_t>(kStreamE, units / (4 * kStreamWarps * 148)));
+    const int ec = (int)std::max<int64_t>(1, std::min<int64_t>(kRunE, units / (2 * 148)));
+    const dim3 wgrid((a.N + ew * kStreamWarps - 1) / (ew * kStreamWarps), a.B);
     const int csmem = run_smem_bytes(a.m, (int)sizeof(ActT), with_ki, rot);
-    const dim3 cgrid((a.N + kRunE - 1) / kRunE, a.B);
+    const dim3 cgrid((a.N + ec - 1) / ec, a.B);
 #define CSA_LAUNCH(KI, KVR)                                                                                   \
     do {                                                                                                      \
     if (a.m <= kStreamMaxM) {                                                                                 \
         auto kern = kv_compress_stream_kernel<ActT, KV_T, IDX_T, KI, KVR>;                                    \
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem);                       \
         kern<<<wgrid, kStreamWarps * 32, wsmem, st>>>(kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data, \
-                                                       a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope);      \
+                                                       a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope, ew);  \
     } else {                                                                                                  \
         auto kern = kv_compress_run_kernel<ActT, KV_T, IDX_T, KI, KVR>;                                       \
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem);                       \
         kern<<<cgrid, kRunThreads, csmem, st>>>(kv, a.z, a.kI_raw, rope, a.c_data, cr, a.c_scale, a.ki_data,   \
-                                                a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope);             \
+                                                a.ki_scale, a.ki_e8, kvr, a.L, a.m, a.N, a.d_rope, ec);         \
     }                                                                                                         \
     } while (0)
     if (a.kI_raw && a.kv_rope) CSA_LAUNCH(true, true);
