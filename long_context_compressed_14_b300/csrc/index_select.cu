@@ -70,7 +70,7 @@ constexpr int kSmemBytes = kKOff + kNK * kTileBytes + 1024;
 constexpr uint32_t kTmemCols = kWG * kN;  // 512
 constexpr int kSample = 0, kFilter = 1;
 constexpr int kFbCtas = 296;              // fallback CTAs (each owns one score-row slot)
-constexpr size_t kBudget = (size_t)3 << 30;  // workspace bytes per chunk of rows (upper bound)
+constexpr size_t kBudget = (size_t)16 << 30;  // workspace bytes per chunk of rows (upper bound)
 }  // namespace isel
 
 struct IselTcParams {
