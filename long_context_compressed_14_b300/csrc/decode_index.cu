@@ -9,7 +9,7 @@
 // Score as in prefill: s(j) = sk_j * sum_h (w[h] * sq[h]) * ReLU(qcode[h] . kcode_j), for the
 // entries j visible to the new token at p = ctx - 1 ((j+1)m - 1 <= p). The scan is bound by
 // the bytes of the cache (64 code bytes + 4 scale bytes per entry), so the work is split into
-// items of 128 entries of one sequence, dealt in contiguous blocks to two CTAs per SM:
+// items of 128 entries of one sequence, dealt in contiguous blocks to three CTAs per SM:
 //   MMA  D[128 entries][16] = KI_tile (128 x 64 E4M3) times qI^T (16 rows: the H_I heads of the
 //        sequence's query, the rest of the 16 rows is ignored), K = 64 as two kind::f8f6f4 MMAs;
 //   TMA  the entry tile and the query rows of the item into a ring of stages, with the entries'
@@ -40,7 +40,7 @@ constexpr int kMmaWarp = 5;
 constexpr int kThreads = 192;
 constexpr int kJ = 128;                   // entries per item (M)
 constexpr int kN = 16;                    // query rows (N)
-constexpr int kNS = 6;                    // ring stages (two CTAs fit one SM)
+constexpr int kNS = 4;                    // ring stages (three CTAs fit one SM)
 constexpr int kKBytes = kJ * 64;          // 8 KB
 constexpr int kQBytes = kN * 64;          // 1 KB
 constexpr int kSBytes = kJ * 4;           // the entries' FP8 scales
@@ -70,7 +70,7 @@ __device__ __forceinline__ uint64_t dix_desc_sw64(uint32_t addr) {
 }
 
 template <int HI>
-__global__ void __launch_bounds__(dix::kThreads, 2) decode_index_tc_kernel(const __grid_constant__ DixParams P) {
+__global__ void __launch_bounds__(dix::kThreads, 3) decode_index_tc_kernel(const __grid_constant__ DixParams P) {
     using namespace dix;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -288,7 +288,7 @@ bool launch_decode_index_tc(const IndexArgs &a, uint32_t *hist, cudaStream_t st)
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int items = a.B * P.tiles;
-    const int grid = items < 2 * sms ? items : 2 * sms;  // two CTAs (pipelines) per SM
+    const int grid = items < 3 * sms ? items : 3 * sms;  // three CTAs (pipelines) per SM
     auto go = [&](auto kern) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         launch_pdl(kern, grid, kThreads, kSmemBytes, st, P);
