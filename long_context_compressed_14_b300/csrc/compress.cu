@@ -197,11 +197,10 @@ __device__ __forceinline__ void finish_entry(float (&c)[4], float k0, float k1, 
 // indexer-key rows and RoPE-table rows (contiguous in memory) are copied into the warp's ring of
 // shared-memory slots kStreamD - 1 blocks ahead of their use by three bulk copies that complete
 // on the slot's mbarrier, so every raw row is read from HBM once (plus one halo block per run)
-// with several blocks in flight per warp. A block
-// feeds two entries: entry beta (its own block, logits of set 0) and entry beta + 1 (its previous
-// block, set 1). The warp keeps the two running sums; after block beta, entry beta is complete
-// and is stored by finish_entry. The window weights of the run's entries are computed first,
-// lane i for entry j0 + i.
+// with several blocks in flight per warp. A block feeds two entries: entry beta (its own block,
+// logits of set 0) and entry beta + 1 (its previous block, set 1). The warp keeps the two
+// running sums; after block beta, entry beta is complete and is stored by finish_entry. The
+// window weights of the run's entries are computed first, lane i for entry j0 + i.
 constexpr int kStreamE = 16;     // entries per warp at most (ew: the launch's run length)
 constexpr int kStreamWarps = 4;  // warps per CTA
 constexpr int kStreamD = 3;      // ring slots per warp (blocks in flight: kStreamD - 1)
