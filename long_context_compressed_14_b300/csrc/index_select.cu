@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(tk::kThreads) sample_thr_kernel(IselRowArgs a)
 constexpr int kSelPer = kIselCap / tk::kThreads;  // candidates per thread (registers): one per segment
 static_assert(kSelPer == 16 && kIselSeg == tk::kThreads, "thread t holds slot t of every segment");
 
-__global__ void __launch_bounds__(tk::kThreads, 4) cand_select_kernel(IselRowArgs a) {
+__global__ void __launch_bounds__(tk::kThreads, 5) cand_select_kernel(IselRowArgs a) {
     using namespace tk;
     extern __shared__ uint32_t dyn[];
     uint32_t *hist = dyn;                 // [kBins]
