@@ -408,7 +408,7 @@ def time_workload(lib, wl, args, graph=False, e2e=False, world=1, rank=0, local_
         for fn in stage_sets[1]:  # the second set's first run (warm-up) outside the timed region
             fn()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        nsteps = max(1, min(args.steps, 5))
+        nsteps = max(1, min(args.steps, 10))
         torch.cuda.synchronize()
         e0.record(stream)
         for s in (s_in, s_comp, s_out):
