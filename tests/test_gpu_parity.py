@@ -255,8 +255,10 @@ def test_index_topk_heavy_ties(lib):
     assert lib.csa_device_status() == 0
 
 
-def test_index_topk_fp8(lib):
-    L, m, H_I, k = 4096, 4, 8, 512
+@pytest.mark.parametrize("H_I", [8, 16])
+def test_index_topk_fp8(lib, H_I):
+    # H_I = 16: a query tile holds 8 tokens of 16 heads (one token per 16-column TMEM chunk)
+    L, m, k = 4096, 4, 512
     g = torch.Generator().manual_seed(9)
     N = L // m
     qI = torch.randn((1, L, H_I, 64), generator=g)
@@ -296,11 +298,12 @@ def _fp8_index_case(lib, L, m, H_I, k, qI, KI, w):
     return out.cpu().numpy()[0], oracle.dequant_fp8(ok_, osk)
 
 
-def test_index_topk_fp8_sampled_threshold(lib):
+@pytest.mark.parametrize("H_I", [8, 16])
+def test_index_topk_fp8_sampled_threshold(lib, H_I):
     # Rows past 4 x 4096 see more than 4096 entries: their threshold comes from the sample of
     # every 16th entry tile and only candidates above it are kept. Rows on both sides of that
     # boundary, random rows and the last rows, by score against the oracle.
-    L, m, H_I, k = 40000, 4, 8, 512
+    L, m, k = 40000, 4, 512
     g = torch.Generator().manual_seed(41)
     N = L // m
     qI = torch.randn((1, L, H_I, 64), generator=g)
@@ -546,6 +549,22 @@ def test_decode(lib, csa, c_t, idx_t, w_t):
     torch.cuda.synchronize()
     assert lib.csa_device_status() == 0
     _check_decode(wl, inp, layer, out, csa, range(4))
+
+
+@pytest.mark.parametrize("H_I,idx_t", [(4, "fp8"), (16, "fp8"), (16, "mxfp4")])
+def test_decode_indexer_heads(lib, H_I, idx_t):
+    # the decode scans at 4 and 16 indexer heads (the other cases run 8)
+    wl = synth.WORKLOADS["decode_b16_ctx131072"].replace(B=4, L=8192, topk=256, H_I=H_I, idx_t=idx_t)
+    from long_context_compressed_14_b300.pipeline import DecodeLayer
+    inp = synth.decode_layer(wl, csa=True)
+    inp["ctx"] = torch.tensor([8192, 3, 4097, 6001], dtype=torch.int32)
+    layer = DecodeLayer.create(wl, csa=True)
+    d = _dev(inp)
+    layer.load_caches(d)
+    out = layer.run(d)
+    torch.cuda.synchronize()
+    assert lib.csa_device_status() == 0
+    _check_decode(wl, inp, layer, out, True, range(4))
 
 
 def test_decode_heavy_ties(lib):
