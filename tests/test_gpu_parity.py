@@ -416,7 +416,8 @@ def test_csa_prefill_f32_pipeline(lib):
     (1, 70, 64, "bf16", False), (1, 515, 128 // 2, "mixed", True),
 ])
 def test_hca_prefill_bf16(lib, B, L, H, c_t, sink):
-    # BF16 HCA prefill runs the tensor-core kernel (H in {16, 32, 64})
+    # BF16 HCA prefill runs the tensor-core kernel (H in {16, 32, 64}: 8, 4 or 2 tokens per
+    # 128-row item; the C ABI takes at most 64 heads)
     wl = synth.WORKLOADS["hca_bf16_L16384"].replace(B=B, L=L, H=H, c_t=c_t)
     from long_context_compressed_14_b300.pipeline import PrefillLayer
     inp = synth.prefill_layer(wl, csa=False)
