@@ -446,8 +446,11 @@ def test_hca_prefill_full_size_sampled(lib):
     assert rel_l2(np64(out[0][rows]), res["o"]) <= 2e-2
 
 
-@pytest.mark.parametrize("B,L,k,c_t", [(2, 3000, 512, "bf16"), (1, 1030, 64, "mixed"), (1, 5, 512, "bf16")])
+@pytest.mark.parametrize("B,L,k,c_t", [(2, 3000, 512, "bf16"), (1, 1030, 64, "mixed"), (1, 5, 512, "bf16"),
+                                       (1, 9000, 2048, "bf16")])
 def test_csa_prefill_bf16_fp8(lib, B, L, k, c_t):
+    # top-2048 (the largest) leaves room for three key-tile buffers instead of four in shared
+    # memory: the kernel's other instance
     wl = synth.WORKLOADS["csa_bf16_4x32768"].replace(B=B, L=L, topk=k, c_t=c_t)
     from long_context_compressed_14_b300.pipeline import PrefillLayer
     inp = synth.prefill_layer(wl, csa=True)
