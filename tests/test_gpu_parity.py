@@ -85,6 +85,9 @@ def test_quant_fp8_rows_bit_exact(lib, rows, cols):
     dict(L=1000, m=16, act="bf16", kv="bf16", idx="fp8"),
     dict(L=777, m=48, act="f32", kv="f32", idx="f32"),
     dict(L=1301, m=128, act="bf16", kv="mixed", idx="fp8"),
+    # without the rotated raw rows (kv_rope = NULL)
+    dict(L=1001, m=4, act="bf16", kv="bf16", idx="fp8", kvr=False),
+    dict(L=517, m=128, act="bf16", kv="mixed", idx=None, kvr=False),
 ])
 def test_kv_compress(lib, case):
     wl = synth.Workload("t", "csa", B=2, L=case["L"], H=8, seed=11, m=case["m"], q_t=case["act"], c_t=case["kv"],
@@ -96,7 +99,7 @@ def test_kv_compress(lib, case):
     C = lib.alloc_entries(p)
     ncap = math.ceil(wl.L / wl.m)
     KI = lib.alloc_index_rows(p, (2, ncap)) if with_ki else None
-    kvr = torch.empty((2, wl.L, 128), dtype=lib.torch_dtype(case["act"]), device=DEV)
+    kvr = torch.empty((2, wl.L, 128), dtype=lib.torch_dtype(case["act"]), device=DEV) if case.get("kvr", True) else None
     d = _dev(inp)
     lib.kv_compress(p, d["kv"], d["z"], d["kI_raw"] if with_ki else None, rope, C, KI, kvr)
     torch.cuda.synchronize()
@@ -143,8 +146,9 @@ def test_kv_compress(lib, case):
                 assert rel_l2(gk, comp["KI"]) < 1e-2
                 np.testing.assert_allclose(KI[1][b].cpu().numpy(), comp["KI_raw"][1], rtol=1e-5)
         # raw rows after RoPE
-        tol = 3e-6 if case["act"] == "f32" else 2 ** -7  # one bf16 ulp
-        np.testing.assert_allclose(np64(kvr[b]), comp["kv_rope"], rtol=tol, atol=1e-6)
+        if kvr is not None:
+            tol = 3e-6 if case["act"] == "f32" else 2 ** -7  # one bf16 ulp
+            np.testing.assert_allclose(np64(kvr[b]), comp["kv_rope"], rtol=tol, atol=1e-6)
 
 
 # ---------------------------------------------------------------------------------------
